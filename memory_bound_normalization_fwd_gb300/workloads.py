@@ -1,0 +1,111 @@
+"""Seeded synthetic inputs for the RMSNorm forward.
+
+This module draws random numbers and nothing else: it holds none of the
+normalisation's arithmetic, so both the CUDA path's tests/benchmark and the
+fp64 oracle take their inputs from here.
+
+Recipe (every workload): one ``torch.Generator('cpu')`` seeded with the
+workload's seed; x is drawn first, in blocks of rows (block = max(1, 2**22 // N)
+rows, each block drawn in full before the next), then w. Values are drawn in
+fp32 and rounded to the activation dtype by torch's ``.to()`` (round to nearest
+even). Arrays come back as raw uint16 bit patterns.
+
+The five named workloads reproduce the shapes and distributions the method is
+benchmarked on: the 16384x512 bf16 shape reported for the persistent cuTile
+kernel (TileGym issue #169), plus a small case, a non-power-of-two hidden size
+with Gemma-style weights (offset 1), a large hidden size with heavy-tailed
+activations, and a large fp16 case whose sum of squares exceeds the fp16 range.
+``N(mu, v)`` below means variance ``v``.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+DTYPES = ("bf16", "fp16")
+_TORCH = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    dtype: str = "bf16"
+    x_std: float = 1.0            # x ~ N(0, x_std^2)
+    outlier_p: float = 0.0        # heavy tail: with probability p, x ~ N(0, outlier_std^2)
+    outlier_std: float = 100.0
+    w_kind: str = "uniform"       # "uniform": U(w_a, w_b); "normal": N(w_a, w_b)
+    w_a: float = 0.5
+    w_b: float = 1.5
+    eps: float = 1e-6
+    offset: float = 0.0
+    seed: int = 0
+    note: str = field(default="", compare=False)
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Bytes one forward must move: x read, y written, w read, rstd written."""
+        return 2 * self.M * self.N + 2 * self.M * self.N + 2 * self.N + 4 * self.M
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("rmsnorm_2048x512_bf16", 2048, 512, note="small case"),
+        Workload("rmsnorm_16384x512_bf16", 16384, 512,
+                 note="the shape of the persistent cuTile kernel report"),
+        Workload("rmsnorm_32768x1000_bf16_gemma", 32768, 1000, w_kind="normal", w_a=0.0,
+                 w_b=0.1, offset=1.0, note="non-power-of-two N, masked tail, Gemma offset"),
+        Workload("rmsnorm_16384x8192_bf16_heavytail", 16384, 8192, outlier_p=0.01,
+                 outlier_std=100.0, eps=1e-5, note="99% N(0,1) + 1% N(0,100^2)"),
+        Workload("rmsnorm_131072x4096_fp16", 131072, 4096, dtype="fp16", x_std=64.0,
+                 note="sum of squares far beyond the fp16 range"),
+    ]
+}
+BENCH_WORKLOAD = "rmsnorm_16384x512_bf16"
+
+
+def _bits(t: torch.Tensor, dtype: str) -> np.ndarray:
+    return t.to(_TORCH[dtype]).view(torch.int16).numpy().view(np.uint16)
+
+
+def generate(wl: Workload) -> tuple[np.ndarray, np.ndarray]:
+    """Return ``(x_bits [M, N] uint16, w_bits [N] uint16)`` for the workload."""
+    M = wl.M
+    g = torch.Generator(device="cpu")
+    g.manual_seed(wl.seed)
+    x = np.empty((M, wl.N), dtype=np.uint16)
+    block = max(1, (1 << 22) // wl.N)
+    for r0 in range(0, M, block):
+        r1 = min(M, r0 + block)
+        t = torch.randn((r1 - r0, wl.N), generator=g, dtype=torch.float32) * wl.x_std
+        if wl.outlier_p > 0.0:
+            mask = torch.rand((r1 - r0, wl.N), generator=g) < wl.outlier_p
+            out = torch.randn((r1 - r0, wl.N), generator=g, dtype=torch.float32) * wl.outlier_std
+            t = torch.where(mask, out, t)
+        x[r0:r1] = _bits(t, wl.dtype)
+    if wl.w_kind == "uniform":
+        w = wl.w_a + (wl.w_b - wl.w_a) * torch.rand(wl.N, generator=g, dtype=torch.float32)
+    elif wl.w_kind == "normal":
+        w = wl.w_a + (wl.w_b ** 0.5) * torch.randn(wl.N, generator=g, dtype=torch.float32)
+    else:
+        raise ValueError(wl.w_kind)
+    return x, _bits(w, wl.dtype)
+
+
+def custom(M: int, N: int, dtype: str = "bf16", seed: int = 0, **kw) -> Workload:
+    """An ad-hoc workload (parity sweeps over small and ragged shapes)."""
+    return Workload(f"custom_{M}x{N}_{dtype}_s{seed}", M, N, dtype=dtype, seed=seed, **kw)
+
+
+def to_torch(bits: np.ndarray, dtype: str) -> torch.Tensor:
+    """uint16 bit patterns -> a CPU torch tensor of the activation dtype (no copy of values)."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(_TORCH[dtype])
+
+
+def from_torch(t: torch.Tensor) -> np.ndarray:
+    """A bf16/fp16 torch tensor (any device) -> uint16 bit patterns on the host."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
