@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""RMSNorm forward benchmark: achieved HBM GB/s on one GB300 (and per rank
+under torchrun), with the roofline fraction, the end-to-end figure through the
+C ABI from host buffers, SM clocks during the timed region, and the fp64 CPU
+oracle timed on the host cores as a reported baseline.
+
+A step is one call of the C ABI's rmsnorm_fwd over one [M, N] batch (the
+whole forward: row load, sum of squares, rsqrt, rstd store, scale, store).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle as the reference arm
+
+Algorithmic bytes per step: 2*M*N (x read) + 2*M*N (y written) + 2*N (w read)
++ 4*M (rstd written); GB/s = bytes / seconds / 1e9 (the GB/s formula of the
+skillmd "RMSNorm Kernel Optimization" page, with the weight and rstd added).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "RMSNorm fwd achieved HBM GB/s and % of GB300 peak (1 GPU), per M×N×dtype"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["common.cuh", "launch.h", "kernels_warp.cu", "kernels_cta.cu",
+                  "kernels_tma.cu", "kernels_generic.cu", "api.cu"]
+
+
+# ---------------------------------------------------------------- host-side helpers
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300000)
+    p.add_argument("--warmup", type=int, default=2000)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=None, help="named workload (default: the 16384x512 bf16 one)")
+    p.add_argument("--e2e-steps", type=int, default=400)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--variant", default="auto", help="force a kernel variant (ablation)")
+    p.add_argument("--lanes-per-row", type=int, default=0)
+    p.add_argument("--stages", type=int, default=0)
+    p.add_argument("--rows-per-stage", type=int, default=0)
+    p.add_argument("--max-ctas", type=int, default=0)
+    return p.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float) -> float:
+    """Max of a host float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def whole_job_gbs(bytes_per_rank_step: int, steps: int, world: int, max_seconds: float) -> float:
+    """Weak scaling: every rank moves its own batch each step; the job's time is the slowest rank's."""
+    return bytes_per_rank_step * steps * world / max_seconds / 1e9
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "memory_bound_normalization_fwd_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (its `kernel_hash` line matches), else None."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_hash:\s*`?([0-9a-f]+)", text)
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*`?([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                [exe, f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[3], parts[4:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        # Samples under load: SM clock above idle; the first/last samples bracket the region.
+        sm = [r[0] for r in rows]
+        busy = [r for r in rows if r[0] >= 0.5 * max(sm)] or rows
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in busy:
+            for name, v in zip(names[1:], r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(busy)}
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+
+def run_oracle_threaded(x, w, wl, rows: int, threads: int):
+    """The oracle over the first `rows` rows, split into contiguous blocks over
+    `threads` Python threads (ctypes releases the GIL in the C call). Returns seconds."""
+    import numpy as np
+    import oracle
+    y = np.empty((rows, wl.N), dtype=np.uint16)
+    r = np.empty(rows, dtype=np.float64)
+    xs = np.ascontiguousarray(x[:rows])
+    bounds = [rows * i // threads for i in range(threads + 1)]
+    oracle.lib()
+    ts = [threading.Thread(target=oracle.rmsnorm_fwd_into,
+                           args=(xs, w, y, r, wl.eps, wl.offset, wl.dtype, bounds[i], bounds[i + 1]))
+          for i in range(threads) if bounds[i + 1] > bounds[i]]
+    t0 = time.perf_counter()
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(x, w, wl, repeats: int = 3):
+    cores = os.cpu_count() or 1
+    secs = [run_oracle_threaded(x, w, wl, wl.M, cores) for _ in range(repeats)]
+    t = statistics.median(secs)
+    return {"value": round(wl.algorithmic_bytes / t / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"whole {wl.M}x{wl.N} {wl.dtype} batch, {repeats} runs, median "
+                      f"({t:.3f} s each, fp64 C oracle, {cores} threads over row blocks)"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def bench_ours(args, wl, rank, world, local_rank):
+    import numpy as np
+    import torch
+    from memory_bound_normalization_fwd_gb300 import binding as B
+    from memory_bound_normalization_fwd_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dcode = B.BF16 if wl.dtype == "bf16" else B.FP16
+    x_bits, w_bits = W.generate(wl)
+    x_host = W.to_torch(x_bits, wl.dtype)
+    w_dev = W.to_torch(w_bits, wl.dtype).to(dev)
+    set_bytes = 4 * wl.M * wl.N + 4 * wl.M
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool = max(2, -(-3 * l2 // set_bytes))  # buffer sets totalling >= 3x L2
+    xs = [x_host.to(dev) for _ in range(pool)]
+    ys = [torch.empty_like(xs[0]) for _ in range(pool)]
+    rs = [torch.empty(wl.M, dtype=torch.float32, device=dev) for _ in range(pool)]
+    opts = B.make_options(variant=args.variant, lanes_per_row=args.lanes_per_row,
+                          stages=args.stages, rows_per_stage=args.rows_per_stage,
+                          max_ctas=args.max_ctas)
+    plan = B.rmsnorm_plan_info(wl.M, wl.N, dcode, xs[0].data_ptr(), w_dev.data_ptr(),
+                               ys[0].data_ptr(), opts)
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+
+    def step(k: int, s: int):
+        i = k % pool
+        rc = B.rmsnorm_fwd_ex(xs[i].data_ptr(), w_dev.data_ptr(), ys[i].data_ptr(), rs[i].data_ptr(),
+                              wl.M, wl.N, wl.eps, wl.offset, dcode, opts, s)
+        if rc != 0:
+            raise RuntimeError(B.rmsnorm_last_error())
+
+    # Eager warm-up (fills the planner caches), then capture one CUDA graph of
+    # `per_graph` back-to-back ABI calls cycling through the buffer pool.
+    with torch.cuda.stream(stream):
+        for k in range(max(3, min(args.warmup, 64))):
+            step(k, sh)
+    stream.synchronize()
+    per_graph = pool * max(1, 384 // pool)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+        for k in range(per_graph):
+            step(k, sh)
+    torch.cuda.synchronize()
+
+    K, Wm = args.steps, max(3, args.warmup)
+    replays, rem = divmod(K, per_graph)
+    with torch.cuda.stream(stream):
+        for _ in range(-(-Wm // per_graph)):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device() if world == 1 else local_rank)
+    with sampler:
+        torch.cuda.synchronize()
+        barrier()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(replays):
+                graph.replay()
+            for k in range(rem):
+                step(k, sh)
+            end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = start.elapsed_time(end)
+    max_s = max_over_ranks(ms / 1e3)
+    value = whole_job_gbs(wl.algorithmic_bytes, K, world, max_s)
+    per_launch_s = ms / 1e3 / K
+    clocks = sampler.summary()
+
+    # End to end: per step, pinned host x -> device, the ABI call, y and rstd -> pinned host.
+    x_pin = x_host.pin_memory()
+    y_pin = torch.empty(x_host.shape, dtype=x_host.dtype).pin_memory()
+    r_pin = torch.empty(wl.M, dtype=torch.float32).pin_memory()
+    x_e, y_e, r_e = xs[0], ys[0], rs[0]
+    Ke = max(20, min(args.e2e_steps, K))
+
+    def e2e_step():
+        x_e.copy_(x_pin, non_blocking=True)
+        rc = B.rmsnorm_fwd_ex(x_e.data_ptr(), w_dev.data_ptr(), y_e.data_ptr(), r_e.data_ptr(),
+                              wl.M, wl.N, wl.eps, wl.offset, dcode, opts, sh)
+        if rc != 0:
+            raise RuntimeError(B.rmsnorm_last_error())
+        y_pin.copy_(y_e, non_blocking=True)
+        r_pin.copy_(r_e, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_s = max_over_ranks(start.elapsed_time(end) / 1e3)
+    # Same answer as the device-resident run (pool set 1 holds the same x).
+    j = 1 % pool
+    if not (np.array_equal(W.from_torch(y_pin), W.from_torch(ys[j]))
+            and torch.equal(r_pin, rs[j].cpu())):
+        raise RuntimeError("end-to-end output differs from the device-resident output")
+
+    peak, peak_src = load_peaks()
+    achieved = wl.algorithmic_bytes / per_launch_s / 1e9
+    traffic = load_traffic(wl.name)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(max_s * 1e3 / K, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded torch CPU generator; see workloads.py)",
+        "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "eps": wl.eps, "offset": wl.offset,
+                   "x": f"N(0,{wl.x_std}^2)" + (f" + {wl.outlier_p} outliers N(0,{wl.outlier_std}^2)"
+                                                if wl.outlier_p else ""),
+                   "bytes_per_step": wl.algorithmic_bytes,
+                   "l2": f"rotating pool of {pool} buffer sets ({pool * set_bytes / 1e6:.0f} MB) "
+                         f"> 3x L2 ({l2 / 1e6:.0f} MB); no flush needed",
+                   "launch": f"CUDA graph of {per_graph} ABI calls, {replays} replays"
+                             + (f" + {rem} direct calls" if rem else ""),
+                   "plan": plan},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s", "algorithmic_bytes": wl.algorithmic_bytes,
+                     "kernel_hash": kernel_hash()},
+        "e2e": {"value": round(whole_job_gbs(wl.algorithmic_bytes, Ke, world, e2e_s), 2),
+                "unit": "GB/s", "h2d_bytes_per_step": 2 * wl.M * wl.N,
+                "d2h_bytes_per_step": 2 * wl.M * wl.N + 4 * wl.M, "steps": Ke,
+                "ms_per_step": round(e2e_s * 1e3 / Ke, 4),
+                "path": "pinned host x -> device, rmsnorm_fwd, y and rstd -> pinned host, one stream"},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x_bits, w_bits, wl)
+    return line
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def bench_reference(args, wl):
+    from memory_bound_normalization_fwd_gb300 import workloads as W
+    cores = os.cpu_count() or 1
+    x, w = W.generate(wl)
+    # Calibrate the rate, then size each step so the whole run takes about a minute.
+    probe = min(wl.M, 64 * cores)
+    t = run_oracle_threaded(x, w, wl, probe, cores)
+    rows_per_s = probe / max(t, 1e-6)
+    total = args.steps + max(3, args.warmup)
+    rows = int(max(cores, min(wl.M, rows_per_s * 60.0 / total)))
+    step_bytes = 4 * rows * wl.N + 2 * wl.N + 4 * rows
+    for _ in range(max(3, args.warmup) if total * rows / rows_per_s < 120 else 3):
+        run_oracle_threaded(x, w, wl, rows, cores)
+    secs = sum(run_oracle_threaded(x, w, wl, rows, cores) for _ in range(args.steps))
+    value = step_bytes * args.steps / secs / 1e9
+    sample = f"first {rows} of {wl.M} rows per step ({wl.N} columns, {wl.dtype}), fp64 C oracle"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(secs * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded torch CPU generator; see workloads.py)",
+        "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "eps": wl.eps, "offset": wl.offset,
+                   "bytes_per_step": step_bytes},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from memory_bound_normalization_fwd_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload or W.BENCH_WORKLOAD]
+    rank, world, local_rank = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(bench_reference(args, wl)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    try:
+        line = bench_ours(args, wl, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,164 @@
+/*
+ * rmsnorm.h — C ABI of the GB300 (sm_103a) RMSNorm forward library
+ * (librmsnorm_gb300.so).
+ *
+ * The operation. For a row-major activation x[M, N] and a weight w[N]:
+ *
+ *   rstd[i] = 1 / sqrt( (1/N) * sum_{j<N} x[i,j]^2 + eps )          (fp32)
+ *   y[i,j]  = dtype( (x[i,j] * rstd[i]) * (offset + w[j]) )
+ *
+ * with offset 0 for Llama-style weights and 1 for Gemma-style weights.
+ * Defined by the kernel listing of "Why cutile's rmsnorm required full
+ * register" (TileGym issue #169): x is widened to fp32 before squaring, the
+ * row sum of squares is divided by the true N, eps is added inside the rsqrt,
+ * the fp32 rstd is stored "for backward", the normalised row is scaled by
+ * (offset + w) in fp32 and cast once to x's dtype. The same formula, with
+ * offset 0, is the Overview and Verification formula of "RMSNorm Kernel
+ * Optimization" (skillmd): out = x / sqrt(mean(x^2) + eps) * weight.
+ * Arithmetic is fp32 throughout (sum of squares, mean, rsqrt, products); y is
+ * rounded to nearest-even once. Results are deterministic: the same inputs and
+ * launch shape always give the same bits.
+ *
+ * Memory. Every pointer is a DEVICE pointer on the calling thread's current
+ * CUDA device (cudaSetDevice), allocated by the caller. The library never
+ * allocates, frees or copies caller memory, and never synchronises except in
+ * rmsnorm_check_device_status().
+ *   x     [M, N] bf16 or fp16, contiguous row-major (row i at x + i*N)
+ *   w     [N]    same dtype as x
+ *   y     [M, N] same dtype as x; may equal x exactly (in place), must not
+ *                otherwise overlap x, w or rstd
+ *   rstd  [M]    fp32; must not overlap x, w or y
+ * x, w, y need only their element alignment (2 bytes) and rstd 4 bytes.
+ * 16-byte-aligned x, w, y with N a multiple of 8 take the vectorised kernels;
+ * anything else takes the general kernel.
+ *
+ * Streams and errors. Work is enqueued on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and the call returns at once. The return value
+ * reports argument errors (checked on the host before any CUDA call) and launch
+ * errors only. Kernels with bounded waits record a timeout in a per-device
+ * status word instead of hanging; rmsnorm_check_device_status() reads it.
+ * Calls are thread-safe. rmsnorm_last_error() gives a detail string for the
+ * last failed call on the calling thread.
+ */
+#ifndef RMSNORM_GB300_H
+#define RMSNORM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RMSNORM_GB300_VERSION 1
+
+typedef enum rmsnorm_dtype {
+    RMSNORM_DTYPE_BF16 = 0,
+    RMSNORM_DTYPE_FP16 = 1
+} rmsnorm_dtype_t;
+
+typedef enum rmsnorm_status {
+    RMSNORM_OK = 0,
+    RMSNORM_ERR_NULL = -1,           /* a required pointer is NULL */
+    RMSNORM_ERR_SHAPE = -2,          /* M < 0, N <= 0, or M*N*2 bytes overflows int64 */
+    RMSNORM_ERR_DTYPE = -3,          /* dtype is not an rmsnorm_dtype_t value */
+    RMSNORM_ERR_SCALAR = -4,         /* eps negative or not finite, or offset not finite */
+    RMSNORM_ERR_OVERLAP = -5,        /* buffers overlap other than y == x exactly */
+    RMSNORM_ERR_CUDA = -6,           /* a CUDA runtime call or launch failed */
+    RMSNORM_ERR_DEVICE_TIMEOUT = -7, /* a kernel's bounded wait ran out (see rmsnorm_check_device_status) */
+    RMSNORM_ERR_UNSUPPORTED = -8,    /* the forced variant cannot take these arguments */
+    RMSNORM_ERR_OPTIONS = -9,        /* malformed rmsnorm_options_t */
+    RMSNORM_ERR_ALIGN = -10          /* x, w or y not 2-byte aligned, or rstd not 4-byte aligned */
+} rmsnorm_status_t;
+
+/* Kernel variants. RMSNORM_VARIANT_AUTO lets the planner choose. */
+typedef enum rmsnorm_variant {
+    RMSNORM_VARIANT_AUTO = 0,
+    /* A team of 1..32 lanes of one warp per row, row held in registers,
+     * several rows per warp when N is small (warp-per-row and
+     * multi-row-per-warp). Needs 16-byte alignment and N % 8 == 0, N <= 1024. */
+    RMSNORM_VARIANT_WARP = 1,
+    /* One CTA per row, row held in registers across the CTA, cross-warp sum
+     * through shared memory. Needs 16-byte alignment and N % 8 == 0,
+     * N <= 32768. */
+    RMSNORM_VARIANT_CTA = 2,
+    /* Rows staged in shared memory by TMA bulk copies (cp.async.bulk with an
+     * mbarrier), multi-stage pipeline, bounded waits. Needs 16-byte alignment
+     * and N % 8 == 0; rows up to the shared-memory limit. */
+    RMSNORM_VARIANT_TMA = 3,
+    /* Any alignment and any N: one CTA per row, two passes over the row. */
+    RMSNORM_VARIANT_GENERIC = 4
+} rmsnorm_variant_t;
+
+/* Optional knobs for rmsnorm_fwd_ex(). Zero-initialise, then set fields. */
+typedef struct rmsnorm_options {
+    int32_t struct_size;     /* sizeof(rmsnorm_options_t) */
+    int32_t variant;         /* rmsnorm_variant_t; 0 = automatic */
+    int32_t max_ctas;        /* >0 caps the persistent grid; 0 = SMs x resident CTAs */
+    int32_t lanes_per_row;   /* WARP: lanes per row (1..32, power of two); CTA, TMA and
+                                GENERIC: threads per CTA; 0 = planner's choice */
+    int32_t stages;          /* TMA: pipeline depth (1..8); 0 = planner's choice */
+    int32_t rows_per_stage;  /* TMA: rows per stage; 0 = planner's choice */
+    int64_t wait_limit_ns;   /* TMA: bound on each mbarrier wait in ns; 0 = 1 second */
+} rmsnorm_options_t;
+
+/* What the planner picked (rmsnorm_plan_info). */
+typedef struct rmsnorm_plan {
+    int32_t variant;         /* rmsnorm_variant_t actually launched */
+    int32_t threads;         /* threads per CTA */
+    int32_t grid;            /* CTAs launched (persistent grid) */
+    int32_t lanes_per_row;   /* threads cooperating on one row */
+    int32_t vecs_per_lane;   /* 16-byte vectors each thread holds per row (0: general kernel) */
+    int32_t rows_per_stage;  /* TMA variant: rows per shared-memory stage (else 0) */
+    int32_t stages;          /* TMA variant: pipeline depth (else 0) */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t ctas_per_sm;     /* resident CTAs per SM (occupancy calculator) */
+    int32_t sm_count;        /* SMs on the device */
+} rmsnorm_plan_t;
+
+/*
+ * RMSNorm forward: y = x * rsqrt(mean(x^2) + eps) * (offset + w), rstd kept.
+ *   x, w, y, rstd  device pointers as described above (x, y, rstd may be NULL
+ *                  when M == 0; w must not be NULL)
+ *   M              rows (>= 0; M == 0 launches nothing and returns RMSNORM_OK)
+ *   N              columns (> 0)
+ *   eps            >= 0 and finite; added to the mean of squares inside the root
+ *   offset         finite; 0 = Llama, 1 = Gemma
+ *   dtype          rmsnorm_dtype_t of x, w and y
+ *   stream         cudaStream_t to enqueue on (NULL = legacy default stream)
+ * Returns RMSNORM_OK or a negative rmsnorm_status_t; on error nothing is
+ * launched and rmsnorm_last_error() says why.
+ */
+int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
+                float eps, float offset, int dtype, void* stream);
+
+/* rmsnorm_fwd with explicit options (variant choice, grid cap, pipeline depth,
+ * wait bound). `opts` may be NULL (same as rmsnorm_fwd). */
+int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
+                   float eps, float offset, int dtype, const rmsnorm_options_t* opts,
+                   void* stream);
+
+/* Fills *out with the launch rmsnorm_fwd_ex would make for these arguments on
+ * the current device (no launch). x, w, y are used only for their alignment
+ * and may be any values with the alignment the real call will have. */
+int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void* w,
+                      const void* y, const rmsnorm_options_t* opts, rmsnorm_plan_t* out);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns RMSNORM_OK, RMSNORM_ERR_DEVICE_TIMEOUT if any kernel since the
+ * last check gave up a bounded wait, or RMSNORM_ERR_CUDA. */
+int rmsnorm_check_device_status(void* stream);
+
+/* Static text for a status code. */
+const char* rmsnorm_strerror(int status);
+
+/* Detail of the last failed call on this thread ("" if none). */
+const char* rmsnorm_last_error(void);
+
+/* RMSNORM_GB300_VERSION of the loaded library. */
+int rmsnorm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_GB300_H */

@@ -1,0 +1,183 @@
+"""Thin Python binding of the C ABI in include/rmsnorm.h (ctypes).
+
+Argument marshalling only: every step of the RMSNorm forward runs in the CUDA
+library. The raw functions keep the C names and take integer device
+addresses; ``fwd`` is a convenience over torch tensors (torch supplies device
+memory and the current stream, nothing else). There is no fallback: if the
+library has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+BF16, FP16 = 0, 1
+VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "tma": 3, "generic": 4}
+VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
+STATUS = {
+    0: "RMSNORM_OK", -1: "RMSNORM_ERR_NULL", -2: "RMSNORM_ERR_SHAPE", -3: "RMSNORM_ERR_DTYPE",
+    -4: "RMSNORM_ERR_SCALAR", -5: "RMSNORM_ERR_OVERLAP", -6: "RMSNORM_ERR_CUDA",
+    -7: "RMSNORM_ERR_DEVICE_TIMEOUT", -8: "RMSNORM_ERR_UNSUPPORTED", -9: "RMSNORM_ERR_OPTIONS",
+    -10: "RMSNORM_ERR_ALIGN",
+}
+# Every function include/rmsnorm.h declares.
+EXPORTS = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_plan_info", "rmsnorm_check_device_status",
+           "rmsnorm_strerror", "rmsnorm_last_error", "rmsnorm_version")
+
+
+class RMSNormError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{STATUS.get(status, status)}: {detail}")
+        self.status = status
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_int32), ("variant", ctypes.c_int32),
+                ("max_ctas", ctypes.c_int32), ("lanes_per_row", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("rows_per_stage", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_int64)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "variant", "threads", "grid", "lanes_per_row", "vecs_per_lane", "rows_per_stage",
+        "stages", "smem_bytes", "ctas_per_sm", "sm_count")]
+
+    def as_dict(self) -> dict:
+        d = {n: getattr(self, n) for n, _ in self._fields_}
+        d["variant"] = VARIANT_NAMES.get(d["variant"], d["variant"])
+        return d
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"RMSNorm CUDA library not built ({path} missing); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(path)
+            vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+            L.rmsnorm_fwd.argtypes = [vp, vp, vp, vp, i64, i64, f32, f32, i32, vp]
+            L.rmsnorm_fwd.restype = i32
+            L.rmsnorm_fwd_ex.argtypes = [vp, vp, vp, vp, i64, i64, f32, f32, i32,
+                                         ctypes.POINTER(Options), vp]
+            L.rmsnorm_fwd_ex.restype = i32
+            L.rmsnorm_plan_info.argtypes = [i64, i64, i32, vp, vp, vp, ctypes.POINTER(Options),
+                                            ctypes.POINTER(Plan)]
+            L.rmsnorm_plan_info.restype = i32
+            L.rmsnorm_check_device_status.argtypes = [vp]
+            L.rmsnorm_check_device_status.restype = i32
+            L.rmsnorm_strerror.argtypes = [i32]
+            L.rmsnorm_strerror.restype = ctypes.c_char_p
+            L.rmsnorm_last_error.argtypes = []
+            L.rmsnorm_last_error.restype = ctypes.c_char_p
+            L.rmsnorm_version.argtypes = []
+            L.rmsnorm_version.restype = i32
+            _lib = L
+    return _lib
+
+
+def _check(rc: int) -> int:
+    if rc != 0:
+        raise RMSNormError(rc, lib().rmsnorm_last_error().decode())
+    return rc
+
+
+def make_options(variant: str | int = "auto", max_ctas: int = 0, lanes_per_row: int = 0,
+                 stages: int = 0, rows_per_stage: int = 0, wait_limit_ns: int = 0) -> Options:
+    v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    return Options(ctypes.sizeof(Options), v, max_ctas, lanes_per_row, stages, rows_per_stage,
+                   wait_limit_ns)
+
+
+# ---- raw C ABI (integer device addresses) --------------------------------
+
+def rmsnorm_fwd(x: int, w: int, y: int, rstd: int, M: int, N: int, eps: float, offset: float,
+                dtype: int, stream: int) -> int:
+    return lib().rmsnorm_fwd(x, w, y, rstd, M, N, eps, offset, dtype, stream)
+
+
+def rmsnorm_fwd_ex(x: int, w: int, y: int, rstd: int, M: int, N: int, eps: float, offset: float,
+                   dtype: int, opts: Options | None, stream: int) -> int:
+    return lib().rmsnorm_fwd_ex(x, w, y, rstd, M, N, eps, offset, dtype,
+                                ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def rmsnorm_plan_info(M: int, N: int, dtype: int, x: int = 0, w: int = 0, y: int = 0,
+                      opts: Options | None = None) -> dict:
+    out = Plan()
+    _check(lib().rmsnorm_plan_info(M, N, dtype, x, w, y,
+                                   ctypes.byref(opts) if opts is not None else None,
+                                   ctypes.byref(out)))
+    return out.as_dict()
+
+
+def rmsnorm_check_device_status(stream: int = 0) -> int:
+    return lib().rmsnorm_check_device_status(stream)
+
+
+def rmsnorm_strerror(status: int) -> str:
+    return lib().rmsnorm_strerror(status).decode()
+
+
+def rmsnorm_last_error() -> str:
+    return lib().rmsnorm_last_error().decode()
+
+
+def rmsnorm_version() -> int:
+    return lib().rmsnorm_version()
+
+
+# ---- torch convenience ---------------------------------------------------
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float16:
+        return FP16
+    raise TypeError(f"RMSNorm forward takes bf16 or fp16 activations, got {t.dtype}")
+
+
+def fwd(x, w, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=None, stream=None,
+        **options):
+    """y, rstd = fwd(x, w): RMSNorm forward of a contiguous CUDA tensor x[..., N].
+
+    ``y`` and ``rstd`` may be passed to write in place (y may be x itself).
+    Keyword ``options`` go to :func:`make_options` (variant, max_ctas, ...).
+    Runs on ``stream`` (a torch.cuda.Stream) or the current stream.
+    """
+    import torch
+    if not (x.is_cuda and w.is_cuda):
+        raise ValueError("x and w must be CUDA tensors")
+    if not x.is_contiguous() or not w.is_contiguous():
+        raise ValueError("x and w must be contiguous")
+    N = x.shape[-1]
+    M = x.numel() // N if N else 0
+    if w.dtype != x.dtype or w.numel() != N:
+        raise ValueError("w must have x's dtype and N elements")
+    if y is None:
+        y = torch.empty_like(x)
+    if rstd is None:
+        rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    opts = make_options(**options) if options else None
+    with torch.cuda.device(x.device):
+        _check(rmsnorm_fwd_ex(x.data_ptr(), w.data_ptr(), y.data_ptr(), rstd.data_ptr(), M, N,
+                              eps, offset, _dtype_code(x), opts, s.cuda_stream))
+    return y, rstd

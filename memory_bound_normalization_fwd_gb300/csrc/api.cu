@@ -1,0 +1,268 @@
+// C ABI front end: argument validation (host only, before any CUDA call),
+// variant planning, per-device caches, launch, error reporting.
+// The operation and its sources are described in include/rmsnorm.h.
+#include "rmsnorm.h"
+
+#include "launch.h"
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+namespace rmsn {
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_dev_once[kMaxDevices];
+DeviceInfo g_dev[kMaxDevices];
+cudaError_t g_dev_err[kMaxDevices];
+
+cudaError_t device_info(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(g_dev_once[dev], [dev] {
+        DeviceInfo d;
+        cudaError_t err = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (err == cudaSuccess)
+            err = cudaDeviceGetAttribute(&d.max_smem_optin,
+                                         cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        g_dev[dev] = d;
+        g_dev_err[dev] = err;
+    });
+    if (g_dev_err[dev] != cudaSuccess) return g_dev_err[dev];
+    *out = g_dev[dev];
+    return cudaSuccess;
+}
+
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+int validate(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N, float eps,
+             float offset, int dtype) {
+    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16)
+        return fail(RMSNORM_ERR_DTYPE, "dtype %d is not RMSNORM_DTYPE_BF16 (0) or _FP16 (1)", dtype);
+    if (M < 0 || N <= 0)
+        return fail(RMSNORM_ERR_SHAPE, "need M >= 0 and N > 0 (got M=%lld N=%lld)",
+                    static_cast<long long>(M), static_cast<long long>(N));
+    if (M > 0 && (N > INT64_MAX / 2 / M || M > INT64_MAX / 4))
+        return fail(RMSNORM_ERR_SHAPE, "M*N elements overflow (M=%lld N=%lld)",
+                    static_cast<long long>(M), static_cast<long long>(N));
+    if (!std::isfinite(eps) || eps < 0.f)
+        return fail(RMSNORM_ERR_SCALAR, "eps must be finite and >= 0 (got %g)", eps);
+    if (!std::isfinite(offset))
+        return fail(RMSNORM_ERR_SCALAR, "offset must be finite (got %g)", offset);
+    if (w == nullptr) return fail(RMSNORM_ERR_NULL, "w is NULL");
+    if (M == 0) return RMSNORM_OK;
+    if (x == nullptr || y == nullptr || rstd == nullptr)
+        return fail(RMSNORM_ERR_NULL, "x, y and rstd must be non-NULL when M > 0");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
+         reinterpret_cast<uintptr_t>(w)) & 1u)
+        return fail(RMSNORM_ERR_ALIGN, "x, w and y must be 2-byte aligned");
+    if (reinterpret_cast<uintptr_t>(rstd) & 3u)
+        return fail(RMSNORM_ERR_ALIGN, "rstd must be 4-byte aligned");
+    const int64_t xb = M * N * 2, wb = N * 2, rb = M * 4;
+    if (x != y && overlaps(x, xb, y, xb))
+        return fail(RMSNORM_ERR_OVERLAP, "y overlaps x without being equal to it");
+    if (overlaps(w, wb, y, xb)) return fail(RMSNORM_ERR_OVERLAP, "w overlaps y");
+    if (overlaps(rstd, rb, x, xb) || overlaps(rstd, rb, y, xb) || overlaps(rstd, rb, w, wb))
+        return fail(RMSNORM_ERR_OVERLAP, "rstd overlaps x, y or w");
+    return RMSNORM_OK;
+}
+
+int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
+    *variant = RMSNORM_VARIANT_AUTO;
+    *k = Knobs{};
+    if (o == nullptr) return RMSNORM_OK;
+    if (o->struct_size != static_cast<int32_t>(sizeof(rmsnorm_options_t)))
+        return fail(RMSNORM_ERR_OPTIONS, "options.struct_size is %d, expected %d", o->struct_size,
+                    static_cast<int>(sizeof(rmsnorm_options_t)));
+    if (o->variant < RMSNORM_VARIANT_AUTO || o->variant > RMSNORM_VARIANT_GENERIC)
+        return fail(RMSNORM_ERR_OPTIONS, "options.variant %d is not a rmsnorm_variant_t",
+                    o->variant);
+    if (o->max_ctas < 0 || o->lanes_per_row < 0 || o->rows_per_stage < 0 || o->stages < 0 ||
+        o->stages > 8 || o->wait_limit_ns < 0)
+        return fail(RMSNORM_ERR_OPTIONS, "options fields out of range");
+    *variant = o->variant;
+    k->max_ctas = o->max_ctas;
+    k->lanes_per_row = o->lanes_per_row;
+    k->stages = o->stages;
+    k->rows_per_stage = o->rows_per_stage;
+    k->wait_limit_ns = o->wait_limit_ns;
+    return RMSNORM_OK;
+}
+
+// Chooses the variant. The automatic choice: the warp-team kernel for rows up
+// to 1024 columns, the TMA-staged kernel for longer rows, each only when x, w
+// and y are 16-byte aligned and N % 8 == 0; the general kernel otherwise.
+int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch& l,
+         int* chosen) {
+    bool ok = false;
+    switch (variant) {
+        case RMSNORM_VARIANT_WARP: ok = warp_choose(a, d, k, l); break;
+        case RMSNORM_VARIANT_CTA: ok = cta_choose(a, d, k, l); break;
+        case RMSNORM_VARIANT_TMA: ok = tma_choose(a, d, k, l); break;
+        case RMSNORM_VARIANT_GENERIC: ok = generic_choose(a, d, k, l); break;
+        default:
+            if (a.N <= 1024 && warp_choose(a, d, k, l)) {
+                variant = RMSNORM_VARIANT_WARP;
+                ok = true;
+            } else if (a.N > 1024 && cta_choose(a, d, k, l)) {
+                variant = RMSNORM_VARIANT_CTA;
+                ok = true;
+            } else {
+                variant = RMSNORM_VARIANT_GENERIC;
+                ok = generic_choose(a, d, k, l);
+            }
+    }
+    if (!ok)
+        return fail(RMSNORM_ERR_UNSUPPORTED,
+                    "variant %d cannot take M=%lld N=%lld with these alignments and options",
+                    variant, static_cast<long long>(a.M), static_cast<long long>(a.N));
+    *chosen = variant;
+    return RMSNORM_OK;
+}
+
+cudaError_t run(int variant, const Args& a, const Launch& l) {
+    switch (variant) {
+        case RMSNORM_VARIANT_WARP: return warp_run(a, l);
+        case RMSNORM_VARIANT_CTA: return cta_run(a, l);
+        case RMSNORM_VARIANT_TMA: return tma_run(a, l);
+        default: return generic_run(a, l);
+    }
+}
+
+}  // namespace
+
+int occupancy(const void* kernel, int threads, int smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void*, int, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const auto key = std::make_tuple(dev, kernel, threads, smem);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads,
+                                                      static_cast<size_t>(smem)) != cudaSuccess)
+        n = 0;
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = n;
+    return n;
+}
+
+}  // namespace rmsn
+
+using namespace rmsn;
+
+extern "C" int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M,
+                              int64_t N, float eps, float offset, int dtype,
+                              const rmsnorm_options_t* opts, void* stream) {
+    int rc = validate(x, w, y, rstd, M, N, eps, offset, dtype);
+    if (rc != RMSNORM_OK) return rc;
+    int variant;
+    Knobs k;
+    rc = read_knobs(opts, &variant, &k);
+    if (rc != RMSNORM_OK) return rc;
+    if (M == 0) return RMSNORM_OK;
+    DeviceInfo d;
+    cudaError_t e = device_info(&d);
+    if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+    const Args a{x, w, y, rstd, M, N, eps, offset, dtype, static_cast<cudaStream_t>(stream)};
+    Launch l;
+    int chosen = 0;
+    rc = plan(a, d, variant, k, l, &chosen);
+    if (rc != RMSNORM_OK) return rc;
+    e = run(chosen, a, l);
+    if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return RMSNORM_OK;
+}
+
+extern "C" int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M,
+                           int64_t N, float eps, float offset, int dtype, void* stream) {
+    return rmsnorm_fwd_ex(x, w, y, rstd, M, N, eps, offset, dtype, nullptr, stream);
+}
+
+extern "C" int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void* w,
+                                 const void* y, const rmsnorm_options_t* opts,
+                                 rmsnorm_plan_t* out) {
+    if (out == nullptr) return fail(RMSNORM_ERR_NULL, "out is NULL");
+    std::memset(out, 0, sizeof(*out));
+    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16)
+        return fail(RMSNORM_ERR_DTYPE, "dtype %d is not a rmsnorm_dtype_t", dtype);
+    if (M < 1 || N <= 0) return fail(RMSNORM_ERR_SHAPE, "plan needs M >= 1 and N > 0");
+    int variant;
+    Knobs k;
+    int rc = read_knobs(opts, &variant, &k);
+    if (rc != RMSNORM_OK) return rc;
+    DeviceInfo d;
+    cudaError_t e = device_info(&d);
+    if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+    const Args a{x, w, const_cast<void*>(y), nullptr, M, N, 0.f, 0.f, dtype, nullptr};
+    Launch l;
+    int chosen = 0;
+    rc = plan(a, d, variant, k, l, &chosen);
+    if (rc != RMSNORM_OK) return rc;
+    out->variant = chosen;
+    out->threads = l.threads;
+    out->grid = l.grid;
+    out->lanes_per_row = l.lanes_per_row;
+    out->vecs_per_lane = l.vecs_per_lane;
+    out->rows_per_stage = l.rows_per_stage;
+    out->stages = l.stages;
+    out->smem_bytes = l.smem;
+    out->ctas_per_sm = l.ctas_per_sm;
+    out->sm_count = d.sm_count;
+    return RMSNORM_OK;
+}
+
+extern "C" int rmsnorm_check_device_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "synchronize: %s", cudaGetErrorString(e));
+    unsigned int v = 0;
+    e = status_read_and_clear(&v);
+    if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+    if (v != 0) return fail(RMSNORM_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
+    return RMSNORM_OK;
+}
+
+extern "C" const char* rmsnorm_strerror(int status) {
+    switch (status) {
+        case RMSNORM_OK: return "ok";
+        case RMSNORM_ERR_NULL: return "null pointer";
+        case RMSNORM_ERR_SHAPE: return "bad shape";
+        case RMSNORM_ERR_DTYPE: return "unknown dtype";
+        case RMSNORM_ERR_SCALAR: return "bad eps or offset";
+        case RMSNORM_ERR_OVERLAP: return "buffers overlap";
+        case RMSNORM_ERR_CUDA: return "CUDA error";
+        case RMSNORM_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case RMSNORM_ERR_UNSUPPORTED: return "variant unsupported for these arguments";
+        case RMSNORM_ERR_OPTIONS: return "bad options";
+        case RMSNORM_ERR_ALIGN: return "misaligned pointer";
+        default: return "unknown status";
+    }
+}
+
+extern "C" const char* rmsnorm_last_error(void) { return t_last_error; }
+
+extern "C" int rmsnorm_version(void) { return RMSNORM_GB300_VERSION; }

@@ -1,0 +1,113 @@
+// Shared device helpers for the RMSNorm forward kernels (sm_103a).
+//
+// The arithmetic every kernel performs per row follows the kernel listing of
+// "Why cutile's rmsnorm required full register" (TileGym issue #169): widen to
+// fp32, sum of squares, divide by N, add eps, rsqrt, store rstd, multiply by
+// rstd and then by (offset + w), one rounding to the activation dtype.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+enum DType : int { kBF16 = 0, kFP16 = 1 };
+
+// Element codecs. A 32-bit word holds two elements, element 0 in the low half
+// (little-endian memory order).
+template <int DT>
+struct Codec;
+
+template <>
+struct Codec<kBF16> {
+    static __device__ __forceinline__ float2 unpack2(uint32_t u) {
+        // bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits.
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+    }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    static __device__ __forceinline__ float unpack1(uint16_t u) {
+        return __uint_as_float(static_cast<uint32_t>(u) << 16);
+    }
+    static __device__ __forceinline__ uint16_t pack1(float a) {
+        __nv_bfloat16 h = __float2bfloat16_rn(a);
+        return *reinterpret_cast<uint16_t*>(&h);
+    }
+};
+
+template <>
+struct Codec<kFP16> {
+    static __device__ __forceinline__ float2 unpack2(uint32_t u) {
+        __half2 h = *reinterpret_cast<__half2*>(&u);
+        return __half22float2(h);
+    }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    static __device__ __forceinline__ float unpack1(uint16_t u) {
+        __half h = *reinterpret_cast<__half*>(&u);
+        return __half2float(h);
+    }
+    static __device__ __forceinline__ uint16_t pack1(float a) {
+        __half h = __float2half_rn(a);
+        return *reinterpret_cast<uint16_t*>(&h);
+    }
+};
+
+// 16-byte vector = 8 elements.
+constexpr int kVecElems = 8;
+
+// Sum of squares of the 8 elements of a vector, accumulated into acc.
+template <int DT>
+__device__ __forceinline__ float sumsq8(const uint4& v, float acc) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float2 f = Codec<DT>::unpack2(w[k]);
+        acc = fmaf(f.x, f.x, acc);
+        acc = fmaf(f.y, f.y, acc);
+    }
+    return acc;
+}
+
+// y = (x * r) * s for 8 elements; s holds offset + w in fp32.
+template <int DT>
+__device__ __forceinline__ uint4 scale8(const uint4& v, float r, const float* s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float2 f = Codec<DT>::unpack2(w[k]);
+        o[k] = Codec<DT>::pack2((f.x * r) * s[2 * k], (f.y * r) * s[2 * k + 1]);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// offset + w for the 8 weights of a vector, in fp32.
+template <int DT>
+__device__ __forceinline__ void weights8(const uint4& v, float offset, float* s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float2 f = Codec<DT>::unpack2(w[k]);
+        s[2 * k] = offset + f.x;
+        s[2 * k + 1] = offset + f.y;
+    }
+}
+
+// Streaming global accesses: x and y are touched once, so they are loaded and
+// stored with the evict-first (.cs) policy and do not displace the weights.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
+
+// The per-row scalar step: mean of squares, plus eps, rsqrt.
+__device__ __forceinline__ float row_rstd(float sumsq, float n, float eps) {
+    return rsqrtf(__fdiv_rn(sumsq, n) + eps);
+}
+
+}  // namespace rmsn

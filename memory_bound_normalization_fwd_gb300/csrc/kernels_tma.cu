@@ -1,0 +1,361 @@
+// TMA-staged variant: rows reach shared memory through bulk asynchronous copies
+// (cp.async.bulk, completion counted on an mbarrier), in a ring of S stages of
+// R consecutive rows each; a stage of R rows is one contiguous span of x, so it
+// is a single copy. One thread issues the copies; all threads consume.
+//
+// This is the CTA-per-row design for large hidden sizes that stages rows
+// through shared memory instead of holding them in registers, so the bytes in
+// flight per SM no longer depend on the register budget (the persistent cuTile
+// kernel of TileGym issue #169 reports 255 registers per thread at 16384x512).
+// The arithmetic per row is that kernel's: fp32 sum of squares, divide by N,
+// add eps, rsqrt, rstd store, (x * rstd) * (offset + w), one rounding.
+// Copies are plain (no cluster multicast); each CTA fetches only its own rows.
+//
+// Consumers: teams of TEAM threads take rows of the stage (TEAM <= 32: several
+// rows per warp; TEAM > 32: a warp butterfly, then a named barrier over the
+// team's warps and a shared-memory sum). Each thread reads its 16-byte vectors
+// of the row from shared memory once, keeps them in registers for the scale
+// step, and writes y with 16-byte evict-first stores.
+//
+// Waits are bounded: a stage that has not landed within the wait limit sets
+// the device status word, the CTA stops consuming, waits (again bounded) for
+// the copies it still has in flight, and exits. No wait depends on another CTA.
+#include "common.cuh"
+#include "launch.h"
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+namespace rmsn {
+
+// Bit 0: some bounded wait ran out since the last read. One word per device.
+__device__ unsigned int g_status;
+
+namespace {
+
+constexpr int kMaxStages = 8;
+constexpr int kHeaderBytes = 128;  // mbarriers, padded so stages start 128-byte aligned
+constexpr int kAlignSlack = 128;   // room to align the dynamic shared memory base
+constexpr long long kDrainLimitNs = 1000000000LL;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Global -> shared bulk copy; completion is signalled on `bar` as `bytes` transactions.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, for at most `limit` SM cycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (clock64() - t0 < limit) {
+        if (mbar_try(bar, parity)) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void team_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+template <int DT, int THREADS, int TEAM, int V>
+__global__ void __launch_bounds__(THREADS)
+tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
+                int64_t M, int nvec, float n, float eps, float offset, int rows_per_stage,
+                int stages, int stage_stride, long long limit_cycles, long long drain_cycles) {
+    constexpr int kTeams = THREADS / TEAM;
+    constexpr int kLanes = TEAM < 32 ? TEAM : 32;        // lanes in the shuffle step
+    constexpr int kTeamWarps = TEAM > 32 ? TEAM / 32 : 1;  // warps per team
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float part[2][kTeams][kTeamWarps];
+
+    const int tid = threadIdx.x;
+    const int team = tid / TEAM;
+    const int t = tid % TEAM;
+    const int R = rows_per_stage;
+    const int64_t ntiles = (M + R - 1) / R;
+    // Round the dynamic shared memory base up to 128 bytes (the launch adds
+    // kAlignSlack bytes for this), so barriers and stages are aligned whatever
+    // the static shared memory in front of it.
+    const uint32_t raw = smem_u32(smem);
+    unsigned char* base = smem + (((raw + 127u) & ~127u) - raw);
+    const uint32_t bars = smem_u32(base);
+    unsigned char* buf = base + kHeaderBytes;
+
+    float s[V][kVecElems];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * TEAM + t;
+        uint4 wv = make_uint4(0u, 0u, 0u, 0u);
+        if (c < nvec) wv = __ldg(w + c);
+        weights8<DT>(wv, offset, s[v]);
+    }
+
+    if (tid == 0) {
+        for (int st = 0; st < stages; ++st) mbar_init(bars + 8 * st, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // Local tile k of this CTA is tile blockIdx.x + k * gridDim.x, in stage k % stages.
+    auto issue = [&](int64_t k) {
+        const int64_t tile = blockIdx.x + k * gridDim.x;
+        if (tile >= ntiles) return;
+        const int st = static_cast<int>(k % stages);
+        const int64_t r0 = tile * R;
+        const int64_t rows = (M - r0) < R ? (M - r0) : R;
+        const uint32_t bytes = static_cast<uint32_t>(rows * nvec * 16);
+        mbar_arrive_expect_tx(bars + 8 * st, bytes);
+        bulk_g2s(smem_u32(buf + static_cast<int64_t>(st) * stage_stride), x + r0 * nvec, bytes,
+                 bars + 8 * st);
+    };
+    if (tid == 0) {
+        for (int k = 0; k < stages; ++k) issue(k);
+    }
+
+    int pp = 0;
+    int64_t k = 0;
+    bool aborted = false;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+        const int st = static_cast<int>(k % stages);
+        const uint32_t phase = static_cast<uint32_t>((k / stages) & 1);
+        const bool ok = mbar_wait_bounded(bars + 8 * st, phase, limit_cycles);
+        if (__syncthreads_or(!ok)) {
+            aborted = true;
+            break;
+        }
+        const uint4* sx = reinterpret_cast<const uint4*>(buf + static_cast<int64_t>(st) * stage_stride);
+        const int64_t r0 = tile * R;
+        const int rows = static_cast<int>((M - r0) < R ? (M - r0) : R);
+        const int iters = (rows + kTeams - 1) / kTeams;  // CTA-uniform
+        for (int i = 0; i < iters; ++i) {
+            const int rr = i * kTeams + team;
+            const bool act = rr < rows;
+            uint4 xv[V];
+            float ss = 0.f;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const int c = v * TEAM + t;
+                xv[v] = make_uint4(0u, 0u, 0u, 0u);
+                if (act && c < nvec) xv[v] = sx[rr * nvec + c];
+                ss = sumsq8<DT>(xv[v], ss);
+            }
+#pragma unroll
+            for (int off = kLanes / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if constexpr (TEAM > 32) {
+                if ((t & 31) == 0) part[pp][team][t >> 5] = ss;
+                team_barrier(1 + team, TEAM);
+                ss = 0.f;
+#pragma unroll
+                for (int q = 0; q < kTeamWarps; ++q) ss += part[pp][team][q];
+                pp ^= 1;
+            }
+            if (act) {
+                const int64_t row = r0 + rr;
+                const float r = row_rstd(ss, n, eps);
+                if (t == 0) rstd[row] = r;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const int c = v * TEAM + t;
+                    if (c < nvec) st_stream(y + row * nvec + c, scale8<DT>(xv[v], r, s[v]));
+                }
+            }
+        }
+        __syncthreads();  // every thread is done reading this stage
+        if (tid == 0) issue(k + stages);
+    }
+
+    if (aborted && tid == 0) {
+        atomicOr(&g_status, 1u);
+        // Copies for local tiles k .. k + stages - 1 may still be in flight into
+        // this CTA's shared memory: wait for them before the CTA retires.
+        for (int64_t j = k; j < k + stages; ++j) {
+            if (blockIdx.x + j * gridDim.x >= ntiles) break;
+            mbar_wait_bounded(bars + 8 * static_cast<int>(j % stages),
+                              static_cast<uint32_t>((j / stages) & 1), drain_cycles);
+        }
+    }
+}
+
+using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, float, float, float,
+                    int, int, int, long long, long long);
+
+template <int DT>
+Fn pick(int team, int V) {
+#define RMSN_CASE(tm, v) \
+    if (team == tm && V == v) return tma_rows_kernel<DT, (tm < 256 ? 256 : tm), tm, v>;
+    RMSN_CASE(16, 1) RMSN_CASE(16, 2) RMSN_CASE(16, 4)
+    RMSN_CASE(32, 1) RMSN_CASE(32, 2) RMSN_CASE(32, 4)
+    RMSN_CASE(64, 1) RMSN_CASE(64, 2) RMSN_CASE(64, 4)
+    RMSN_CASE(128, 1) RMSN_CASE(128, 2) RMSN_CASE(128, 4)
+    RMSN_CASE(256, 1) RMSN_CASE(256, 2) RMSN_CASE(256, 4)
+    RMSN_CASE(512, 1) RMSN_CASE(512, 2) RMSN_CASE(512, 4)
+    RMSN_CASE(1024, 1) RMSN_CASE(1024, 2) RMSN_CASE(1024, 4)
+#undef RMSN_CASE
+    return nullptr;
+}
+
+// Opts a TMA kernel into all of the device's dynamic shared memory, once per
+// device; returns that byte count (0 on failure). Later calls touch only a cache,
+// so planning makes no CUDA call (and stays legal inside stream capture).
+int max_dynamic_smem(const void* fn, int max_optin) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> g(mu);
+    auto it = done.find({dev, fn});
+    if (it != done.end()) return it->second;
+    cudaFuncAttributes attr;
+    int bytes = 0;
+    if (cudaFuncGetAttributes(&attr, fn) == cudaSuccess) {
+        bytes = max_optin - static_cast<int>(attr.sharedSizeBytes);
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+            cudaSuccess)
+            bytes = 0;
+    }
+    done[{dev, fn}] = bytes;
+    return bytes;
+}
+
+int next_pow2(int64_t v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+}  // namespace
+
+bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
+    if (a.N % kVecElems != 0 || !aligned16(a.x) || !aligned16(a.y) || !aligned16(a.w)) return false;
+    const int64_t nvec = a.N / kVecElems;
+    int team = k.lanes_per_row;
+    if (team == 0) {
+        team = next_pow2((nvec + 3) / 4);
+        if (team < 16) team = 16;
+    }
+    if (team < 16 || team > 1024 || (team & (team - 1)) != 0) return false;
+    const int V = next_pow2((nvec + team - 1) / team);
+    if (V > 4) return false;
+    Fn fn = a.dtype == kBF16 ? pick<kBF16>(team, V) : pick<kFP16>(team, V);
+    if (!fn) return false;
+    const int threads = team < 256 ? 256 : team;
+    const int teams = threads / team;
+
+    const int max_dyn = max_dynamic_smem(reinterpret_cast<const void*>(fn), d.max_smem_optin);
+    if (max_dyn <= 0) return false;
+
+    const int64_t row_bytes = nvec * 16;
+    int64_t R = k.rows_per_stage;
+    if (R == 0) {
+        // About 32 KB per stage, a whole number of rows per team.
+        R = (32 * 1024) / row_bytes;
+        R = R / teams * teams;
+        if (R < 1) R = 1;
+    }
+    if (R > a.M && a.M > 0) R = a.M;
+    const int64_t stage_stride = (R * row_bytes + 127) / 128 * 128;
+    int S = k.stages;
+    if (S == 0) {
+        S = static_cast<int>((96 * 1024) / stage_stride);
+        if (S < 2) S = 2;
+        if (S > 4) S = 4;
+    }
+    if (S < 1 || S > kMaxStages) return false;
+    while (S > 1 && kAlignSlack + kHeaderBytes + S * stage_stride > max_dyn) --S;
+    const int64_t smem = kAlignSlack + kHeaderBytes + S * stage_stride;
+    if (smem > max_dyn || R * row_bytes >= (1 << 20)) return false;
+
+    l.kernel = reinterpret_cast<const void*>(fn);
+    l.threads = threads;
+    l.lanes_per_row = team;
+    l.vecs_per_lane = V;
+    l.rows_per_stage = static_cast<int>(R);
+    l.stages = S;
+    l.smem = static_cast<int>(smem);
+    l.ctas_per_sm = occupancy(l.kernel, threads, l.smem);
+    if (l.ctas_per_sm < 1) return false;
+    l.work_items = (a.M + R - 1) / R;
+    l.grid = persistent_grid(l.work_items, 1, d.sm_count, l.ctas_per_sm, k.max_ctas);
+    l.wait_limit_ns = k.wait_limit_ns > 0 ? k.wait_limit_ns : 1000000000LL;
+    return true;
+}
+
+cudaError_t tma_run(const Args& a, const Launch& l) {
+    Fn fn = reinterpret_cast<Fn>(const_cast<void*>(l.kernel));
+    // The bound is counted in SM cycles; 2.1 cycles per ns is the top SM clock
+    // (2070 MHz), so the wait lasts at least the requested time at any clock.
+    const long long limit = static_cast<long long>(l.wait_limit_ns * 21 / 10);
+    const long long drain = kDrainLimitNs * 21 / 10;
+    const int64_t stage_stride =
+        (static_cast<int64_t>(l.rows_per_stage) * (a.N / kVecElems) * 16 + 127) / 128 * 128;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(l.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(l.threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
+    cfg.stream = a.stream;
+    return cudaLaunchKernelEx(&cfg, fn, static_cast<const uint4*>(a.x),
+                              static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
+                              a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
+                              a.eps, a.offset, l.rows_per_stage, l.stages,
+                              static_cast<int>(stage_stride), limit < 1 ? 1LL : limit, drain);
+}
+
+cudaError_t status_read_and_clear(unsigned int* value) {
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
+    if (e != cudaSuccess) return e;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+        if (e != cudaSuccess) return e;
+    }
+    *value = v;
+    return cudaSuccess;
+}
+
+}  // namespace rmsn

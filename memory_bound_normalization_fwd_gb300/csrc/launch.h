@@ -1,0 +1,86 @@
+// Internal interface between the C ABI front end (api.cu) and the kernel
+// translation units. Host-only declarations; no CUDA types beyond the runtime's.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+// Everything a kernel launch needs, already validated by the front end.
+struct Args {
+    const void* x;
+    const void* w;
+    void* y;
+    float* rstd;
+    int64_t M;
+    int64_t N;
+    float eps;
+    float offset;
+    int dtype;  // 0 bf16, 1 fp16
+    cudaStream_t stream;
+};
+
+// A launch shape chosen by a variant's planner.
+struct Launch {
+    const void* kernel = nullptr;  // the __global__ function (for occupancy queries)
+    int threads = 0;
+    int grid = 0;
+    int lanes_per_row = 0;
+    int vecs_per_lane = 0;
+    int rows_per_stage = 0;
+    int stages = 0;
+    int smem = 0;
+    int ctas_per_sm = 0;
+    int64_t work_items = 0;  // independent units the grid strides over
+    int64_t wait_limit_ns = 0;
+};
+
+// Caller knobs (rmsnorm_options_t), validated by the front end. 0 = planner's choice.
+struct Knobs {
+    int max_ctas = 0;
+    int lanes_per_row = 0;
+    int stages = 0;
+    int rows_per_stage = 0;
+    int64_t wait_limit_ns = 0;
+};
+
+// Device facts, cached per device by the front end.
+struct DeviceInfo {
+    int sm_count = 0;
+    int max_smem_optin = 0;
+};
+
+// Resident CTAs per SM for a kernel at a block size and dynamic smem (cached).
+int occupancy(const void* kernel, int threads, int smem);
+
+// Each variant: choose() fills `l`, or returns false if it cannot take the
+// arguments; run() launches with a filled `l` and returns the launch's error.
+bool warp_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l);
+cudaError_t warp_run(const Args& a, const Launch& l);
+
+bool cta_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l);
+cudaError_t cta_run(const Args& a, const Launch& l);
+
+bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l);
+cudaError_t tma_run(const Args& a, const Launch& l);
+
+bool generic_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l);
+cudaError_t generic_run(const Args& a, const Launch& l);
+
+// Device status word (bounded-wait timeouts): read and clear on the current device.
+cudaError_t status_read_and_clear(unsigned int* value);
+
+// Grid size: min(work items / items per CTA, SMs x resident CTAs), at least 1.
+inline int persistent_grid(int64_t work_items, int64_t items_per_cta, int sm_count,
+                           int ctas_per_sm, int max_ctas) {
+    int64_t need = (work_items + items_per_cta - 1) / items_per_cta;
+    int64_t cap = static_cast<int64_t>(sm_count) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+    if (max_ctas > 0 && max_ctas < cap) cap = max_ctas;
+    int64_t g = need < cap ? need : cap;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace rmsn

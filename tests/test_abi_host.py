@@ -1,0 +1,95 @@
+"""Host-only checks of the C ABI (no GPU needed): the library loads, exports
+every function include/rmsnorm.h declares, and rejects bad arguments on the
+host before any CUDA call. Pointers here are never dereferenced: each case
+fails validation first.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from memory_bound_normalization_fwd_gb300 import binding as B
+from memory_bound_normalization_fwd_gb300 import build as BUILD
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rmsnorm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    BUILD.build()
+    return B.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rmsnorm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared_functions() == sorted(B.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_strerror(lib):
+    assert B.rmsnorm_version() == 1
+    for code in B.STATUS:
+        assert B.rmsnorm_strerror(code) != "unknown status"
+    assert B.rmsnorm_strerror(12345) == "unknown status"
+
+
+def test_options_struct_layout_matches_header():
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct rmsnorm_options \{(.*?)\} rmsnorm_options_t;", text, re.S)
+    fields = re.findall(r"int(32|64)_t\s+(\w+);", body.group(1))
+    assert [n for _, n in fields] == [n for n, _ in B.Options._fields_]
+    assert ctypes.sizeof(B.Options) == 32
+    body = re.search(r"typedef struct rmsnorm_plan \{(.*?)\} rmsnorm_plan_t;", text, re.S)
+    assert [n for n in re.findall(r"int32_t\s+(\w+);", body.group(1))] == \
+        [n for n, _ in B.Plan._fields_]
+
+
+X, W_, Y, R = 0x10000, 0x20000000, 0x30000000, 0x40000000  # never dereferenced
+
+
+def _call(lib, x=X, w=W_, y=Y, r=R, M=4, N=8, eps=1e-6, off=0.0, dt=0, opts=None):
+    return B.rmsnorm_fwd_ex(x, w, y, r, M, N, eps, off, dt, opts, 0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dt=2), -3), (dict(dt=-1), -3),
+    (dict(M=-1), -2), (dict(N=0), -2), (dict(N=-5), -2), (dict(M=1 << 62, N=4), -2),
+    (dict(eps=-1e-6), -4), (dict(eps=float("nan")), -4), (dict(eps=float("inf")), -4),
+    (dict(off=float("nan")), -4), (dict(off=float("inf")), -4),
+    (dict(w=0), -1), (dict(x=0), -1), (dict(y=0), -1), (dict(r=0), -1),
+    (dict(x=X + 1), -10), (dict(y=Y + 1), -10), (dict(w=W_ + 1), -10), (dict(r=R + 2), -10),
+    (dict(y=X + 2), -5),            # y overlaps x without being equal to it
+    (dict(r=X + 16), -5),           # rstd inside x
+    (dict(r=Y + 8), -5),            # rstd inside y
+    (dict(w=Y + 4), -5),            # w inside y
+    (dict(x=Y, w=Y + 2), -5),       # in place, w inside x == y
+])
+def test_validation_errors(lib, kw, code):
+    assert _call(lib, **kw) == code
+    assert B.rmsnorm_last_error() != ""
+
+
+def test_m_zero_is_ok_without_buffers(lib):
+    assert _call(lib, x=0, y=0, r=0, M=0) == 0
+
+
+@pytest.mark.parametrize("field,value", [("variant", 9), ("variant", -1), ("max_ctas", -1),
+                                         ("stages", 9), ("stages", -1), ("wait_limit_ns", -5),
+                                         ("lanes_per_row", -2), ("struct_size", 8)])
+def test_bad_options(lib, field, value):
+    o = B.make_options()
+    setattr(o, field, value)
+    assert _call(lib, opts=o) == -9

@@ -1,0 +1,252 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle
+on the same seeded inputs (y within 1 ulp, rstd within 1e-5 relative).
+
+Covers the five named workloads at full size in the automatic launch
+configuration (the one the benchmark times), every kernel variant on shapes
+that span several tiles with ragged tails, forced small grids (many rows per
+CTA), every lanes-per-row / stage setting the variants take, odd N and
+misaligned pointers, in-place calls, M = 0, zero rows, canaries around every
+buffer, element counts past 2^31, and the bounded-wait timeout path.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_normalization_fwd_gb300 import binding as B
+from memory_bound_normalization_fwd_gb300 import workloads as W
+from parity_util import DeviceCase, compare, oracle_rows, sample_rows, DT
+
+pytestmark = pytest.mark.gpu
+
+
+def _plan(M, N, dtype, case=None, **opts):
+    x = case.x.data_ptr() if case else 0
+    w = case.w.data_ptr() if case else 0
+    y = case.y.data_ptr() if case else 0
+    return B.rmsnorm_plan_info(M, N, DT[dtype], x, w, y, B.make_options(**opts) if opts else None)
+
+
+def _run_and_check(x, w, dtype, eps, offset, rows=None, x_shift=0, y_shift=0, inplace=False,
+                   expect_variant=None, **opts):
+    case = DeviceCase(x, w, dtype, x_shift=x_shift, y_shift=y_shift, inplace=inplace)
+    if expect_variant is not None:
+        assert _plan(x.shape[0], x.shape[1], dtype, case, **opts)["variant"] == expect_variant
+    rc = case.run(eps, offset, **opts)
+    assert rc == 0, B.rmsnorm_last_error()
+    y, r = case.results()
+    case.check_guards()
+    yo, ro = oracle_rows(x, w, eps, offset, dtype, rows)
+    if rows is not None:
+        y, r = y[rows], r[rows]
+    return compare(y, r, yo, ro, dtype, where=f"{dtype} {x.shape} {opts}")
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_workload_full_size_automatic_launch(name):
+    wl = W.WORKLOADS[name]
+    x, w = W.generate(wl)
+    rows = None if wl.M * wl.N <= (1 << 23) else sample_rows(wl.M, 192, seed=1)
+    case = DeviceCase(x, w, wl.dtype)
+    assert case.run(wl.eps, wl.offset) == 0, B.rmsnorm_last_error()
+    y, r = case.results()
+    case.check_guards()
+    # Properties over every row: rstd finite and positive, y finite.
+    assert np.all(np.isfinite(r)) and np.all(r > 0)
+    exp_mask = 0x7F80 if wl.dtype == "bf16" else 0x7C00
+    assert not np.any((y & exp_mask) == exp_mask), "non-finite y"
+    yo, ro = oracle_rows(x, w, wl.eps, wl.offset, wl.dtype, rows)
+    if rows is not None:
+        y, r = y[rows], r[rows]
+    compare(y, r, yo, ro, wl.dtype, where=name)
+    if wl.dtype == "fp16":
+        assert abs(float(np.mean(r)) * wl.x_std - 1.0) < 0.01  # rstd ~ 1/64
+
+
+# ---------------------------------------------------------------- every variant
+
+SHAPES = [(1, 8), (3, 64), (37, 512), (257, 1000), (64, 1024), (17, 2048), (9, 4096),
+          (5, 8192), (130, 520), (11, 16384)]
+
+
+@pytest.mark.parametrize("variant", ["warp", "cta", "tma", "generic"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("M,N", SHAPES)
+def test_variant_parity(variant, dtype, M, N):
+    wl = W.custom(M, N, dtype, seed=M * 131 + N, eps=1e-6, offset=float(N % 2 == 0 and M % 2))
+    x, w = W.generate(wl)
+    try:
+        _plan(M, N, dtype, variant=variant)
+    except B.RMSNormError as e:
+        assert e.status == -8
+        pytest.skip(f"{variant} does not take N={N}")
+    for max_ctas in (0, 2):
+        _run_and_check(x, w, dtype, wl.eps, wl.offset, variant=variant, max_ctas=max_ctas,
+                       expect_variant=variant)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("N", [8, 64, 256, 512, 1000])
+def test_warp_lanes_per_row(G, N):
+    if (N // 8 + G - 1) // G > 4:
+        pytest.skip("more than 4 vectors per lane")
+    wl = W.custom(203, N, "bf16", seed=G + N, offset=1.0)
+    x, w = W.generate(wl)
+    for max_ctas in (0, 1):
+        _run_and_check(x, w, "bf16", wl.eps, wl.offset, variant="warp", lanes_per_row=G,
+                       max_ctas=max_ctas, expect_variant="warp")
+
+
+@pytest.mark.parametrize("T", [64, 128, 256, 512, 1024])
+@pytest.mark.parametrize("N", [512, 4096, 8192])
+def test_cta_threads(T, N):
+    if (N // 8 + T - 1) // T > 4:
+        pytest.skip("more than 4 vectors per thread")
+    wl = W.custom(41, N, "fp16", seed=T + N, x_std=30.0)
+    x, w = W.generate(wl)
+    _run_and_check(x, w, "fp16", wl.eps, wl.offset, variant="cta", lanes_per_row=T, max_ctas=3,
+                   expect_variant="cta")
+
+
+@pytest.mark.parametrize("team,rows,stages", [(16, 1, 1), (16, 7, 2), (32, 16, 3), (64, 5, 4),
+                                              (128, 3, 2), (256, 1, 8), (512, 2, 2),
+                                              (1024, 1, 3), (0, 0, 0)])
+@pytest.mark.parametrize("N", [512, 1000, 4096, 8192])
+def test_tma_team_rows_stages(team, rows, stages, N):
+    wl = W.custom(77, N, "bf16", seed=team + rows + stages + N, outlier_p=0.01)
+    x, w = W.generate(wl)
+    try:
+        _plan(77, N, "bf16", variant="tma", lanes_per_row=team, rows_per_stage=rows, stages=stages)
+    except B.RMSNormError as e:
+        assert e.status == -8
+        pytest.skip("configuration not taken")
+    for max_ctas in (0, 1, 5):
+        _run_and_check(x, w, "bf16", wl.eps, wl.offset, variant="tma", lanes_per_row=team,
+                       rows_per_stage=rows, stages=stages, max_ctas=max_ctas,
+                       expect_variant="tma")
+
+
+# ---------------------------------------------------------------- odd shapes, alignment
+
+@pytest.mark.parametrize("N", [1, 2, 3, 7, 9, 31, 127, 1023, 1025, 4097, 8193])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_odd_n_takes_general_kernel(N, dtype):
+    wl = W.custom(33, N, dtype, seed=N)
+    x, w = W.generate(wl)
+    for max_ctas in (0, 4):
+        _run_and_check(x, w, dtype, wl.eps, wl.offset, max_ctas=max_ctas,
+                       expect_variant="generic")
+
+
+@pytest.mark.parametrize("x_shift,y_shift", [(1, 0), (0, 1), (3, 5), (4, 0)])
+def test_misaligned_pointers(x_shift, y_shift):
+    wl = W.custom(129, 512, "bf16", seed=x_shift * 10 + y_shift)
+    x, w = W.generate(wl)
+    _run_and_check(x, w, "bf16", wl.eps, wl.offset, x_shift=x_shift, y_shift=y_shift,
+                   expect_variant="generic")
+
+
+@pytest.mark.parametrize("variant,N", [("warp", 512), ("warp", 1000), ("cta", 8192),
+                                       ("tma", 512), ("tma", 8192), ("generic", 777),
+                                       ("auto", 4096)])
+def test_in_place(variant, N):
+    wl = W.custom(300, N, "bf16", seed=N + 5)
+    x, w = W.generate(wl)
+    _run_and_check(x, w, "bf16", wl.eps, wl.offset, inplace=True, variant=variant, max_ctas=7)
+
+
+def test_zero_rows_and_eps_zero():
+    # Row 0 all zeros with eps = 0: rstd = inf and y = NaN, as in IEEE fp32 and fp64.
+    wl = W.custom(64, 512, "bf16", seed=3)
+    x, w = W.generate(wl)
+    x[0] = 0
+    x[5] = 0
+    for variant in ("warp", "cta", "tma", "generic"):
+        _run_and_check(x, w, "bf16", 0.0, 0.0, variant=variant)
+    x[5, 7] = 0x3F80  # one 1.0
+    _run_and_check(x, w, "bf16", 1e-5, 1.0)
+
+
+def test_m_zero_launches_nothing():
+    w = torch.ones(512, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.rmsnorm_fwd(0, w.data_ptr(), 0, 0, 0, 512, 1e-6, 0.0, B.BF16, s) == 0
+
+
+def test_torch_convenience_and_streams():
+    wl = W.custom(1000, 1024, "fp16", seed=9)
+    x, w = W.generate(wl)
+    xt = W.to_torch(x, "fp16").cuda()
+    wt = W.to_torch(w, "fp16").cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y, r = B.fwd(xt, wt, eps=wl.eps, offset=wl.offset)
+    s.synchronize()
+    yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "fp16")
+    compare(W.from_torch(y), r.cpu().numpy(), yo, ro, "fp16")
+
+
+# ---------------------------------------------------------------- past 2^31 elements
+
+@pytest.mark.parametrize("variant,N", [("auto", 4096), ("tma", 4096), ("warp", 1024),
+                                       ("generic", 1024)])
+def test_more_than_2_31_elements(variant, N):
+    block = 256
+    M = (1 << 31) // N + 3 * block // 2  # ragged: the last block is cut in half
+    wl = W.custom(block, N, "bf16", seed=N)
+    xb, w = W.generate(wl)
+    reps = (M + block - 1) // block
+    x_dev = W.to_torch(xb, "bf16").cuda().repeat(reps, 1)[:M].contiguous()
+    w_dev = W.to_torch(w, "bf16").cuda()
+    y_dev = torch.empty_like(x_dev)
+    r_dev = torch.empty(M, dtype=torch.float32, device="cuda")
+    opts = B.make_options(variant=variant)
+    rc = B.rmsnorm_fwd_ex(x_dev.data_ptr(), w_dev.data_ptr(), y_dev.data_ptr(), r_dev.data_ptr(),
+                          M, N, wl.eps, 0.0, B.BF16, opts, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, B.rmsnorm_last_error()
+    rows = np.array([0, 1, block - 1, M // 2, (1 << 31) // N, (1 << 31) // N + 1, M - 2, M - 1])
+    y = W.from_torch(y_dev[torch.from_numpy(rows).cuda()])
+    r = r_dev.cpu().numpy()[rows]
+    yo, ro = oracle.rmsnorm_fwd(xb, w, wl.eps, 0.0, "bf16")
+    compare(y, r, yo[rows % block], ro[rows % block], "bf16", where=f"M={M}")
+    del x_dev, y_dev
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- bounded waits
+
+def test_tma_bounded_wait_reports_timeout_and_recovers():
+    # A 1 ns wait bound makes the first stage's wait give up before its copy
+    # lands: the kernel records the timeout, drains its own copies and exits.
+    wl = W.custom(4096, 4096, "bf16", seed=11)
+    x, w = W.generate(wl)
+    case = DeviceCase(x, w, "bf16")
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.rmsnorm_check_device_status(s) == 0
+    assert case.run(wl.eps, wl.offset, variant="tma", wait_limit_ns=1) == 0
+    assert B.rmsnorm_check_device_status(s) == -7
+    assert B.rmsnorm_check_device_status(s) == 0  # the status word was cleared
+    case.check_guards()
+    # The context is still usable and a normal call is exact.
+    assert case.run(wl.eps, wl.offset, variant="tma") == 0
+    assert B.rmsnorm_check_device_status(s) == 0
+    y, r = case.results()
+    yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "bf16")
+    compare(y, r, yo, ro, "bf16")
+
+
+def test_results_are_deterministic():
+    wl = W.WORKLOADS["rmsnorm_16384x512_bf16"]
+    x, w = W.generate(wl)
+    case = DeviceCase(x, w, "bf16")
+    outs = []
+    for _ in range(3):
+        assert case.run(wl.eps, wl.offset) == 0
+        y, r = case.results()
+        outs.append((y.copy(), r.copy()))
+    assert all(np.array_equal(outs[0][0], o[0]) and np.array_equal(outs[0][1], o[1])
+               for o in outs[1:])
