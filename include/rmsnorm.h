@@ -33,7 +33,10 @@
  * anything else takes the general kernel.
  *
  * Streams and errors. Work is enqueued on `stream` (a cudaStream_t; NULL is the
- * legacy default stream) and the call returns at once. The return value
+ * legacy default stream) and the call returns at once. Kernels are launched
+ * with programmatic dependent launch allowed: a kernel may be scheduled while
+ * the previous kernel on the stream finishes, but it touches no memory before
+ * that kernel has completed, so stream order is kept. The return value
  * reports argument errors (checked on the host before any CUDA call) and launch
  * errors only. Kernels with bounded waits record a timeout in a per-device
  * status word instead of hanging; rmsnorm_check_device_status() reads it.
@@ -59,7 +62,7 @@ typedef enum rmsnorm_dtype {
 typedef enum rmsnorm_status {
     RMSNORM_OK = 0,
     RMSNORM_ERR_NULL = -1,           /* a required pointer is NULL */
-    RMSNORM_ERR_SHAPE = -2,          /* M < 0, N <= 0, or M*N*2 bytes overflows int64 */
+    RMSNORM_ERR_SHAPE = -2,          /* M < 0, N <= 0, or x larger than 2^48 bytes */
     RMSNORM_ERR_DTYPE = -3,          /* dtype is not an rmsnorm_dtype_t value */
     RMSNORM_ERR_SCALAR = -4,         /* eps negative or not finite, or offset not finite */
     RMSNORM_ERR_OVERLAP = -5,        /* buffers overlap other than y == x exactly */
@@ -90,14 +93,21 @@ typedef enum rmsnorm_variant {
 } rmsnorm_variant_t;
 
 /* Optional knobs for rmsnorm_fwd_ex(). Zero-initialise, then set fields. */
+/* rmsnorm_options_t.flags bits. */
+#define RMSNORM_FLAG_NO_PDL 1 /* launch without programmatic dependent launch */
+
 typedef struct rmsnorm_options {
     int32_t struct_size;     /* sizeof(rmsnorm_options_t) */
     int32_t variant;         /* rmsnorm_variant_t; 0 = automatic */
     int32_t max_ctas;        /* >0 caps the persistent grid; 0 = SMs x resident CTAs */
-    int32_t lanes_per_row;   /* WARP: lanes per row (1..32, power of two); CTA, TMA and
+    int32_t lanes_per_row;   /* WARP: lanes per row (1..32, power of two); CTA: threads per
+                                row (= per CTA); TMA: threads per row (16..1024);
                                 GENERIC: threads per CTA; 0 = planner's choice */
-    int32_t stages;          /* TMA: pipeline depth (1..8); 0 = planner's choice */
+    int32_t stages;          /* WARP: rows each team keeps in flight (2 or 4); TMA: pipeline
+                                depth (1..8); 0 = planner's choice */
     int32_t rows_per_stage;  /* TMA: rows per stage; 0 = planner's choice */
+    int32_t flags;           /* RMSNORM_FLAG_* bits */
+    int32_t reserved;        /* must be 0 */
     int64_t wait_limit_ns;   /* TMA: bound on each mbarrier wait in ns; 0 = 1 second */
 } rmsnorm_options_t;
 

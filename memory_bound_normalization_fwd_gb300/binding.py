@@ -38,6 +38,7 @@ class Options(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_int32), ("variant", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("lanes_per_row", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("rows_per_stage", ctypes.c_int32),
+                ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64)]
 
 
@@ -98,11 +99,15 @@ def _check(rc: int) -> int:
     return rc
 
 
+FLAG_NO_PDL = 1
+
+
 def make_options(variant: str | int = "auto", max_ctas: int = 0, lanes_per_row: int = 0,
-                 stages: int = 0, rows_per_stage: int = 0, wait_limit_ns: int = 0) -> Options:
+                 stages: int = 0, rows_per_stage: int = 0, wait_limit_ns: int = 0,
+                 pdl: bool = True) -> Options:
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     return Options(ctypes.sizeof(Options), v, max_ctas, lanes_per_row, stages, rows_per_stage,
-                   wait_limit_ns)
+                   0 if pdl else FLAG_NO_PDL, 0, wait_limit_ns)
 
 
 # ---- raw C ABI (integer device addresses) --------------------------------

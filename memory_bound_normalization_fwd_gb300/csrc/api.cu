@@ -62,8 +62,10 @@ int validate(const void* x, const void* w, void* y, float* rstd, int64_t M, int6
     if (M < 0 || N <= 0)
         return fail(RMSNORM_ERR_SHAPE, "need M >= 0 and N > 0 (got M=%lld N=%lld)",
                     static_cast<long long>(M), static_cast<long long>(N));
-    if (M > 0 && (N > INT64_MAX / 2 / M || M > INT64_MAX / 4))
-        return fail(RMSNORM_ERR_SHAPE, "M*N elements overflow (M=%lld N=%lld)",
+    // 2^48 bytes bounds any array a GPU can hold and keeps the kernels' 64-bit
+    // index arithmetic (row block bounds are CTA index * M) far from overflow.
+    if (M > 0 && (N > (int64_t(1) << 47) / M || M > (int64_t(1) << 46)))
+        return fail(RMSNORM_ERR_SHAPE, "x would exceed 2^48 bytes (M=%lld N=%lld)",
                     static_cast<long long>(M), static_cast<long long>(N));
     if (!std::isfinite(eps) || eps < 0.f)
         return fail(RMSNORM_ERR_SCALAR, "eps must be finite and >= 0 (got %g)", eps);
@@ -98,9 +100,11 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
         return fail(RMSNORM_ERR_OPTIONS, "options.variant %d is not a rmsnorm_variant_t",
                     o->variant);
     if (o->max_ctas < 0 || o->lanes_per_row < 0 || o->rows_per_stage < 0 || o->stages < 0 ||
-        o->stages > 8 || o->wait_limit_ns < 0)
+        o->stages > 8 || o->wait_limit_ns < 0 || o->reserved != 0 ||
+        (o->flags & ~RMSNORM_FLAG_NO_PDL) != 0)
         return fail(RMSNORM_ERR_OPTIONS, "options fields out of range");
     *variant = o->variant;
+    k->flags = o->flags;
     k->max_ctas = o->max_ctas;
     k->lanes_per_row = o->lanes_per_row;
     k->stages = o->stages;
@@ -193,6 +197,7 @@ extern "C" int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd
     int chosen = 0;
     rc = plan(a, d, variant, k, l, &chosen);
     if (rc != RMSNORM_OK) return rc;
+    l.pdl = (k.flags & RMSNORM_FLAG_NO_PDL) == 0;
     e = run(chosen, a, l);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
     return RMSNORM_OK;

@@ -105,6 +105,27 @@ __device__ __forceinline__ void weights8(const uint4& v, float offset, float* s)
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
 
+// y = (x * r) * s for 8 elements, with the 8 scales read as two float4 (from
+// shared memory).
+template <int DT>
+__device__ __forceinline__ uint4 scale8(const uint4& v, float r, const float4& s0,
+                                        const float4& s1) {
+    const float s[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    return scale8<DT>(v, r, s);
+}
+
+// Programmatic dependent launch. Every kernel is launched with programmatic
+// stream serialisation allowed, so it may be scheduled while the previous
+// kernel on the stream is finishing. pdl_wait() blocks until that kernel has
+// completed and its memory is visible; it comes before the first global
+// memory access. pdl_launch_dependents() lets the next kernel be scheduled
+// into SM slots as this one's CTAs retire. Without a programmatic dependency
+// both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // The per-row scalar step: mean of squares, plus eps, rsqrt.
 __device__ __forceinline__ float row_rstd(float sumsq, float n, float eps) {
     return rsqrtf(__fdiv_rn(sumsq, n) + eps);

@@ -6,8 +6,9 @@
 // (skillmd, Row-Parallel Design: load the row in fp32, sum of squares, rsqrt,
 // multiply by the weight, store) sized for large hidden dimensions, inside
 // the persistent loop of the TileGym issue #169 kernel (weight loaded once
-// per program, programs stride over rows). The next row is loaded before the
-// current row's reduction, so two rows per thread are in flight.
+// per program). Each CTA owns one contiguous block of rows (block sizes differ
+// by at most one row). The next row is loaded before the current row's
+// reduction, so two rows per thread are in flight.
 #include "common.cuh"
 #include "launch.h"
 
@@ -27,6 +28,8 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     const int lane = tid & 31;
     const int wid = tid >> 5;
 
+    pdl_wait();
+    pdl_launch_dependents();
     float s[V][kVecElems];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -36,24 +39,26 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         weights8<DT>(wv, offset, s[v]);
     }
 
-    int64_t row = blockIdx.x;
+    // This CTA's rows: a contiguous block, the blocks of all CTAs differing by at most one row.
+    const int64_t r_end = static_cast<int64_t>(blockIdx.x + 1) * M / gridDim.x;
+    int64_t row = static_cast<int64_t>(blockIdx.x) * M / gridDim.x;
     uint4 cur[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = v * THREADS + tid;
         cur[v] = make_uint4(0u, 0u, 0u, 0u);
-        if (row < M && c < nvec) cur[v] = ld_stream(x + row * nvec + c);
+        if (row < r_end && c < nvec) cur[v] = ld_stream(x + row * nvec + c);
     }
 
     int parity = 0;
-    for (; row < M; row += gridDim.x) {
-        const int64_t nrow = row + gridDim.x;
+    for (; row < r_end; ++row) {
+        const int64_t nrow = row + 1;
         uint4 nxt[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = v * THREADS + tid;
             nxt[v] = make_uint4(0u, 0u, 0u, 0u);
-            if (nrow < M && c < nvec) nxt[v] = ld_stream(x + nrow * nvec + c);
+            if (nrow < r_end && c < nvec) nxt[v] = ld_stream(x + nrow * nvec + c);
         }
 
         float ss = 0.f;
@@ -125,12 +130,8 @@ bool cta_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
 
 cudaError_t cta_run(const Args& a, const Launch& l) {
     Fn fn = reinterpret_cast<Fn>(const_cast<void*>(l.kernel));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(l.grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(l.threads));
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = a.stream;
-    return cudaLaunchKernelEx(&cfg, fn, static_cast<const uint4*>(a.x),
+    LaunchCfg c(l, a.stream, l.pdl);
+    return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
                               a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
                               a.eps, a.offset);

@@ -23,7 +23,10 @@ generic_rows_kernel(const uint16_t* x, const uint16_t* __restrict__ w, uint16_t*
     __shared__ float part[2][kWarps];
     const int tid = threadIdx.x;
     int parity = 0;
-    for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t r_end = static_cast<int64_t>(blockIdx.x + 1) * M / gridDim.x;
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * M / gridDim.x; row < r_end; ++row) {
         const uint16_t* xr = x + row * N;
         float ss = 0.f;
         for (int64_t j = tid; j < N; j += THREADS) {
@@ -88,12 +91,8 @@ bool generic_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& 
 
 cudaError_t generic_run(const Args& a, const Launch& l) {
     Fn fn = reinterpret_cast<Fn>(const_cast<void*>(l.kernel));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(l.grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(l.threads));
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = a.stream;
-    return cudaLaunchKernelEx(&cfg, fn, static_cast<const uint16_t*>(a.x),
+    LaunchCfg c(l, a.stream, l.pdl);
+    return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint16_t*>(a.x),
                               static_cast<const uint16_t*>(a.w), static_cast<uint16_t*>(a.y),
                               a.rstd, a.M, a.N, static_cast<float>(a.N), a.eps, a.offset);
 }

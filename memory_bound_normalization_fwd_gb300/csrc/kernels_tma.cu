@@ -117,7 +117,11 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     const int team = tid / TEAM;
     const int t = tid % TEAM;
     const int R = rows_per_stage;
-    const int64_t ntiles = (M + R - 1) / R;
+    // This CTA's rows: a contiguous block (block sizes differ by at most one
+    // row), taken R rows per stage: local chunk k is rows r_begin + k*R onwards.
+    const int64_t r_begin = static_cast<int64_t>(blockIdx.x) * M / gridDim.x;
+    const int64_t r_end = static_cast<int64_t>(blockIdx.x + 1) * M / gridDim.x;
+    const int64_t nchunks = (r_end - r_begin + R - 1) / R;
     // Round the dynamic shared memory base up to 128 bytes (the launch adds
     // kAlignSlack bytes for this), so barriers and stages are aligned whatever
     // the static shared memory in front of it.
@@ -126,6 +130,11 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     const uint32_t bars = smem_u32(base);
     unsigned char* buf = base + kHeaderBytes;
 
+    if (tid == 0) {
+        for (int st = 0; st < stages; ++st) mbar_init(bars + 8 * st, 1);
+        fence_mbar_init();
+    }
+    pdl_wait();  // no global memory is touched before the previous kernel completes
     float s[V][kVecElems];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -134,20 +143,14 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         if (c < nvec) wv = __ldg(w + c);
         weights8<DT>(wv, offset, s[v]);
     }
-
-    if (tid == 0) {
-        for (int st = 0; st < stages; ++st) mbar_init(bars + 8 * st, 1);
-        fence_mbar_init();
-    }
     __syncthreads();
 
-    // Local tile k of this CTA is tile blockIdx.x + k * gridDim.x, in stage k % stages.
+    // Local chunk k goes to stage k % stages.
     auto issue = [&](int64_t k) {
-        const int64_t tile = blockIdx.x + k * gridDim.x;
-        if (tile >= ntiles) return;
+        if (k >= nchunks) return;
         const int st = static_cast<int>(k % stages);
-        const int64_t r0 = tile * R;
-        const int64_t rows = (M - r0) < R ? (M - r0) : R;
+        const int64_t r0 = r_begin + k * R;
+        const int64_t rows = (r_end - r0) < R ? (r_end - r0) : R;
         const uint32_t bytes = static_cast<uint32_t>(rows * nvec * 16);
         mbar_arrive_expect_tx(bars + 8 * st, bytes);
         bulk_g2s(smem_u32(buf + static_cast<int64_t>(st) * stage_stride), x + r0 * nvec, bytes,
@@ -156,11 +159,12 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     if (tid == 0) {
         for (int k = 0; k < stages; ++k) issue(k);
     }
+    pdl_launch_dependents();
 
     int pp = 0;
     int64_t k = 0;
     bool aborted = false;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    for (; k < nchunks; ++k) {
         const int st = static_cast<int>(k % stages);
         const uint32_t phase = static_cast<uint32_t>((k / stages) & 1);
         const bool ok = mbar_wait_bounded(bars + 8 * st, phase, limit_cycles);
@@ -169,8 +173,8 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
             break;
         }
         const uint4* sx = reinterpret_cast<const uint4*>(buf + static_cast<int64_t>(st) * stage_stride);
-        const int64_t r0 = tile * R;
-        const int rows = static_cast<int>((M - r0) < R ? (M - r0) : R);
+        const int64_t r0 = r_begin + k * R;
+        const int rows = static_cast<int>((r_end - r0) < R ? (r_end - r0) : R);
         const int iters = (rows + kTeams - 1) / kTeams;  // CTA-uniform
         for (int i = 0; i < iters; ++i) {
             const int rr = i * kTeams + team;
@@ -213,8 +217,7 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         atomicOr(&g_status, 1u);
         // Copies for local tiles k .. k + stages - 1 may still be in flight into
         // this CTA's shared memory: wait for them before the CTA retires.
-        for (int64_t j = k; j < k + stages; ++j) {
-            if (blockIdx.x + j * gridDim.x >= ntiles) break;
+        for (int64_t j = k; j < k + stages && j < nchunks; ++j) {
             mbar_wait_bounded(bars + 8 * static_cast<int>(j % stages),
                               static_cast<uint32_t>((j / stages) & 1), drain_cycles);
         }
@@ -292,21 +295,18 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     const int64_t row_bytes = nvec * 16;
     int64_t R = k.rows_per_stage;
     if (R == 0) {
-        // About 32 KB per stage, a whole number of rows per team.
-        R = (32 * 1024) / row_bytes;
-        R = R / teams * teams;
+        // About 16 KB per stage (measured best on GB300 from 1 KB to 16 KB rows),
+        // a whole number of rows per team when a stage holds several rows.
+        R = (16 * 1024) / row_bytes;
+        if (R > teams) R = R / teams * teams;
         if (R < 1) R = 1;
     }
     if (R > a.M && a.M > 0) R = a.M;
     const int64_t stage_stride = (R * row_bytes + 127) / 128 * 128;
-    int S = k.stages;
-    if (S == 0) {
-        S = static_cast<int>((96 * 1024) / stage_stride);
-        if (S < 2) S = 2;
-        if (S > 4) S = 4;
-    }
+    int S = k.stages > 0 ? k.stages : 2;
     if (S < 1 || S > kMaxStages) return false;
-    while (S > 1 && kAlignSlack + kHeaderBytes + S * stage_stride > max_dyn) --S;
+    if (k.stages == 0)
+        while (S > 1 && kAlignSlack + kHeaderBytes + S * stage_stride > max_dyn) --S;
     const int64_t smem = kAlignSlack + kHeaderBytes + S * stage_stride;
     if (smem > max_dyn || R * row_bytes >= (1 << 20)) return false;
 
@@ -333,12 +333,8 @@ cudaError_t tma_run(const Args& a, const Launch& l) {
     const long long drain = kDrainLimitNs * 21 / 10;
     const int64_t stage_stride =
         (static_cast<int64_t>(l.rows_per_stage) * (a.N / kVecElems) * 16 + 127) / 128 * 128;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(l.grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(l.threads));
-    cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
-    cfg.stream = a.stream;
-    return cudaLaunchKernelEx(&cfg, fn, static_cast<const uint4*>(a.x),
+    LaunchCfg c(l, a.stream, l.pdl);
+    return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
                               a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
                               a.eps, a.offset, l.rows_per_stage, l.stages,

@@ -9,9 +9,14 @@
 //
 // Per row: 16-byte evict-first loads, fp32 sum of squares, a __shfl_xor_sync
 // butterfly over the G lanes, rsqrt(sum/N + eps), rstd store by the team's
-// first lane, then y = (x * rstd) * (offset + w) with 16-byte stores. The next
-// row of the team is loaded before the current one is reduced, so two rows per
-// thread are in flight.
+// first lane, then y = (x * rstd) * (offset + w) with 16-byte stores. Each
+// team keeps D rows in flight in a register ring: a row's slot is refilled
+// with the team's row D passes ahead as soon as the row is stored.
+//
+// (offset + w) is computed once per CTA in fp32 into shared memory (N * 4
+// bytes), which keeps registers for rows in flight. Each CTA owns one
+// contiguous block of rows (block sizes differ by at most one row), so the
+// work is balanced across SMs and each CTA streams through consecutive rows.
 #include "common.cuh"
 #include "launch.h"
 
@@ -20,78 +25,87 @@ namespace {
 
 constexpr int kWarps = 8;  // 256 threads per CTA
 
-template <int DT, int G, int V>
+template <int DT, int G, int V, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
                  int64_t M, int nvec, float n, float eps, float offset) {
+    extern __shared__ float4 sw[];  // 2 float4 of (offset + w) per 16-byte vector of w
     constexpr int kTeams = 32 / G;  // rows per warp per pass
+    constexpr int kPass = kWarps * kTeams;  // rows per CTA per pass
     const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
     const int sub = lane & (G - 1);
-    const int64_t warp = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps * kTeams;
-    const int64_t first = warp * kTeams;  // this warp's first team row in pass 0
     const int team = lane / G;
+    // This CTA's rows: a contiguous block, the blocks of all CTAs differing by at most one row.
+    const int64_t r_begin = static_cast<int64_t>(blockIdx.x) * M / gridDim.x;
+    const int64_t r_end = static_cast<int64_t>(blockIdx.x + 1) * M / gridDim.x;
+    const int64_t first0 = r_begin + wid * kTeams;  // team 0 of this warp, pass 0
 
-    // offset + w for this lane's columns, fp32, loaded once.
-    float s[V][kVecElems];
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-        const int c = v * G + sub;
-        uint4 wv = make_uint4(0u, 0u, 0u, 0u);
-        if (c < nvec) wv = __ldg(w + c);
-        weights8<DT>(wv, offset, s[v]);
+    pdl_wait();
+    for (int i = threadIdx.x; i < nvec; i += kWarps * 32) {
+        float s[kVecElems];
+        weights8<DT>(__ldg(w + i), offset, s);
+        sw[2 * i] = make_float4(s[0], s[1], s[2], s[3]);
+        sw[2 * i + 1] = make_float4(s[4], s[5], s[6], s[7]);
     }
+    __syncthreads();
+    pdl_launch_dependents();
 
-    uint4 cur[V];
-    {
-        const int64_t row = first + team;
+    uint4 buf[D][V];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+        const int64_t row = first0 + d * kPass + team;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = v * G + sub;
-            cur[v] = make_uint4(0u, 0u, 0u, 0u);
-            if (row < M && c < nvec) cur[v] = ld_stream(x + row * nvec + c);
+            buf[d][v] = make_uint4(0u, 0u, 0u, 0u);
+            if (row < r_end && c < nvec) buf[d][v] = ld_stream(x + row * nvec + c);
         }
     }
 
-    // The loop bound is warp-uniform (first team's row), so every lane takes
-    // part in every shuffle; teams past M compute on zeros and store nothing.
-    for (int64_t base = first; base < M; base += stride) {
-        const int64_t row = base + team;
-        const int64_t nrow = row + stride;
-        uint4 nxt[V];
+    for (int64_t k0 = 0; first0 + k0 * kPass < r_end; k0 += D) {
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
-            const int c = v * G + sub;
-            nxt[v] = make_uint4(0u, 0u, 0u, 0u);
-            if (nrow < M && c < nvec) nxt[v] = ld_stream(x + nrow * nvec + c);
-        }
-
-        float ss = 0.f;
+        for (int d = 0; d < D; ++d) {
+            const int64_t row0 = first0 + (k0 + d) * kPass;
+            // Warp-uniform: every lane takes part in every shuffle; teams past the
+            // block's end reduce zeros and store nothing.
+            if (row0 < r_end) {
+                const int64_t row = row0 + team;
+                float ss = 0.f;
 #pragma unroll
-        for (int v = 0; v < V; ++v) ss = sumsq8<DT>(cur[v], ss);
+                for (int v = 0; v < V; ++v) ss = sumsq8<DT>(buf[d][v], ss);
 #pragma unroll
-        for (int off = G / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-
-        if (row < M) {
-            const float r = row_rstd(ss, n, eps);
-            if (sub == 0) rstd[row] = r;
+                for (int off = G / 2; off > 0; off >>= 1)
+                    ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (row < r_end) {
+                    const float r = row_rstd(ss, n, eps);
+                    if (sub == 0) rstd[row] = r;
 #pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const int c = v * G + sub;
-                if (c < nvec) st_stream(y + row * nvec + c, scale8<DT>(cur[v], r, s[v]));
+                    for (int v = 0; v < V; ++v) {
+                        const int c = v * G + sub;
+                        if (c < nvec)
+                            st_stream(y + row * nvec + c,
+                                      scale8<DT>(buf[d][v], r, sw[2 * c], sw[2 * c + 1]));
+                    }
+                }
+                const int64_t nrow = row + D * kPass;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const int c = v * G + sub;
+                    buf[d][v] = make_uint4(0u, 0u, 0u, 0u);
+                    if (nrow < r_end && c < nvec) buf[d][v] = ld_stream(x + nrow * nvec + c);
+                }
             }
         }
-#pragma unroll
-        for (int v = 0; v < V; ++v) cur[v] = nxt[v];
     }
 }
 
 using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, float, float, float);
 
-template <int DT>
-Fn pick(int G, int V) {
+template <int DT, int D>
+Fn pick_d(int G, int V) {
 #define RMSN_CASE(g, v) \
-    if (G == g && V == v) return warp_rows_kernel<DT, g, v>;
+    if (G == g && V == v) return warp_rows_kernel<DT, g, v, D>;
     RMSN_CASE(1, 1) RMSN_CASE(1, 2) RMSN_CASE(1, 4)
     RMSN_CASE(2, 1) RMSN_CASE(2, 2) RMSN_CASE(2, 4)
     RMSN_CASE(4, 1) RMSN_CASE(4, 2) RMSN_CASE(4, 4)
@@ -100,6 +114,11 @@ Fn pick(int G, int V) {
     RMSN_CASE(32, 1) RMSN_CASE(32, 2) RMSN_CASE(32, 4)
 #undef RMSN_CASE
     return nullptr;
+}
+
+template <int DT>
+Fn pick(int G, int V, int D) {
+    return D == 4 ? pick_d<DT, 4>(G, V) : D == 2 ? pick_d<DT, 2>(G, V) : nullptr;
 }
 
 int next_pow2(int v) {
@@ -127,14 +146,16 @@ bool warp_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) 
         G = 32;
         V = nvec <= 64 ? 2 : 4;
     }
-    Fn fn = a.dtype == kBF16 ? pick<kBF16>(G, V) : pick<kFP16>(G, V);
+    const int D = k.stages > 0 ? k.stages : 2;
+    Fn fn = a.dtype == kBF16 ? pick<kBF16>(G, V, D) : pick<kFP16>(G, V, D);
     if (!fn) return false;
     l.kernel = reinterpret_cast<const void*>(fn);
     l.threads = kWarps * 32;
     l.lanes_per_row = G;
     l.vecs_per_lane = V;
-    l.smem = 0;
-    l.ctas_per_sm = occupancy(l.kernel, l.threads, 0);
+    l.stages = D;
+    l.smem = static_cast<int>(nvec * 32);
+    l.ctas_per_sm = occupancy(l.kernel, l.threads, l.smem);
     l.work_items = a.M;
     l.grid = persistent_grid(a.M, static_cast<int64_t>(kWarps) * (32 / G), d.sm_count,
                              l.ctas_per_sm, k.max_ctas);
@@ -143,12 +164,8 @@ bool warp_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) 
 
 cudaError_t warp_run(const Args& a, const Launch& l) {
     Fn fn = reinterpret_cast<Fn>(const_cast<void*>(l.kernel));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(l.grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(l.threads));
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = a.stream;
-    return cudaLaunchKernelEx(&cfg, fn, static_cast<const uint4*>(a.x),
+    LaunchCfg c(l, a.stream, l.pdl);
+    return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
                               a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
                               a.eps, a.offset);

@@ -34,10 +34,12 @@ struct Launch {
     int ctas_per_sm = 0;
     int64_t work_items = 0;  // independent units the grid strides over
     int64_t wait_limit_ns = 0;
+    bool pdl = true;
 };
 
 // Caller knobs (rmsnorm_options_t), validated by the front end. 0 = planner's choice.
 struct Knobs {
+    int flags = 0;  // RMSNORM_FLAG_*
     int max_ctas = 0;
     int lanes_per_row = 0;
     int stages = 0;
@@ -82,5 +84,22 @@ inline int persistent_grid(int64_t work_items, int64_t items_per_cta, int sm_cou
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch configuration shared by every variant: programmatic stream
+// serialisation (PDL) unless the caller turned it off.
+struct LaunchCfg {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    LaunchCfg(const Launch& l, cudaStream_t stream, bool pdl) {
+        cfg.gridDim = dim3(static_cast<unsigned>(l.grid));
+        cfg.blockDim = dim3(static_cast<unsigned>(l.threads));
+        cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
+        cfg.stream = stream;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+    }
+};
 
 }  // namespace rmsn

@@ -51,7 +51,7 @@ def test_options_struct_layout_matches_header():
     body = re.search(r"typedef struct rmsnorm_options \{(.*?)\} rmsnorm_options_t;", text, re.S)
     fields = re.findall(r"int(32|64)_t\s+(\w+);", body.group(1))
     assert [n for _, n in fields] == [n for n, _ in B.Options._fields_]
-    assert ctypes.sizeof(B.Options) == 32
+    assert ctypes.sizeof(B.Options) == 40
     body = re.search(r"typedef struct rmsnorm_plan \{(.*?)\} rmsnorm_plan_t;", text, re.S)
     assert [n for n in re.findall(r"int32_t\s+(\w+);", body.group(1))] == \
         [n for n, _ in B.Plan._fields_]
@@ -88,7 +88,8 @@ def test_m_zero_is_ok_without_buffers(lib):
 
 @pytest.mark.parametrize("field,value", [("variant", 9), ("variant", -1), ("max_ctas", -1),
                                          ("stages", 9), ("stages", -1), ("wait_limit_ns", -5),
-                                         ("lanes_per_row", -2), ("struct_size", 8)])
+                                         ("lanes_per_row", -2), ("struct_size", 8),
+                                         ("flags", 2), ("reserved", 1)])
 def test_bad_options(lib, field, value):
     o = B.make_options()
     setattr(o, field, value)
