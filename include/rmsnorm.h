@@ -94,7 +94,9 @@ typedef enum rmsnorm_variant {
 
 /* Optional knobs for rmsnorm_fwd_ex(). Zero-initialise, then set fields. */
 /* rmsnorm_options_t.flags bits. */
-#define RMSNORM_FLAG_NO_PDL 1 /* launch without programmatic dependent launch */
+#define RMSNORM_FLAG_NO_PDL 1       /* launch without programmatic dependent launch */
+#define RMSNORM_FLAG_BLOCKED_ROWS 2 /* each CTA takes one contiguous block of rows
+                                       (default: CTAs stride over rows in passes) */
 
 typedef struct rmsnorm_options {
     int32_t struct_size;     /* sizeof(rmsnorm_options_t) */
@@ -103,7 +105,7 @@ typedef struct rmsnorm_options {
     int32_t lanes_per_row;   /* WARP: lanes per row (1..32, power of two); CTA: threads per
                                 row (= per CTA); TMA: threads per row (16..1024);
                                 GENERIC: threads per CTA; 0 = planner's choice */
-    int32_t stages;          /* WARP: rows each team keeps in flight (2 or 4); TMA: pipeline
+    int32_t stages;          /* WARP: rows each team keeps in flight (1, 2 or 4); TMA: pipeline
                                 depth (1..8); 0 = planner's choice */
     int32_t rows_per_stage;  /* TMA: rows per stage; 0 = planner's choice */
     int32_t flags;           /* RMSNORM_FLAG_* bits */

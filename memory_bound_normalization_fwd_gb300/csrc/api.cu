@@ -101,7 +101,7 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
                     o->variant);
     if (o->max_ctas < 0 || o->lanes_per_row < 0 || o->rows_per_stage < 0 || o->stages < 0 ||
         o->stages > 8 || o->wait_limit_ns < 0 || o->reserved != 0 ||
-        (o->flags & ~RMSNORM_FLAG_NO_PDL) != 0)
+        (o->flags & ~(RMSNORM_FLAG_NO_PDL | RMSNORM_FLAG_BLOCKED_ROWS)) != 0)
         return fail(RMSNORM_ERR_OPTIONS, "options fields out of range");
     *variant = o->variant;
     k->flags = o->flags;
@@ -113,9 +113,11 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
     return RMSNORM_OK;
 }
 
-// Chooses the variant. The automatic choice: the warp-team kernel for rows up
-// to 1024 columns, the TMA-staged kernel for longer rows, each only when x, w
-// and y are 16-byte aligned and N % 8 == 0; the general kernel otherwise.
+// Chooses the variant. The automatic choice, when x, w and y are 16-byte
+// aligned and N % 8 == 0: the warp-team kernel for rows up to 768 columns, the
+// TMA-staged kernel for longer rows (measured on GB300: warp team ahead at
+// N = 512, TMA ahead from N = 1000 up), the register CTA kernel if the TMA
+// kernel cannot take the row; the general kernel otherwise.
 int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch& l,
          int* chosen) {
     bool ok = false;
@@ -125,13 +127,17 @@ int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch
         case RMSNORM_VARIANT_TMA: ok = tma_choose(a, d, k, l); break;
         case RMSNORM_VARIANT_GENERIC: ok = generic_choose(a, d, k, l); break;
         default:
-            if (a.N <= 1024 && warp_choose(a, d, k, l)) {
+            if (a.N <= 768 && warp_choose(a, d, k, l)) {
                 variant = RMSNORM_VARIANT_WARP;
                 ok = true;
-            } else if (a.N > 1024 && cta_choose(a, d, k, l)) {
+            } else if ((l = Launch{}, tma_choose(a, d, k, l))) {
+                variant = RMSNORM_VARIANT_TMA;
+                ok = true;
+            } else if ((l = Launch{}, cta_choose(a, d, k, l))) {
                 variant = RMSNORM_VARIANT_CTA;
                 ok = true;
             } else {
+                l = Launch{};
                 variant = RMSNORM_VARIANT_GENERIC;
                 ok = generic_choose(a, d, k, l);
             }
@@ -198,6 +204,7 @@ extern "C" int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd
     rc = plan(a, d, variant, k, l, &chosen);
     if (rc != RMSNORM_OK) return rc;
     l.pdl = (k.flags & RMSNORM_FLAG_NO_PDL) == 0;
+    l.blocked = (k.flags & RMSNORM_FLAG_BLOCKED_ROWS) != 0;
     e = run(chosen, a, l);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
     return RMSNORM_OK;

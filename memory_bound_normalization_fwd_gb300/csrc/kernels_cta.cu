@@ -6,8 +6,8 @@
 // (skillmd, Row-Parallel Design: load the row in fp32, sum of squares, rsqrt,
 // multiply by the weight, store) sized for large hidden dimensions, inside
 // the persistent loop of the TileGym issue #169 kernel (weight loaded once
-// per program). Each CTA owns one contiguous block of rows (block sizes differ
-// by at most one row). The next row is loaded before the current row's
+// per program, programs stride over rows; or, as an option, one contiguous
+// block of rows per CTA). The next row is loaded before the current row's
 // reduction, so two rows per thread are in flight.
 #include "common.cuh"
 #include "launch.h"
@@ -18,7 +18,7 @@ namespace {
 template <int DT, int THREADS, int V>
 __global__ void __launch_bounds__(THREADS)
 cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
-                int64_t M, int nvec, float n, float eps, float offset) {
+                int64_t M, int nvec, float n, float eps, float offset, int blocked) {
     constexpr int kWarps = THREADS / 32;
     // Two slots per warp, alternating by row parity, so one barrier per row suffices:
     // slot p is rewritten two rows later, after every thread has passed the
@@ -39,9 +39,11 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         weights8<DT>(wv, offset, s[v]);
     }
 
-    // This CTA's rows: a contiguous block, the blocks of all CTAs differing by at most one row.
-    const int64_t r_end = static_cast<int64_t>(blockIdx.x + 1) * M / gridDim.x;
-    int64_t row = static_cast<int64_t>(blockIdx.x) * M / gridDim.x;
+    // Row order. Strided (default): rows blockIdx.x, + gridDim.x, ... Blocked: one
+    // contiguous block per CTA, the blocks differing by at most one row.
+    const int64_t r_end = blocked ? static_cast<int64_t>(blockIdx.x + 1) * M / gridDim.x : M;
+    const int64_t step = blocked ? 1 : gridDim.x;
+    int64_t row = blocked ? static_cast<int64_t>(blockIdx.x) * M / gridDim.x : blockIdx.x;
     uint4 cur[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -51,8 +53,8 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     }
 
     int parity = 0;
-    for (; row < r_end; ++row) {
-        const int64_t nrow = row + 1;
+    for (; row < r_end; row += step) {
+        const int64_t nrow = row + step;
         uint4 nxt[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) {
@@ -84,7 +86,8 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     }
 }
 
-using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, float, float, float);
+using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, float, float, float,
+                    int);
 
 template <int DT>
 Fn pick(int T, int V) {
@@ -134,7 +137,7 @@ cudaError_t cta_run(const Args& a, const Launch& l) {
     return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
                               a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
-                              a.eps, a.offset);
+                              a.eps, a.offset, l.blocked ? 1 : 0);
 }
 
 }  // namespace rmsn

@@ -25,8 +25,7 @@ generic_rows_kernel(const uint16_t* x, const uint16_t* __restrict__ w, uint16_t*
     int parity = 0;
     pdl_wait();
     pdl_launch_dependents();
-    const int64_t r_end = static_cast<int64_t>(blockIdx.x + 1) * M / gridDim.x;
-    for (int64_t row = static_cast<int64_t>(blockIdx.x) * M / gridDim.x; row < r_end; ++row) {
+    for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
         const uint16_t* xr = x + row * N;
         float ss = 0.f;
         for (int64_t j = tid; j < N; j += THREADS) {

@@ -106,7 +106,8 @@ template <int DT, int THREADS, int TEAM, int V>
 __global__ void __launch_bounds__(THREADS)
 tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
                 int64_t M, int nvec, float n, float eps, float offset, int rows_per_stage,
-                int stages, int stage_stride, long long limit_cycles, long long drain_cycles) {
+                int stages, int stage_stride, long long limit_cycles, long long drain_cycles,
+                int blocked) {
     constexpr int kTeams = THREADS / TEAM;
     constexpr int kLanes = TEAM < 32 ? TEAM : 32;        // lanes in the shuffle step
     constexpr int kTeamWarps = TEAM > 32 ? TEAM / 32 : 1;  // warps per team
@@ -117,11 +118,18 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     const int team = tid / TEAM;
     const int t = tid % TEAM;
     const int R = rows_per_stage;
-    // This CTA's rows: a contiguous block (block sizes differ by at most one
-    // row), taken R rows per stage: local chunk k is rows r_begin + k*R onwards.
-    const int64_t r_begin = static_cast<int64_t>(blockIdx.x) * M / gridDim.x;
-    const int64_t r_end = static_cast<int64_t>(blockIdx.x + 1) * M / gridDim.x;
-    const int64_t nchunks = (r_end - r_begin + R - 1) / R;
+    // Chunks of R consecutive rows. Strided (default): this CTA takes chunks
+    // blockIdx.x, + gridDim.x, ... of x. Blocked: this CTA owns one contiguous
+    // block of rows (block sizes differ by at most one row) and cuts it into
+    // chunks. Local chunk k starts at row chunk_row(k) and ends before chunk_end(k).
+    const int64_t r_begin = blocked ? static_cast<int64_t>(blockIdx.x) * M / gridDim.x : 0;
+    const int64_t r_end = blocked ? static_cast<int64_t>(blockIdx.x + 1) * M / gridDim.x : M;
+    const int64_t ntiles = (M + R - 1) / R;
+    const int64_t nchunks = blocked ? (r_end - r_begin + R - 1) / R
+                                    : (ntiles > blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0);
+    auto chunk_row = [&](int64_t k) -> int64_t {
+        return blocked ? r_begin + k * R : (blockIdx.x + k * gridDim.x) * R;
+    };
     // Round the dynamic shared memory base up to 128 bytes (the launch adds
     // kAlignSlack bytes for this), so barriers and stages are aligned whatever
     // the static shared memory in front of it.
@@ -149,7 +157,7 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     auto issue = [&](int64_t k) {
         if (k >= nchunks) return;
         const int st = static_cast<int>(k % stages);
-        const int64_t r0 = r_begin + k * R;
+        const int64_t r0 = chunk_row(k);
         const int64_t rows = (r_end - r0) < R ? (r_end - r0) : R;
         const uint32_t bytes = static_cast<uint32_t>(rows * nvec * 16);
         mbar_arrive_expect_tx(bars + 8 * st, bytes);
@@ -173,7 +181,7 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
             break;
         }
         const uint4* sx = reinterpret_cast<const uint4*>(buf + static_cast<int64_t>(st) * stage_stride);
-        const int64_t r0 = r_begin + k * R;
+        const int64_t r0 = chunk_row(k);
         const int rows = static_cast<int>((r_end - r0) < R ? (r_end - r0) : R);
         const int iters = (rows + kTeams - 1) / kTeams;  // CTA-uniform
         for (int i = 0; i < iters; ++i) {
@@ -225,7 +233,7 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
 }
 
 using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, float, float, float,
-                    int, int, int, long long, long long);
+                    int, int, int, long long, long long, int);
 
 template <int DT>
 Fn pick(int team, int V) {
@@ -278,8 +286,11 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     const int64_t nvec = a.N / kVecElems;
     int team = k.lanes_per_row;
     if (team == 0) {
-        team = next_pow2((nvec + 3) / 4);
+        // Four vectors per thread (two for rows of 8192+ columns), 16..1024
+        // threads per row; measured best on GB300 for 1000 <= N <= 8192.
+        team = nvec >= 1024 ? next_pow2((nvec + 1) / 2) : next_pow2((nvec + 3) / 4);
         if (team < 16) team = 16;
+        if (team > 1024) team = 1024;
     }
     if (team < 16 || team > 1024 || (team & (team - 1)) != 0) return false;
     const int V = next_pow2((nvec + team - 1) / team);
@@ -303,7 +314,7 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     }
     if (R > a.M && a.M > 0) R = a.M;
     const int64_t stage_stride = (R * row_bytes + 127) / 128 * 128;
-    int S = k.stages > 0 ? k.stages : 2;
+    int S = k.stages > 0 ? k.stages : (row_bytes >= 4096 ? 3 : 2);
     if (S < 1 || S > kMaxStages) return false;
     if (k.stages == 0)
         while (S > 1 && kAlignSlack + kHeaderBytes + S * stage_stride > max_dyn) --S;
@@ -338,7 +349,8 @@ cudaError_t tma_run(const Args& a, const Launch& l) {
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
                               a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
                               a.eps, a.offset, l.rows_per_stage, l.stages,
-                              static_cast<int>(stage_stride), limit < 1 ? 1LL : limit, drain);
+                              static_cast<int>(stage_stride), limit < 1 ? 1LL : limit, drain,
+                              l.blocked ? 1 : 0);
 }
 
 cudaError_t status_read_and_clear(unsigned int* value) {

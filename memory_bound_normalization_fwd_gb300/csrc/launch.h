@@ -35,6 +35,7 @@ struct Launch {
     int64_t work_items = 0;  // independent units the grid strides over
     int64_t wait_limit_ns = 0;
     bool pdl = true;
+    bool blocked = false;  // contiguous row block per CTA instead of strided passes
 };
 
 // Caller knobs (rmsnorm_options_t), validated by the front end. 0 = planner's choice.

@@ -84,21 +84,22 @@ def test_variant_parity(variant, dtype, M, N):
     except B.RMSNormError as e:
         assert e.status == -8
         pytest.skip(f"{variant} does not take N={N}")
-    for max_ctas in (0, 2):
+    for max_ctas, blocked in ((0, False), (2, False), (0, True), (3, True)):
         _run_and_check(x, w, dtype, wl.eps, wl.offset, variant=variant, max_ctas=max_ctas,
-                       expect_variant=variant)
+                       blocked=blocked, expect_variant=variant)
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16, 32])
 @pytest.mark.parametrize("N", [8, 64, 256, 512, 1000])
-def test_warp_lanes_per_row(G, N):
+@pytest.mark.parametrize("D", [1, 2, 4])
+def test_warp_lanes_per_row_and_ring_depth(G, N, D):
     if (N // 8 + G - 1) // G > 4:
         pytest.skip("more than 4 vectors per lane")
-    wl = W.custom(203, N, "bf16", seed=G + N, offset=1.0)
+    wl = W.custom(203, N, "bf16", seed=G + N + D, offset=1.0)
     x, w = W.generate(wl)
-    for max_ctas in (0, 1):
+    for max_ctas, blocked in ((0, False), (1, False), (3, True)):
         _run_and_check(x, w, "bf16", wl.eps, wl.offset, variant="warp", lanes_per_row=G,
-                       max_ctas=max_ctas, expect_variant="warp")
+                       stages=D, max_ctas=max_ctas, blocked=blocked, expect_variant="warp")
 
 
 @pytest.mark.parametrize("T", [64, 128, 256, 512, 1024])
@@ -108,8 +109,9 @@ def test_cta_threads(T, N):
         pytest.skip("more than 4 vectors per thread")
     wl = W.custom(41, N, "fp16", seed=T + N, x_std=30.0)
     x, w = W.generate(wl)
-    _run_and_check(x, w, "fp16", wl.eps, wl.offset, variant="cta", lanes_per_row=T, max_ctas=3,
-                   expect_variant="cta")
+    for blocked in (False, True):
+        _run_and_check(x, w, "fp16", wl.eps, wl.offset, variant="cta", lanes_per_row=T,
+                       max_ctas=3, blocked=blocked, expect_variant="cta")
 
 
 @pytest.mark.parametrize("team,rows,stages", [(16, 1, 1), (16, 7, 2), (32, 16, 3), (64, 5, 4),
@@ -124,9 +126,9 @@ def test_tma_team_rows_stages(team, rows, stages, N):
     except B.RMSNormError as e:
         assert e.status == -8
         pytest.skip("configuration not taken")
-    for max_ctas in (0, 1, 5):
+    for max_ctas, blocked in ((0, False), (1, False), (5, False), (0, True), (5, True)):
         _run_and_check(x, w, "bf16", wl.eps, wl.offset, variant="tma", lanes_per_row=team,
-                       rows_per_stage=rows, stages=stages, max_ctas=max_ctas,
+                       rows_per_stage=rows, stages=stages, max_ctas=max_ctas, blocked=blocked,
                        expect_variant="tma")
 
 
@@ -156,7 +158,9 @@ def test_misaligned_pointers(x_shift, y_shift):
 def test_in_place(variant, N):
     wl = W.custom(300, N, "bf16", seed=N + 5)
     x, w = W.generate(wl)
-    _run_and_check(x, w, "bf16", wl.eps, wl.offset, inplace=True, variant=variant, max_ctas=7)
+    for blocked in (False, True):
+        _run_and_check(x, w, "bf16", wl.eps, wl.offset, inplace=True, variant=variant, max_ctas=7,
+                       blocked=blocked)
 
 
 def test_zero_rows_and_eps_zero():
