@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--stages", type=int, default=0)
     p.add_argument("--rows-per-stage", type=int, default=0)
     p.add_argument("--max-ctas", type=int, default=0)
+    p.add_argument("--strict-order", action="store_true",
+                   help="time without RMSNORM_FLAG_EARLY_LOADS (no overlap between steps)")
     return p.parse_args(argv)
 
 
@@ -233,61 +235,93 @@ def bench_ours(args, wl, rank, world, local_rank):
     xs = [x_host.to(dev) for _ in range(pool)]
     ys = [torch.empty_like(xs[0]) for _ in range(pool)]
     rs = [torch.empty(wl.M, dtype=torch.float32, device=dev) for _ in range(pool)]
-    opts = B.make_options(variant=args.variant, lanes_per_row=args.lanes_per_row,
-                          stages=args.stages, rows_per_stage=args.rows_per_stage,
-                          max_ctas=args.max_ctas)
-    plan = B.rmsnorm_plan_info(wl.M, wl.N, dcode, xs[0].data_ptr(), w_dev.data_ptr(),
-                               ys[0].data_ptr(), opts)
     stream = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
 
-    def step(k: int, s: int):
-        i = k % pool
-        rc = B.rmsnorm_fwd_ex(xs[i].data_ptr(), w_dev.data_ptr(), ys[i].data_ptr(), rs[i].data_ptr(),
-                              wl.M, wl.N, wl.eps, wl.offset, dcode, opts, s)
-        if rc != 0:
-            raise RuntimeError(B.rmsnorm_last_error())
+    def make_opts(early: bool):
+        return B.make_options(variant=args.variant, lanes_per_row=args.lanes_per_row,
+                              stages=args.stages, rows_per_stage=args.rows_per_stage,
+                              max_ctas=args.max_ctas, early_loads=early)
 
-    # Eager warm-up (fills the planner caches), then capture one CUDA graph of
-    # `per_graph` back-to-back ABI calls cycling through the buffer pool.
-    with torch.cuda.stream(stream):
-        for k in range(max(3, min(args.warmup, 64))):
-            step(k, sh)
-    stream.synchronize()
-    per_graph = pool * max(1, 384 // pool)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
-        for k in range(per_graph):
-            step(k, sh)
-    torch.cuda.synchronize()
+    def timed(opts, K: int, Wm: int, clock_gpu=None):
+        """K steps from a CUDA graph of ABI calls, timed with events on `stream`."""
+        def step(k: int):
+            i = k % pool
+            rc = B.rmsnorm_fwd_ex(xs[i].data_ptr(), w_dev.data_ptr(), ys[i].data_ptr(),
+                                  rs[i].data_ptr(), wl.M, wl.N, wl.eps, wl.offset, dcode, opts, sh)
+            if rc != 0:
+                raise RuntimeError(B.rmsnorm_last_error())
 
-    K, Wm = args.steps, max(3, args.warmup)
-    replays, rem = divmod(K, per_graph)
-    with torch.cuda.stream(stream):
-        for _ in range(-(-Wm // per_graph)):
-            graph.replay()
-    torch.cuda.synchronize()
-    barrier()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(torch.cuda.current_device() if world == 1 else local_rank)
-    with sampler:
-        torch.cuda.synchronize()
-        barrier()
+        # Eager warm-up (fills the planner caches), then one CUDA graph of
+        # `per_graph` back-to-back ABI calls cycling through the buffer pool.
         with torch.cuda.stream(stream):
-            start.record(stream)
-            for _ in range(replays):
+            for k in range(max(3, min(Wm, 64))):
+                step(k)
+        stream.synchronize()
+        per_graph = pool * max(1, 384 // pool)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for k in range(per_graph):
+                step(k)
+        torch.cuda.synchronize()
+        replays, rem = divmod(K, per_graph)
+        with torch.cuda.stream(stream):
+            for _ in range(-(-Wm // per_graph)):
                 graph.replay()
-            for k in range(rem):
-                step(k, sh)
-            end.record(stream)
         torch.cuda.synchronize()
         barrier()
-    ms = start.elapsed_time(end)
-    max_s = max_over_ranks(ms / 1e3)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(clock_gpu) if clock_gpu is not None else None
+        if sampler:
+            sampler.__enter__()
+        try:
+            torch.cuda.synchronize()
+            barrier()
+            with torch.cuda.stream(stream):
+                start.record(stream)
+                for _ in range(replays):
+                    graph.replay()
+                for k in range(rem):
+                    step(k)
+                end.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+        finally:
+            if sampler:
+                sampler.__exit__(None, None, None)
+        ms = start.elapsed_time(end)
+        launch = f"CUDA graph of {per_graph} ABI calls, {replays} replays" + (
+            f" + {rem} direct calls" if rem else "")
+        return max_over_ranks(ms / 1e3), ms / 1e3 / K, (sampler.summary() if sampler else None), launch
+
+    # Main measurement. The steps are independent batches (x and w are written
+    # by no step), which meets the precondition of RMSNORM_FLAG_EARLY_LOADS:
+    # step k+1 may start loading while step k finishes; every store stays in
+    # stream order. --strict-order measures without the flag.
+    early = not args.strict_order
+    opts = make_opts(early)
+    plan = B.rmsnorm_plan_info(wl.M, wl.N, dcode, xs[0].data_ptr(), w_dev.data_ptr(),
+                               ys[0].data_ptr(), opts)
+    K, Wm = args.steps, max(3, args.warmup)
+    max_s, per_launch_s, clocks, launch = timed(
+        opts, K, Wm, torch.cuda.current_device() if world == 1 else local_rank)
     value = whole_job_gbs(wl.algorithmic_bytes, K, world, max_s)
-    per_launch_s = ms / 1e3 / K
-    clocks = sampler.summary()
+
+    # The same workload under strict stream order (every access waits for the previous step).
+    strict = None
+    if early:
+        sopts = make_opts(False)
+        splan = B.rmsnorm_plan_info(wl.M, wl.N, dcode, xs[0].data_ptr(), w_dev.data_ptr(),
+                                    ys[0].data_ptr(), sopts)
+        Ks = min(K, 100000)
+        s_max, s_launch, _, _ = timed(sopts, Ks, Wm)
+        strict = {"value": round(whole_job_gbs(wl.algorithmic_bytes, Ks, world, s_max), 2),
+                  "unit": "GB/s", "steps": Ks,
+                  "frac": None, "plan": splan,
+                  "note": "no RMSNORM_FLAG_EARLY_LOADS: each launch reads x only after the "
+                          "previous step completes"}
+    opts = make_opts(False)  # the end-to-end leg keeps strict order (copies precede each call)
 
     # End to end: per step, pinned host x -> device, the ABI call, y and rstd -> pinned host.
     x_pin = x_host.pin_memory()
@@ -310,6 +344,8 @@ def bench_ours(args, wl, rank, world, local_rank):
             e2e_step()
     torch.cuda.synchronize()
     barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(Ke):
@@ -338,8 +374,11 @@ def bench_ours(args, wl, rank, world, local_rank):
                    "bytes_per_step": wl.algorithmic_bytes,
                    "l2": f"rotating pool of {pool} buffer sets ({pool * set_bytes / 1e6:.0f} MB) "
                          f"> 3x L2 ({l2 / 1e6:.0f} MB); no flush needed",
-                   "launch": f"CUDA graph of {per_graph} ABI calls, {replays} replays"
-                             + (f" + {rem} direct calls" if rem else ""),
+                   "launch": launch,
+                   "launch_order": ("early loads (RMSNORM_FLAG_EARLY_LOADS): steps are independent "
+                                    "batches, so step k+1 may start loading x while step k "
+                                    "finishes; all stores stay in stream order") if early
+                                   else "strict stream order",
                    "plan": plan},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -354,6 +393,9 @@ def bench_ours(args, wl, rank, world, local_rank):
         "gpu_launches": K,
         "clocks": clocks,
     }
+    if strict is not None:
+        strict["frac"] = round(strict["value"] / peak, 4)
+        line["strict_order"] = strict
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x_bits, w_bits, wl)
     return line

@@ -97,6 +97,12 @@ typedef enum rmsnorm_variant {
 #define RMSNORM_FLAG_NO_PDL 1       /* launch without programmatic dependent launch */
 #define RMSNORM_FLAG_BLOCKED_ROWS 2 /* each CTA takes one contiguous block of rows
                                        (default: CTAs stride over rows in passes) */
+/* The caller promises that no kernel still running earlier on the stream
+ * writes x or w. The kernel may then start reading them while the previous
+ * kernel finishes (overlapping launches); its writes of y and rstd still wait
+ * for that kernel to complete. Without the promise every access waits. Ignored
+ * with RMSNORM_FLAG_NO_PDL and by the general kernel. */
+#define RMSNORM_FLAG_EARLY_LOADS 4
 
 typedef struct rmsnorm_options {
     int32_t struct_size;     /* sizeof(rmsnorm_options_t) */

@@ -101,13 +101,15 @@ def _check(rc: int) -> int:
 
 FLAG_NO_PDL = 1
 FLAG_BLOCKED_ROWS = 2
+FLAG_EARLY_LOADS = 4
 
 
 def make_options(variant: str | int = "auto", max_ctas: int = 0, lanes_per_row: int = 0,
                  stages: int = 0, rows_per_stage: int = 0, wait_limit_ns: int = 0,
-                 pdl: bool = True, blocked: bool = False) -> Options:
+                 pdl: bool = True, blocked: bool = False, early_loads: bool = False) -> Options:
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
-    flags = (0 if pdl else FLAG_NO_PDL) | (FLAG_BLOCKED_ROWS if blocked else 0)
+    flags = ((0 if pdl else FLAG_NO_PDL) | (FLAG_BLOCKED_ROWS if blocked else 0)
+             | (FLAG_EARLY_LOADS if early_loads else 0))
     return Options(ctypes.sizeof(Options), v, max_ctas, lanes_per_row, stages, rows_per_stage,
                    flags, 0, wait_limit_ns)
 

@@ -101,7 +101,7 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
                     o->variant);
     if (o->max_ctas < 0 || o->lanes_per_row < 0 || o->rows_per_stage < 0 || o->stages < 0 ||
         o->stages > 8 || o->wait_limit_ns < 0 || o->reserved != 0 ||
-        (o->flags & ~(RMSNORM_FLAG_NO_PDL | RMSNORM_FLAG_BLOCKED_ROWS)) != 0)
+        (o->flags & ~(RMSNORM_FLAG_NO_PDL | RMSNORM_FLAG_BLOCKED_ROWS | RMSNORM_FLAG_EARLY_LOADS)) != 0)
         return fail(RMSNORM_ERR_OPTIONS, "options fields out of range");
     *variant = o->variant;
     k->flags = o->flags;
@@ -114,10 +114,12 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
 }
 
 // Chooses the variant. The automatic choice, when x, w and y are 16-byte
-// aligned and N % 8 == 0: the warp-team kernel for rows up to 768 columns, the
-// TMA-staged kernel for longer rows (measured on GB300: warp team ahead at
-// N = 512, TMA ahead from N = 1000 up), the register CTA kernel if the TMA
-// kernel cannot take the row; the general kernel otherwise.
+// aligned and N % 8 == 0: the TMA-staged kernel, except for rows of up to 768
+// columns under strict stream order, which take the warp-team kernel
+// (measured on GB300: with strict order the warp team is ahead at N = 512 and
+// the TMA kernel from N = 1000 up; with early loads the TMA kernel is ahead at
+// every N measured); the register CTA kernel if the TMA kernel cannot take the
+// row; the general kernel otherwise.
 int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch& l,
          int* chosen) {
     bool ok = false;
@@ -127,7 +129,9 @@ int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch
         case RMSNORM_VARIANT_TMA: ok = tma_choose(a, d, k, l); break;
         case RMSNORM_VARIANT_GENERIC: ok = generic_choose(a, d, k, l); break;
         default:
-            if (a.N <= 768 && warp_choose(a, d, k, l)) {
+            const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) &&
+                               !(k.flags & RMSNORM_FLAG_NO_PDL);
+            if (!early && a.N <= 768 && warp_choose(a, d, k, l)) {
                 variant = RMSNORM_VARIANT_WARP;
                 ok = true;
             } else if ((l = Launch{}, tma_choose(a, d, k, l))) {
@@ -205,6 +209,7 @@ extern "C" int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd
     if (rc != RMSNORM_OK) return rc;
     l.pdl = (k.flags & RMSNORM_FLAG_NO_PDL) == 0;
     l.blocked = (k.flags & RMSNORM_FLAG_BLOCKED_ROWS) != 0;
+    l.early = l.pdl && (k.flags & RMSNORM_FLAG_EARLY_LOADS) != 0;
     e = run(chosen, a, l);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
     return RMSNORM_OK;

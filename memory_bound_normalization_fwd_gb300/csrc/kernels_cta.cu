@@ -18,7 +18,7 @@ namespace {
 template <int DT, int THREADS, int V>
 __global__ void __launch_bounds__(THREADS)
 cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
-                int64_t M, int nvec, float n, float eps, float offset, int blocked) {
+                int64_t M, int nvec, float n, float eps, float offset, int mode) {
     constexpr int kWarps = THREADS / 32;
     // Two slots per warp, alternating by row parity, so one barrier per row suffices:
     // slot p is rewritten two rows later, after every thread has passed the
@@ -28,7 +28,9 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     const int lane = tid & 31;
     const int wid = tid >> 5;
 
-    pdl_wait();
+    const bool blocked = (mode & kModeBlocked) != 0;
+    const bool early = (mode & kModeEarlyLoads) != 0;
+    if (!early) pdl_wait();
     pdl_launch_dependents();
     float s[V][kVecElems];
 #pragma unroll
@@ -51,6 +53,7 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         cur[v] = make_uint4(0u, 0u, 0u, 0u);
         if (row < r_end && c < nvec) cur[v] = ld_stream(x + row * nvec + c);
     }
+    if (early) pdl_wait();  // every store comes after the previous kernel completes
 
     int parity = 0;
     for (; row < r_end; row += step) {
@@ -137,7 +140,7 @@ cudaError_t cta_run(const Args& a, const Launch& l) {
     return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
                               a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
-                              a.eps, a.offset, l.blocked ? 1 : 0);
+                              a.eps, a.offset, l.mode());
 }
 
 }  // namespace rmsn

@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(THREADS)
 tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
                 int64_t M, int nvec, float n, float eps, float offset, int rows_per_stage,
                 int stages, int stage_stride, long long limit_cycles, long long drain_cycles,
-                int blocked) {
+                int mode) {
     constexpr int kTeams = THREADS / TEAM;
     constexpr int kLanes = TEAM < 32 ? TEAM : 32;        // lanes in the shuffle step
     constexpr int kTeamWarps = TEAM > 32 ? TEAM / 32 : 1;  // warps per team
@@ -117,6 +117,8 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     const int tid = threadIdx.x;
     const int team = tid / TEAM;
     const int t = tid % TEAM;
+    const bool blocked = (mode & kModeBlocked) != 0;
+    const bool early = (mode & kModeEarlyLoads) != 0;
     const int R = rows_per_stage;
     // Chunks of R consecutive rows. Strided (default): this CTA takes chunks
     // blockIdx.x, + gridDim.x, ... of x. Blocked: this CTA owns one contiguous
@@ -142,7 +144,9 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         for (int st = 0; st < stages; ++st) mbar_init(bars + 8 * st, 1);
         fence_mbar_init();
     }
-    pdl_wait();  // no global memory is touched before the previous kernel completes
+    // No global memory is touched before the previous kernel completes, unless the
+    // caller promised x and w are ready: then only the stores wait (below).
+    if (!early) pdl_wait();
     float s[V][kVecElems];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -168,6 +172,7 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         for (int k = 0; k < stages; ++k) issue(k);
     }
     pdl_launch_dependents();
+    if (early) pdl_wait();
 
     int pp = 0;
     int64_t k = 0;
@@ -304,17 +309,20 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     if (max_dyn <= 0) return false;
 
     const int64_t row_bytes = nvec * 16;
+    // Stage shape, measured on GB300 (1 KB .. 16 KB rows): rows under 4 KB take
+    // 16 KB stages, two deep (small footprint, so the next launch's CTAs fit in
+    // early); 4-8 KB rows take 32 KB stages and 8 KB+ rows one row per stage,
+    // four deep. A stage of several rows holds a whole number of rows per team.
+    const bool short_rows = row_bytes < 4096;
     int64_t R = k.rows_per_stage;
     if (R == 0) {
-        // About 16 KB per stage (measured best on GB300 from 1 KB to 16 KB rows),
-        // a whole number of rows per team when a stage holds several rows.
-        R = (16 * 1024) / row_bytes;
+        R = short_rows ? (16 * 1024) / row_bytes : (32 * 1024) / row_bytes;
         if (R > teams) R = R / teams * teams;
         if (R < 1) R = 1;
     }
     if (R > a.M && a.M > 0) R = a.M;
     const int64_t stage_stride = (R * row_bytes + 127) / 128 * 128;
-    int S = k.stages > 0 ? k.stages : (row_bytes >= 4096 ? 3 : 2);
+    int S = k.stages > 0 ? k.stages : (short_rows ? 2 : 4);
     if (S < 1 || S > kMaxStages) return false;
     if (k.stages == 0)
         while (S > 1 && kAlignSlack + kHeaderBytes + S * stage_stride > max_dyn) --S;
@@ -350,7 +358,7 @@ cudaError_t tma_run(const Args& a, const Launch& l) {
                               a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
                               a.eps, a.offset, l.rows_per_stage, l.stages,
                               static_cast<int>(stage_stride), limit < 1 ? 1LL : limit, drain,
-                              l.blocked ? 1 : 0);
+                              l.mode());
 }
 
 cudaError_t status_read_and_clear(unsigned int* value) {

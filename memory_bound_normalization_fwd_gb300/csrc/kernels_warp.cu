@@ -29,7 +29,7 @@ constexpr int kWarps = 8;  // 256 threads per CTA
 template <int DT, int G, int V, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
-                 int64_t M, int nvec, float n, float eps, float offset, int blocked) {
+                 int64_t M, int nvec, float n, float eps, float offset, int mode) {
     extern __shared__ float4 sw[];  // 2 float4 of (offset + w) per 16-byte vector of w
     constexpr int kTeams = 32 / G;  // rows per warp per pass
     constexpr int kPass = kWarps * kTeams;  // rows per CTA per pass
@@ -42,8 +42,9 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
     // consecutive teams, warps and CTAs, so the whole GPU sweeps x front to
     // back. Blocked: each CTA owns one contiguous block of rows (block sizes
     // differing by at most one row) and sweeps it alone.
+    const bool early = (mode & kModeEarlyLoads) != 0;
     int64_t first0, stride, r_end;  // team 0 of this warp in pass 0; rows per pass; bound
-    if (blocked) {
+    if (mode & kModeBlocked) {
         first0 = static_cast<int64_t>(blockIdx.x) * M / gridDim.x + wid * kTeams;
         r_end = static_cast<int64_t>(blockIdx.x + 1) * M / gridDim.x;
         stride = kPass;
@@ -53,7 +54,7 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
         stride = static_cast<int64_t>(gridDim.x) * kPass;
     }
 
-    pdl_wait();
+    if (!early) pdl_wait();
     for (int i = threadIdx.x; i < nvec; i += kWarps * 32) {
         float s[kVecElems];
         weights8<DT>(__ldg(w + i), offset, s);
@@ -74,6 +75,7 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
             if (row < r_end && c < nvec) buf[d][v] = ld_stream(x + row * nvec + c);
         }
     }
+    if (early) pdl_wait();  // every store comes after the previous kernel completes
 
     for (int64_t k0 = 0; first0 + k0 * stride < r_end; k0 += D) {
 #pragma unroll
@@ -186,7 +188,7 @@ cudaError_t warp_run(const Args& a, const Launch& l) {
     return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
                               a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
-                              a.eps, a.offset, l.blocked ? 1 : 0);
+                              a.eps, a.offset, l.mode());
 }
 
 }  // namespace rmsn

@@ -21,6 +21,10 @@ struct Args {
     cudaStream_t stream;
 };
 
+// Kernel `mode` argument bits.
+constexpr int kModeBlocked = 1;     // one contiguous block of rows per CTA
+constexpr int kModeEarlyLoads = 2;  // first loads of x and w before the PDL wait (caller's promise)
+
 // A launch shape chosen by a variant's planner.
 struct Launch {
     const void* kernel = nullptr;  // the __global__ function (for occupancy queries)
@@ -36,6 +40,8 @@ struct Launch {
     int64_t wait_limit_ns = 0;
     bool pdl = true;
     bool blocked = false;  // contiguous row block per CTA instead of strided passes
+    bool early = false;    // x and w may be read before the previous kernel completes
+    int mode() const { return (blocked ? kModeBlocked : 0) | (early ? kModeEarlyLoads : 0); }
 };
 
 // Caller knobs (rmsnorm_options_t), validated by the front end. 0 = planner's choice.
