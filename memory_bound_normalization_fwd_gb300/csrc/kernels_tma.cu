@@ -311,12 +311,13 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     const int64_t row_bytes = nvec * 16;
     // Stage shape, measured on GB300 (1 KB .. 16 KB rows): rows under 4 KB take
     // 16 KB stages, two deep (small footprint, so the next launch's CTAs fit in
-    // early); 4-8 KB rows take 32 KB stages and 8 KB+ rows one row per stage,
+    // early); 4-8 KB rows take 32 KB stages and longer rows one row per stage,
     // four deep. A stage of several rows holds a whole number of rows per team.
     const bool short_rows = row_bytes < 4096;
     int64_t R = k.rows_per_stage;
     if (R == 0) {
-        R = short_rows ? (16 * 1024) / row_bytes : (32 * 1024) / row_bytes;
+        R = short_rows ? (16 * 1024) / row_bytes
+                       : (row_bytes <= 8192 ? (32 * 1024) / row_bytes : 1);
         if (R > teams) R = R / teams * teams;
         if (R < 1) R = 1;
     }

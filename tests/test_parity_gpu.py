@@ -46,13 +46,17 @@ def _run_and_check(x, w, dtype, eps, offset, rows=None, x_shift=0, y_shift=0, in
 
 # ---------------------------------------------------------------- full-size workloads
 
+@pytest.mark.parametrize("early", [False, True], ids=["strict", "early_loads"])
 @pytest.mark.parametrize("name", list(W.WORKLOADS))
-def test_workload_full_size_automatic_launch(name):
+def test_workload_full_size_automatic_launch(name, early):
+    # The automatic plan, in both launch modes bench.py times (early loads is the
+    # headline mode: two back-to-back calls, the second overlapping the first).
     wl = W.WORKLOADS[name]
     x, w = W.generate(wl)
     rows = None if wl.M * wl.N <= (1 << 23) else sample_rows(wl.M, 192, seed=1)
     case = DeviceCase(x, w, wl.dtype)
-    assert case.run(wl.eps, wl.offset) == 0, B.rmsnorm_last_error()
+    for _ in range(2 if early else 1):
+        assert case.run(wl.eps, wl.offset, early_loads=early) == 0, B.rmsnorm_last_error()
     y, r = case.results()
     case.check_guards()
     # Properties over every row: rstd finite and positive, y finite.
