@@ -34,8 +34,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "RMSNorm fwd achieved HBM GB/s and % of GB300 peak (1 GPU), per M×N×dtype"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["common.cuh", "launch.h", "kernels_warp.cu", "kernels_cta.cu",
-                  "kernels_tma.cu", "kernels_generic.cu", "api.cu"]
+KERNEL_SOURCES = ["common.cuh", "async_copy.cuh", "launch.h", "kernels_warp.cu", "kernels_cta.cu",
+                  "kernels_tma.cu", "kernels_cluster.cu", "kernels_generic.cu", "api.cu"]
 
 
 # ---------------------------------------------------------------- host-side helpers

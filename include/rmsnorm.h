@@ -89,7 +89,12 @@ typedef enum rmsnorm_variant {
      * and N % 8 == 0; rows up to the shared-memory limit. */
     RMSNORM_VARIANT_TMA = 3,
     /* Any alignment and any N: one CTA per row, two passes over the row. */
-    RMSNORM_VARIANT_GENERIC = 4
+    RMSNORM_VARIANT_GENERIC = 4,
+    /* Rows longer than one CTA's shared memory: a row split over a thread-block
+     * cluster of 2..16 CTAs, each staging its column slice by TMA bulk copy; the
+     * slice sums meet through distributed shared memory. Needs 16-byte alignment
+     * and N % 8 == 0; rows up to 16 slices of about 70 KB. */
+    RMSNORM_VARIANT_CLUSTER = 5
 } rmsnorm_variant_t;
 
 /* Optional knobs for rmsnorm_fwd_ex(). Zero-initialise, then set fields. */
@@ -112,10 +117,10 @@ typedef struct rmsnorm_options {
                                 row (= per CTA); TMA: threads per row (16..1024);
                                 GENERIC: threads per CTA; 0 = planner's choice */
     int32_t stages;          /* WARP: rows each team keeps in flight (1, 2 or 4); TMA: pipeline
-                                depth (1..8); 0 = planner's choice */
+                                depth (1..8); CLUSTER: 1..4; 0 = planner's choice */
     int32_t rows_per_stage;  /* TMA: rows per stage; 0 = planner's choice */
     int32_t flags;           /* RMSNORM_FLAG_* bits */
-    int32_t reserved;        /* must be 0 */
+    int32_t cluster_size;    /* CLUSTER: CTAs per row (2..16); 0 = planner's choice */
     int64_t wait_limit_ns;   /* TMA: bound on each mbarrier wait in ns; 0 = 1 second */
 } rmsnorm_options_t;
 
@@ -131,6 +136,7 @@ typedef struct rmsnorm_plan {
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t ctas_per_sm;     /* resident CTAs per SM (occupancy calculator) */
     int32_t sm_count;        /* SMs on the device */
+    int32_t cluster_size;    /* CTAs per cluster (cluster variant; else 0) */
 } rmsnorm_plan_t;
 
 /*

@@ -15,7 +15,7 @@ import threading
 from . import build as _build
 
 BF16, FP16 = 0, 1
-VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "tma": 3, "generic": 4}
+VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "tma": 3, "generic": 4, "cluster": 5}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 STATUS = {
     0: "RMSNORM_OK", -1: "RMSNORM_ERR_NULL", -2: "RMSNORM_ERR_SHAPE", -3: "RMSNORM_ERR_DTYPE",
@@ -38,14 +38,14 @@ class Options(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_int32), ("variant", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("lanes_per_row", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("rows_per_stage", ctypes.c_int32),
-                ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("flags", ctypes.c_int32), ("cluster_size", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64)]
 
 
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "variant", "threads", "grid", "lanes_per_row", "vecs_per_lane", "rows_per_stage",
-        "stages", "smem_bytes", "ctas_per_sm", "sm_count")]
+        "stages", "smem_bytes", "ctas_per_sm", "sm_count", "cluster_size")]
 
     def as_dict(self) -> dict:
         d = {n: getattr(self, n) for n, _ in self._fields_}
@@ -106,12 +106,13 @@ FLAG_EARLY_LOADS = 4
 
 def make_options(variant: str | int = "auto", max_ctas: int = 0, lanes_per_row: int = 0,
                  stages: int = 0, rows_per_stage: int = 0, wait_limit_ns: int = 0,
-                 pdl: bool = True, blocked: bool = False, early_loads: bool = False) -> Options:
+                 pdl: bool = True, blocked: bool = False, early_loads: bool = False,
+                 cluster_size: int = 0) -> Options:
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     flags = ((0 if pdl else FLAG_NO_PDL) | (FLAG_BLOCKED_ROWS if blocked else 0)
              | (FLAG_EARLY_LOADS if early_loads else 0))
     return Options(ctypes.sizeof(Options), v, max_ctas, lanes_per_row, stages, rows_per_stage,
-                   flags, 0, wait_limit_ns)
+                   flags, cluster_size, wait_limit_ns)
 
 
 # ---- raw C ABI (integer device addresses) --------------------------------

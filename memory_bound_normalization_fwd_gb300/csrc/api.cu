@@ -96,11 +96,11 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
     if (o->struct_size != static_cast<int32_t>(sizeof(rmsnorm_options_t)))
         return fail(RMSNORM_ERR_OPTIONS, "options.struct_size is %d, expected %d", o->struct_size,
                     static_cast<int>(sizeof(rmsnorm_options_t)));
-    if (o->variant < RMSNORM_VARIANT_AUTO || o->variant > RMSNORM_VARIANT_GENERIC)
+    if (o->variant < RMSNORM_VARIANT_AUTO || o->variant > RMSNORM_VARIANT_CLUSTER)
         return fail(RMSNORM_ERR_OPTIONS, "options.variant %d is not a rmsnorm_variant_t",
                     o->variant);
     if (o->max_ctas < 0 || o->lanes_per_row < 0 || o->rows_per_stage < 0 || o->stages < 0 ||
-        o->stages > 8 || o->wait_limit_ns < 0 || o->reserved != 0 ||
+        o->stages > 8 || o->wait_limit_ns < 0 || o->cluster_size < 0 || o->cluster_size > 16 ||
         (o->flags & ~(RMSNORM_FLAG_NO_PDL | RMSNORM_FLAG_BLOCKED_ROWS | RMSNORM_FLAG_EARLY_LOADS)) != 0)
         return fail(RMSNORM_ERR_OPTIONS, "options fields out of range");
     *variant = o->variant;
@@ -110,6 +110,7 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
     k->stages = o->stages;
     k->rows_per_stage = o->rows_per_stage;
     k->wait_limit_ns = o->wait_limit_ns;
+    k->cluster_size = o->cluster_size;
     return RMSNORM_OK;
 }
 
@@ -128,14 +129,18 @@ int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch
         case RMSNORM_VARIANT_CTA: ok = cta_choose(a, d, k, l); break;
         case RMSNORM_VARIANT_TMA: ok = tma_choose(a, d, k, l); break;
         case RMSNORM_VARIANT_GENERIC: ok = generic_choose(a, d, k, l); break;
+        case RMSNORM_VARIANT_CLUSTER: ok = cluster_choose(a, d, k, l); break;
         default:
             const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) &&
                                !(k.flags & RMSNORM_FLAG_NO_PDL);
             if (!early && a.N <= 768 && warp_choose(a, d, k, l)) {
                 variant = RMSNORM_VARIANT_WARP;
                 ok = true;
-            } else if ((l = Launch{}, tma_choose(a, d, k, l))) {
+            } else if ((l = Launch{}, tma_choose(a, d, k, l)) && (l.stages >= 2 || k.stages > 0)) {
                 variant = RMSNORM_VARIANT_TMA;
+                ok = true;
+            } else if ((l = Launch{}, cluster_choose(a, d, k, l))) {
+                variant = RMSNORM_VARIANT_CLUSTER;
                 ok = true;
             } else if ((l = Launch{}, cta_choose(a, d, k, l))) {
                 variant = RMSNORM_VARIANT_CTA;
@@ -159,6 +164,7 @@ cudaError_t run(int variant, const Args& a, const Launch& l) {
         case RMSNORM_VARIANT_WARP: return warp_run(a, l);
         case RMSNORM_VARIANT_CTA: return cta_run(a, l);
         case RMSNORM_VARIANT_TMA: return tma_run(a, l);
+        case RMSNORM_VARIANT_CLUSTER: return cluster_run(a, l);
         default: return generic_run(a, l);
     }
 }
@@ -250,16 +256,18 @@ extern "C" int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x,
     out->smem_bytes = l.smem;
     out->ctas_per_sm = l.ctas_per_sm;
     out->sm_count = d.sm_count;
+    out->cluster_size = l.cluster;
     return RMSNORM_OK;
 }
 
 extern "C" int rmsnorm_check_device_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "synchronize: %s", cudaGetErrorString(e));
-    unsigned int v = 0;
+    unsigned int v = 0, vc = 0;
     e = status_read_and_clear(&v);
+    if (e == cudaSuccess) e = cluster_status_read_and_clear(&vc);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
-    if (v != 0) return fail(RMSNORM_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
+    if (v != 0 || vc != 0) return fail(RMSNORM_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
     return RMSNORM_OK;
 }
 

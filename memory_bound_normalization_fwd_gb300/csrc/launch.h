@@ -36,6 +36,8 @@ struct Launch {
     int stages = 0;
     int smem = 0;
     int ctas_per_sm = 0;
+    int cluster = 0;     // CTAs per cluster (cluster variant)
+    int slice_vecs = 0;  // 16-byte vectors of a row per CTA (cluster variant)
     int64_t work_items = 0;  // independent units the grid strides over
     int64_t wait_limit_ns = 0;
     bool pdl = true;
@@ -51,6 +53,7 @@ struct Knobs {
     int lanes_per_row = 0;
     int stages = 0;
     int rows_per_stage = 0;
+    int cluster_size = 0;
     int64_t wait_limit_ns = 0;
 };
 
@@ -74,11 +77,16 @@ cudaError_t cta_run(const Args& a, const Launch& l);
 bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l);
 cudaError_t tma_run(const Args& a, const Launch& l);
 
+bool cluster_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l);
+cudaError_t cluster_run(const Args& a, const Launch& l);
+
 bool generic_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l);
 cudaError_t generic_run(const Args& a, const Launch& l);
 
-// Device status word (bounded-wait timeouts): read and clear on the current device.
+// Device status words (bounded-wait timeouts) of the staged variants: read and
+// clear on the current device.
 cudaError_t status_read_and_clear(unsigned int* value);
+cudaError_t cluster_status_read_and_clear(unsigned int* value);
 
 // Grid size: min(work items / items per CTA, SMs x resident CTAs), at least 1.
 inline int persistent_grid(int64_t work_items, int64_t items_per_cta, int sm_count,

@@ -77,7 +77,7 @@ SHAPES = [(1, 8), (3, 64), (37, 512), (257, 1000), (64, 1024), (17, 2048), (9, 4
           (5, 8192), (130, 520), (11, 16384)]
 
 
-@pytest.mark.parametrize("variant", ["warp", "cta", "tma", "generic"])
+@pytest.mark.parametrize("variant", ["warp", "cta", "tma", "cluster", "generic"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("M,N", SHAPES)
 def test_variant_parity(variant, dtype, M, N):
@@ -158,7 +158,7 @@ def test_misaligned_pointers(x_shift, y_shift):
 
 @pytest.mark.parametrize("variant,N", [("warp", 512), ("warp", 1000), ("cta", 8192),
                                        ("tma", 512), ("tma", 8192), ("generic", 777),
-                                       ("auto", 4096)])
+                                       ("auto", 4096), ("cluster", 16384)])
 def test_in_place(variant, N):
     wl = W.custom(300, N, "bf16", seed=N + 5)
     x, w = W.generate(wl)
@@ -173,7 +173,7 @@ def test_zero_rows_and_eps_zero():
     x, w = W.generate(wl)
     x[0] = 0
     x[5] = 0
-    for variant in ("warp", "cta", "tma", "generic"):
+    for variant in ("warp", "cta", "tma", "cluster", "generic"):
         _run_and_check(x, w, "bf16", 0.0, 0.0, variant=variant)
     x[5, 7] = 0x3F80  # one 1.0
     _run_and_check(x, w, "bf16", 1e-5, 1.0)
@@ -270,7 +270,7 @@ def _raw_call(x, w, y, r, M, N, eps, offset, **opts):
 
 
 @pytest.mark.parametrize("variant,N", [("warp", 512), ("tma", 1000), ("tma", 4096),
-                                       ("cta", 8192), ("generic", 1000)])
+                                       ("cta", 8192), ("generic", 1000), ("cluster", 65536)])
 def test_chained_calls_keep_stream_order(variant, N):
     # Each call reads the previous call's output (ping-pong between two buffers),
     # launched back to back with programmatic dependent launch: the result must be
@@ -318,3 +318,49 @@ def test_early_loads_on_independent_batches(variant, N):
     yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "bf16")
     for i in range(4):
         compare(W.from_torch(ys[i]), rs[i].cpu().numpy(), yo, ro, "bf16", where=f"buffer {i}")
+
+
+# ---------------------------------------------------------------- long rows (cluster variant)
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("M,N,C,S", [(37, 16384, 2, 2), (21, 65536, 0, 0), (19, 100000, 0, 0),
+                                     (12, 131072, 4, 2), (9, 262144, 0, 1), (7, 65536, 16, 3),
+                                     (64, 24576, 8, 4)])
+def test_cluster_parity(dtype, M, N, C, S):
+    wl = W.custom(M, N, dtype, seed=N + C, offset=float(C % 2), outlier_p=0.01)
+    x, w = W.generate(wl)
+    for max_ctas, early in ((0, False), (0, True), (C or 4, False)):
+        _run_and_check(x, w, dtype, wl.eps, wl.offset, variant="cluster", cluster_size=C,
+                       stages=S, max_ctas=max_ctas, early_loads=early, expect_variant="cluster")
+
+
+def test_automatic_plan_takes_clusters_for_long_rows():
+    wl = W.custom(40, 131072, "bf16", seed=5)
+    x, w = W.generate(wl)
+    p = _plan(40, 131072, "bf16")
+    assert p["variant"] == "cluster" and p["cluster_size"] >= 2
+    _run_and_check(x, w, "bf16", wl.eps, wl.offset, expect_variant="cluster")
+    _run_and_check(x, w, "bf16", wl.eps, wl.offset, inplace=True, expect_variant="cluster")
+
+
+def test_rows_beyond_cluster_reach_take_general_kernel():
+    wl = W.custom(2, (1 << 21) + 8, "bf16", seed=6)
+    x, w = W.generate(wl)
+    _run_and_check(x, w, "bf16", wl.eps, wl.offset, expect_variant="generic")
+
+
+def test_cluster_bounded_wait_reports_timeout_and_recovers():
+    wl = W.custom(64, 65536, "bf16", seed=12)
+    x, w = W.generate(wl)
+    case = DeviceCase(x, w, "bf16")
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.rmsnorm_check_device_status(s) == 0
+    assert case.run(wl.eps, wl.offset, variant="cluster", wait_limit_ns=1) == 0
+    assert B.rmsnorm_check_device_status(s) == -7
+    assert B.rmsnorm_check_device_status(s) == 0
+    case.check_guards()
+    assert case.run(wl.eps, wl.offset, variant="cluster") == 0
+    assert B.rmsnorm_check_device_status(s) == 0
+    y, r = case.results()
+    yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "bf16")
+    compare(y, r, yo, ro, "bf16")
