@@ -115,12 +115,15 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
 }
 
 // Chooses the variant. The automatic choice, when x, w and y are 16-byte
-// aligned and N % 8 == 0: the TMA-staged kernel, except for rows of up to 768
-// columns under strict stream order, which take the warp-team kernel
-// (measured on GB300: with strict order the warp team is ahead at N = 512 and
-// the TMA kernel from N = 1000 up; with early loads the TMA kernel is ahead at
-// every N measured); the register CTA kernel if the TMA kernel cannot take the
-// row; the general kernel otherwise.
+// aligned and N % 8 == 0 (measured on GB300, bf16):
+//   rows of up to 768 columns under strict stream order: the warp-team kernel
+//     (ahead of the TMA kernel at N = 512; with early loads the TMA kernel is
+//     ahead at every N measured);
+//   rows of up to 8192 columns: the TMA-staged kernel (ahead from N = 1000 to 8192);
+//   rows of up to 32768 columns: the register CTA kernel (6.4 TB/s at N = 16384
+//     against 5.4 for the TMA kernel, 5.8 against 5.3 at N = 32768);
+//   longer rows: the cluster kernel, while 16 slices fit in shared memory.
+// Anything else takes the general kernel.
 int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch& l,
          int* chosen) {
     bool ok = false;
@@ -135,21 +138,18 @@ int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch
                                !(k.flags & RMSNORM_FLAG_NO_PDL);
             if (!early && a.N <= 768 && warp_choose(a, d, k, l)) {
                 variant = RMSNORM_VARIANT_WARP;
-                ok = true;
-            } else if ((l = Launch{}, tma_choose(a, d, k, l)) && (l.stages >= 2 || k.stages > 0)) {
+            } else if (a.N <= 8192 && (l = Launch{}, tma_choose(a, d, k, l)) &&
+                       (l.stages >= 2 || k.stages > 0)) {
                 variant = RMSNORM_VARIANT_TMA;
-                ok = true;
+            } else if (a.N <= 32768 && (l = Launch{}, cta_choose(a, d, k, l))) {
+                variant = RMSNORM_VARIANT_CTA;
             } else if ((l = Launch{}, cluster_choose(a, d, k, l))) {
                 variant = RMSNORM_VARIANT_CLUSTER;
-                ok = true;
-            } else if ((l = Launch{}, cta_choose(a, d, k, l))) {
-                variant = RMSNORM_VARIANT_CTA;
-                ok = true;
             } else {
                 l = Launch{};
                 variant = RMSNORM_VARIANT_GENERIC;
-                ok = generic_choose(a, d, k, l);
             }
+            ok = variant != RMSNORM_VARIANT_GENERIC || generic_choose(a, d, k, l);
     }
     if (!ok)
         return fail(RMSNORM_ERR_UNSUPPORTED,
