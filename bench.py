@@ -56,6 +56,11 @@ def parse_args(argv=None):
     p.add_argument("--max-ctas", type=int, default=0)
     p.add_argument("--strict-order", action="store_true",
                    help="time without RMSNORM_FLAG_EARLY_LOADS (no overlap between steps)")
+    p.add_argument("--blocked", action="store_true", help="contiguous row block per CTA")
+    p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    p.add_argument("--cluster-size", type=int, default=0)
+    p.add_argument("--ablation", action="store_true",
+                   help="time a matrix of kernel variants and knobs per workload, one JSON line each")
     return p.parse_args(argv)
 
 
@@ -182,6 +187,95 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(busy)}
 
 
+# ---------------------------------------------------------------- timing harness
+
+class PoolBench:
+    """Inputs resident in HBM in a rotating pool of buffer sets (>= 3x L2, so no
+    step reads another step's lines from L2), steps issued as a CUDA graph of
+    C-ABI calls, timed with CUDA events on the launching stream."""
+
+    def __init__(self, wl, x_bits, w_bits, dev):
+        import torch
+        from memory_bound_normalization_fwd_gb300 import binding as B
+        from memory_bound_normalization_fwd_gb300 import workloads as W
+        self.wl, self.dev = wl, dev
+        self.dcode = B.BF16 if wl.dtype == "bf16" else B.FP16
+        self.x_host = W.to_torch(x_bits, wl.dtype)
+        self.w_dev = W.to_torch(w_bits, wl.dtype).to(dev)
+        self.set_bytes = 4 * wl.M * wl.N + 4 * wl.M
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.pool = max(2, -(-3 * self.l2 // self.set_bytes))
+        self.xs = [self.x_host.to(dev) for _ in range(self.pool)]
+        self.ys = [torch.empty_like(self.xs[0]) for _ in range(self.pool)]
+        self.rs = [torch.empty(wl.M, dtype=torch.float32, device=dev) for _ in range(self.pool)]
+        self.stream = torch.cuda.Stream(dev)
+
+    def _graph_time(self, step, K: int, Wm: int, clock_gpu=None):
+        import torch
+        stream = self.stream
+        with torch.cuda.stream(stream):
+            for k in range(max(3, min(Wm, 64))):
+                step(k)
+        stream.synchronize()
+        per_graph = self.pool * max(1, 384 // self.pool)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for k in range(per_graph):
+                step(k)
+        torch.cuda.synchronize()
+        replays, rem = divmod(K, per_graph)
+        with torch.cuda.stream(stream):
+            for _ in range(-(-Wm // per_graph)):
+                graph.replay()
+        torch.cuda.synchronize()
+        barrier()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(clock_gpu) if clock_gpu is not None else None
+        if sampler:
+            sampler.__enter__()
+        try:
+            torch.cuda.synchronize()
+            barrier()
+            with torch.cuda.stream(stream):
+                start.record(stream)
+                for _ in range(replays):
+                    graph.replay()
+                for k in range(rem):
+                    step(k)
+                end.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+        finally:
+            if sampler:
+                sampler.__exit__(None, None, None)
+        ms = start.elapsed_time(end)
+        launch = f"CUDA graph of {per_graph} ABI calls, {replays} replays" + (
+            f" + {rem} direct calls" if rem else "")
+        return max_over_ranks(ms / 1e3), ms / 1e3 / K, (sampler.summary() if sampler else None), launch
+
+    def timed(self, opts, K: int, Wm: int, clock_gpu=None):
+        """(max-over-ranks seconds, seconds per step, clocks, launch text) for K steps."""
+        from memory_bound_normalization_fwd_gb300 import binding as B
+        wl, sh = self.wl, self.stream.cuda_stream
+
+        def step(k: int):
+            i = k % self.pool
+            rc = B.rmsnorm_fwd_ex(self.xs[i].data_ptr(), self.w_dev.data_ptr(), self.ys[i].data_ptr(),
+                                  self.rs[i].data_ptr(), wl.M, wl.N, wl.eps, wl.offset, self.dcode,
+                                  opts, sh)
+            if rc != 0:
+                raise RuntimeError(B.rmsnorm_last_error())
+        return self._graph_time(step, K, Wm, clock_gpu)
+
+    def copy_timed(self, K: int, Wm: int):
+        """A plain device copy of x into y at the same size, same pool, same graph shape."""
+        def step(k: int):
+            i = k % self.pool
+            self.ys[i].copy_(self.xs[i])
+        return self._graph_time(step, K, Wm)
+
+
 # ---------------------------------------------------------------- CPU oracle legs
 
 def run_oracle_threaded(x, w, wl, rows: int, threads: int):
@@ -227,73 +321,16 @@ def bench_ours(args, wl, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     dcode = B.BF16 if wl.dtype == "bf16" else B.FP16
     x_bits, w_bits = W.generate(wl)
-    x_host = W.to_torch(x_bits, wl.dtype)
-    w_dev = W.to_torch(w_bits, wl.dtype).to(dev)
-    set_bytes = 4 * wl.M * wl.N + 4 * wl.M
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    pool = max(2, -(-3 * l2 // set_bytes))  # buffer sets totalling >= 3x L2
-    xs = [x_host.to(dev) for _ in range(pool)]
-    ys = [torch.empty_like(xs[0]) for _ in range(pool)]
-    rs = [torch.empty(wl.M, dtype=torch.float32, device=dev) for _ in range(pool)]
-    stream = torch.cuda.Stream(dev)
-    sh = stream.cuda_stream
+    pb = PoolBench(wl, x_bits, w_bits, dev)
+    x_host, w_dev, xs, ys, rs = pb.x_host, pb.w_dev, pb.xs, pb.ys, pb.rs
+    pool, set_bytes, l2, stream, sh = pb.pool, pb.set_bytes, pb.l2, pb.stream, pb.stream.cuda_stream
+    timed = pb.timed
 
     def make_opts(early: bool):
         return B.make_options(variant=args.variant, lanes_per_row=args.lanes_per_row,
                               stages=args.stages, rows_per_stage=args.rows_per_stage,
-                              max_ctas=args.max_ctas, early_loads=early)
-
-    def timed(opts, K: int, Wm: int, clock_gpu=None):
-        """K steps from a CUDA graph of ABI calls, timed with events on `stream`."""
-        def step(k: int):
-            i = k % pool
-            rc = B.rmsnorm_fwd_ex(xs[i].data_ptr(), w_dev.data_ptr(), ys[i].data_ptr(),
-                                  rs[i].data_ptr(), wl.M, wl.N, wl.eps, wl.offset, dcode, opts, sh)
-            if rc != 0:
-                raise RuntimeError(B.rmsnorm_last_error())
-
-        # Eager warm-up (fills the planner caches), then one CUDA graph of
-        # `per_graph` back-to-back ABI calls cycling through the buffer pool.
-        with torch.cuda.stream(stream):
-            for k in range(max(3, min(Wm, 64))):
-                step(k)
-        stream.synchronize()
-        per_graph = pool * max(1, 384 // pool)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
-            for k in range(per_graph):
-                step(k)
-        torch.cuda.synchronize()
-        replays, rem = divmod(K, per_graph)
-        with torch.cuda.stream(stream):
-            for _ in range(-(-Wm // per_graph)):
-                graph.replay()
-        torch.cuda.synchronize()
-        barrier()
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        sampler = ClockSampler(clock_gpu) if clock_gpu is not None else None
-        if sampler:
-            sampler.__enter__()
-        try:
-            torch.cuda.synchronize()
-            barrier()
-            with torch.cuda.stream(stream):
-                start.record(stream)
-                for _ in range(replays):
-                    graph.replay()
-                for k in range(rem):
-                    step(k)
-                end.record(stream)
-            torch.cuda.synchronize()
-            barrier()
-        finally:
-            if sampler:
-                sampler.__exit__(None, None, None)
-        ms = start.elapsed_time(end)
-        launch = f"CUDA graph of {per_graph} ABI calls, {replays} replays" + (
-            f" + {rem} direct calls" if rem else "")
-        return max_over_ranks(ms / 1e3), ms / 1e3 / K, (sampler.summary() if sampler else None), launch
+                              max_ctas=args.max_ctas, early_loads=early, blocked=args.blocked,
+                              pdl=not args.no_pdl, cluster_size=args.cluster_size)
 
     # Main measurement. The steps are independent batches (x and w are written
     # by no step), which meets the precondition of RMSNORM_FLAG_EARLY_LOADS:
@@ -401,6 +438,64 @@ def bench_ours(args, wl, rank, world, local_rank):
     return line
 
 
+# ---------------------------------------------------------------- ablation matrix
+
+def ablation_configs(wl):
+    """Kernel variants and knobs to compare on one workload (the pages' knobs:
+    TMA staging on or off, prefetch depth, rows per warp, registers and
+    occupancy; plus launch overlap and row order)."""
+    nvec, row = wl.N // 8, 2 * wl.N
+    cfgs = [dict(), dict(early_loads=True), dict(pdl=False), dict(blocked=True)]
+    if nvec <= 128:
+        for G in (8, 16, 32):
+            for D in (1, 2, 4):
+                if (nvec + G - 1) // G <= 4:
+                    cfgs.append(dict(variant="warp", lanes_per_row=G, stages=D))
+    for T in (64, 128, 256, 512, 1024):
+        if T // 2 < nvec <= 4 * T:
+            cfgs.append(dict(variant="cta", lanes_per_row=T))
+    for kb in (8, 16, 32):
+        R = max(1, kb * 1024 // row)
+        for S in (1, 2, 3, 4):
+            if S * R * row <= 200 * 1024:
+                for early in (False, True):
+                    cfgs.append(dict(variant="tma", rows_per_stage=R, stages=S, early_loads=early))
+    if nvec >= 512:
+        for C in (2, 4):
+            cfgs.append(dict(variant="cluster", cluster_size=C, early_loads=True))
+    cfgs.append(dict(variant="generic"))
+    return cfgs
+
+
+def run_ablation(args, names):
+    import torch
+    from memory_bound_normalization_fwd_gb300 import binding as B
+    from memory_bound_normalization_fwd_gb300 import workloads as W
+    peak, _ = load_peaks()
+    dev = torch.device("cuda", 0)
+    for name in names:
+        wl = W.WORKLOADS[name]
+        x_bits, w_bits = W.generate(wl)
+        pb = PoolBench(wl, x_bits, w_bits, dev)
+        K = args.steps if wl.M * wl.N < (1 << 26) else max(200, args.steps // 20)
+        s, _, _, _ = pb.copy_timed(K, 3)
+        print(json.dumps({"ablation": name, "config": "device copy x -> y (torch)",
+                          "gbs": round(4 * wl.M * wl.N * K / s / 1e9, 1)}), flush=True)
+        for cfg in ablation_configs(wl):
+            opts = B.make_options(**cfg)
+            try:
+                plan = B.rmsnorm_plan_info(wl.M, wl.N, pb.dcode, pb.xs[0].data_ptr(),
+                                           pb.w_dev.data_ptr(), pb.ys[0].data_ptr(), opts)
+            except B.RMSNormError:
+                continue
+            s, _, _, _ = pb.timed(opts, K, 3)
+            gbs = wl.algorithmic_bytes * K / s / 1e9
+            print(json.dumps({"ablation": name, "config": cfg, "gbs": round(gbs, 1),
+                              "frac": round(gbs / peak, 4), "plan": plan}), flush=True)
+        del pb
+        torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 
 def bench_reference(args, wl):
@@ -439,6 +534,10 @@ def main(argv=None):
     from memory_bound_normalization_fwd_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload or W.BENCH_WORKLOAD]
     rank, world, local_rank = dist_env()
+
+    if args.ablation:
+        run_ablation(args, [args.workload] if args.workload else list(W.WORKLOADS))
+        return 0
 
     if args.impl == "reference":
         if rank != 0:
