@@ -27,7 +27,12 @@
  *   w     [N]    same dtype as x
  *   y     [M, N] same dtype as x; may equal x exactly (in place), must not
  *                otherwise overlap x, w or rstd
- *   rstd  [M]    fp32; must not overlap x, w or y
+ *   rstd  [M]    fp32; must not overlap x, w or y; may be NULL (inference:
+ *                rstd is then not stored)
+ * rmsnorm_fwd_strided() takes row strides instead (row i of x at x + i*ldx,
+ * of y at y + i*ldy, in elements, each >= N), for rows that are slices of
+ * wider tensors; the overlap rules then apply to the spans from the first to
+ * the last element of each array.
  * x, w, y need only their element alignment (2 bytes) and rstd 4 bytes.
  * 16-byte-aligned x, w, y with N a multiple of 8 take the vectorised kernels;
  * anything else takes the general kernel.
@@ -141,8 +146,8 @@ typedef struct rmsnorm_plan {
 
 /*
  * RMSNorm forward: y = x * rsqrt(mean(x^2) + eps) * (offset + w), rstd kept.
- *   x, w, y, rstd  device pointers as described above (x, y, rstd may be NULL
- *                  when M == 0; w must not be NULL)
+ *   x, w, y, rstd  device pointers as described above (x and y may be NULL
+ *                  when M == 0, rstd may always be NULL; w must not be NULL)
  *   M              rows (>= 0; M == 0 launches nothing and returns RMSNORM_OK)
  *   N              columns (> 0)
  *   eps            >= 0 and finite; added to the mean of squares inside the root
@@ -160,6 +165,15 @@ int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, i
 int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
                    float eps, float offset, int dtype, const rmsnorm_options_t* opts,
                    void* stream);
+
+/* rmsnorm_fwd_ex over strided rows: row i of x starts at element i*ldx, row i
+ * of y at element i*ldy (ldx, ldy >= N; in place needs y == x and ldy == ldx).
+ * The vectorised kernels additionally need ldx and ldy to be multiples of 8;
+ * other strides take the general kernel. Same operation and errors as
+ * rmsnorm_fwd; RMSNORM_ERR_SHAPE if a stride is below N. */
+int rmsnorm_fwd_strided(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy,
+                        float* rstd, int64_t M, int64_t N, float eps, float offset, int dtype,
+                        const rmsnorm_options_t* opts, void* stream);
 
 /* Fills *out with the launch rmsnorm_fwd_ex would make for these arguments on
  * the current device (no launch). x, w, y are used only for their alignment

@@ -8,6 +8,6 @@ seeded input generator (:mod:`.workloads`).
 """
 from .binding import (  # noqa: F401
     BF16, FP16, EXPORTS, VARIANTS, Options, RMSNormError, fwd, lib, make_options,
-    rmsnorm_check_device_status, rmsnorm_fwd, rmsnorm_fwd_ex, rmsnorm_last_error,
+    rmsnorm_check_device_status, rmsnorm_fwd, rmsnorm_fwd_ex, rmsnorm_fwd_strided, rmsnorm_last_error,
     rmsnorm_plan_info, rmsnorm_strerror, rmsnorm_version,
 )

@@ -24,8 +24,9 @@ STATUS = {
     -10: "RMSNORM_ERR_ALIGN",
 }
 # Every function include/rmsnorm.h declares.
-EXPORTS = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_plan_info", "rmsnorm_check_device_status",
-           "rmsnorm_strerror", "rmsnorm_last_error", "rmsnorm_version")
+EXPORTS = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_strided", "rmsnorm_plan_info",
+           "rmsnorm_check_device_status", "rmsnorm_strerror", "rmsnorm_last_error",
+           "rmsnorm_version")
 
 
 class RMSNormError(RuntimeError):
@@ -78,6 +79,9 @@ def lib() -> ctypes.CDLL:
             L.rmsnorm_fwd_ex.argtypes = [vp, vp, vp, vp, i64, i64, f32, f32, i32,
                                          ctypes.POINTER(Options), vp]
             L.rmsnorm_fwd_ex.restype = i32
+            L.rmsnorm_fwd_strided.argtypes = [vp, i64, vp, vp, i64, vp, i64, i64, f32, f32, i32,
+                                              ctypes.POINTER(Options), vp]
+            L.rmsnorm_fwd_strided.restype = i32
             L.rmsnorm_plan_info.argtypes = [i64, i64, i32, vp, vp, vp, ctypes.POINTER(Options),
                                             ctypes.POINTER(Plan)]
             L.rmsnorm_plan_info.restype = i32
@@ -128,6 +132,13 @@ def rmsnorm_fwd_ex(x: int, w: int, y: int, rstd: int, M: int, N: int, eps: float
                                 ctypes.byref(opts) if opts is not None else None, stream)
 
 
+def rmsnorm_fwd_strided(x: int, ldx: int, w: int, y: int, ldy: int, rstd: int, M: int, N: int,
+                        eps: float, offset: float, dtype: int, opts: Options | None,
+                        stream: int) -> int:
+    return lib().rmsnorm_fwd_strided(x, ldx, w, y, ldy, rstd, M, N, eps, offset, dtype,
+                                     ctypes.byref(opts) if opts is not None else None, stream)
+
+
 def rmsnorm_plan_info(M: int, N: int, dtype: int, x: int = 0, w: int = 0, y: int = 0,
                       opts: Options | None = None) -> dict:
     out = Plan()
@@ -168,26 +179,37 @@ def fwd(x, w, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=None, stream=
         **options):
     """y, rstd = fwd(x, w): RMSNorm forward of a contiguous CUDA tensor x[..., N].
 
-    ``y`` and ``rstd`` may be passed to write in place (y may be x itself).
+    ``y`` and ``rstd`` may be passed to write in place (y may be x itself);
+    ``rstd=False`` skips storing rstd (inference). 2-D ``x``/``y`` views with unit
+    column stride (rows of wider tensors) go through ``rmsnorm_fwd_strided``.
     Keyword ``options`` go to :func:`make_options` (variant, max_ctas, ...).
     Runs on ``stream`` (a torch.cuda.Stream) or the current stream.
     """
     import torch
     if not (x.is_cuda and w.is_cuda):
         raise ValueError("x and w must be CUDA tensors")
-    if not x.is_contiguous() or not w.is_contiguous():
-        raise ValueError("x and w must be contiguous")
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
     N = x.shape[-1]
-    M = x.numel() // N if N else 0
     if w.dtype != x.dtype or w.numel() != N:
         raise ValueError("w must have x's dtype and N elements")
+    if x.is_contiguous():
+        M, ldx = (x.numel() // N if N else 0), N
+    elif x.dim() == 2 and x.stride(1) == 1:
+        M, ldx = x.shape[0], x.stride(0)  # rows of a wider tensor
+    else:
+        raise ValueError("x must be contiguous, or 2-D with unit column stride")
     if y is None:
-        y = torch.empty_like(x)
+        y = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    ldy = y.stride(0) if (y.dim() == 2 and not y.is_contiguous()) else N
+    if y.shape != x.shape or (ldy == N and not y.is_contiguous()):
+        raise ValueError("y must have x's shape, contiguous or 2-D with unit column stride")
     if rstd is None:
         rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    r_ptr = 0 if rstd is False else rstd.data_ptr()
     s = stream if stream is not None else torch.cuda.current_stream(x.device)
     opts = make_options(**options) if options else None
     with torch.cuda.device(x.device):
-        _check(rmsnorm_fwd_ex(x.data_ptr(), w.data_ptr(), y.data_ptr(), rstd.data_ptr(), M, N,
-                              eps, offset, _dtype_code(x), opts, s.cuda_stream))
-    return y, rstd
+        _check(rmsnorm_fwd_strided(x.data_ptr(), ldx, w.data_ptr(), y.data_ptr(), ldy, r_ptr, M,
+                                   N, eps, offset, _dtype_code(x), opts, s.cuda_stream))
+    return y, (None if rstd is False else rstd)

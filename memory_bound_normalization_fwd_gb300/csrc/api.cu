@@ -55,36 +55,47 @@ bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
     return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
 }
 
-int validate(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N, float eps,
-             float offset, int dtype) {
+int validate(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, float* rstd,
+             int64_t M, int64_t N, float eps, float offset, int dtype) {
     if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16)
         return fail(RMSNORM_ERR_DTYPE, "dtype %d is not RMSNORM_DTYPE_BF16 (0) or _FP16 (1)", dtype);
     if (M < 0 || N <= 0)
         return fail(RMSNORM_ERR_SHAPE, "need M >= 0 and N > 0 (got M=%lld N=%lld)",
                     static_cast<long long>(M), static_cast<long long>(N));
+    if (ldx < N || ldy < N)
+        return fail(RMSNORM_ERR_SHAPE, "row strides must be >= N (ldx=%lld ldy=%lld N=%lld)",
+                    static_cast<long long>(ldx), static_cast<long long>(ldy),
+                    static_cast<long long>(N));
     // 2^48 bytes bounds any array a GPU can hold and keeps the kernels' 64-bit
     // index arithmetic (row block bounds are CTA index * M) far from overflow.
-    if (M > 0 && (N > (int64_t(1) << 47) / M || M > (int64_t(1) << 46)))
-        return fail(RMSNORM_ERR_SHAPE, "x would exceed 2^48 bytes (M=%lld N=%lld)",
-                    static_cast<long long>(M), static_cast<long long>(N));
+    const int64_t lim = int64_t(1) << 47;
+    if (M > 0 && (M > (int64_t(1) << 46) || ldx > lim / M || ldy > lim / M))
+        return fail(RMSNORM_ERR_SHAPE, "x or y would span more than 2^48 bytes (M=%lld)",
+                    static_cast<long long>(M));
     if (!std::isfinite(eps) || eps < 0.f)
         return fail(RMSNORM_ERR_SCALAR, "eps must be finite and >= 0 (got %g)", eps);
     if (!std::isfinite(offset))
         return fail(RMSNORM_ERR_SCALAR, "offset must be finite (got %g)", offset);
     if (w == nullptr) return fail(RMSNORM_ERR_NULL, "w is NULL");
     if (M == 0) return RMSNORM_OK;
-    if (x == nullptr || y == nullptr || rstd == nullptr)
-        return fail(RMSNORM_ERR_NULL, "x, y and rstd must be non-NULL when M > 0");
+    if (x == nullptr || y == nullptr)
+        return fail(RMSNORM_ERR_NULL, "x and y must be non-NULL when M > 0");
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
          reinterpret_cast<uintptr_t>(w)) & 1u)
         return fail(RMSNORM_ERR_ALIGN, "x, w and y must be 2-byte aligned");
     if (reinterpret_cast<uintptr_t>(rstd) & 3u)
         return fail(RMSNORM_ERR_ALIGN, "rstd must be 4-byte aligned");
-    const int64_t xb = M * N * 2, wb = N * 2, rb = M * 4;
-    if (x != y && overlaps(x, xb, y, xb))
+    // Byte spans from the first element of row 0 to the last element of row M-1.
+    const int64_t xb = ((M - 1) * ldx + N) * 2, yb = ((M - 1) * ldy + N) * 2;
+    const int64_t wb = N * 2, rb = M * 4;
+    if (x == y) {
+        if (ldx != ldy) return fail(RMSNORM_ERR_OVERLAP, "in place (y == x) needs ldy == ldx");
+    } else if (overlaps(x, xb, y, yb)) {
         return fail(RMSNORM_ERR_OVERLAP, "y overlaps x without being equal to it");
-    if (overlaps(w, wb, y, xb)) return fail(RMSNORM_ERR_OVERLAP, "w overlaps y");
-    if (overlaps(rstd, rb, x, xb) || overlaps(rstd, rb, y, xb) || overlaps(rstd, rb, w, wb))
+    }
+    if (overlaps(w, wb, y, yb)) return fail(RMSNORM_ERR_OVERLAP, "w overlaps y");
+    if (rstd != nullptr &&
+        (overlaps(rstd, rb, x, xb) || overlaps(rstd, rb, y, yb) || overlaps(rstd, rb, w, wb)))
         return fail(RMSNORM_ERR_OVERLAP, "rstd overlaps x, y or w");
     return RMSNORM_OK;
 }
@@ -195,10 +206,12 @@ int occupancy(const void* kernel, int threads, int smem) {
 
 using namespace rmsn;
 
-extern "C" int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M,
-                              int64_t N, float eps, float offset, int dtype,
-                              const rmsnorm_options_t* opts, void* stream) {
-    int rc = validate(x, w, y, rstd, M, N, eps, offset, dtype);
+namespace {
+
+int forward(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, float* rstd,
+            int64_t M, int64_t N, float eps, float offset, int dtype,
+            const rmsnorm_options_t* opts, void* stream) {
+    int rc = validate(x, ldx, w, y, ldy, rstd, M, N, eps, offset, dtype);
     if (rc != RMSNORM_OK) return rc;
     int variant;
     Knobs k;
@@ -208,7 +221,8 @@ extern "C" int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd
     DeviceInfo d;
     cudaError_t e = device_info(&d);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
-    const Args a{x, w, y, rstd, M, N, eps, offset, dtype, static_cast<cudaStream_t>(stream)};
+    const Args a{x, w, y, rstd, M, N, ldx, ldy, eps, offset, dtype,
+                 static_cast<cudaStream_t>(stream)};
     Launch l;
     int chosen = 0;
     rc = plan(a, d, variant, k, l, &chosen);
@@ -221,9 +235,24 @@ extern "C" int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd
     return RMSNORM_OK;
 }
 
+}  // namespace
+
+extern "C" int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M,
+                              int64_t N, float eps, float offset, int dtype,
+                              const rmsnorm_options_t* opts, void* stream) {
+    return forward(x, N, w, y, N, rstd, M, N, eps, offset, dtype, opts, stream);
+}
+
 extern "C" int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M,
                            int64_t N, float eps, float offset, int dtype, void* stream) {
-    return rmsnorm_fwd_ex(x, w, y, rstd, M, N, eps, offset, dtype, nullptr, stream);
+    return forward(x, N, w, y, N, rstd, M, N, eps, offset, dtype, nullptr, stream);
+}
+
+extern "C" int rmsnorm_fwd_strided(const void* x, int64_t ldx, const void* w, void* y,
+                                   int64_t ldy, float* rstd, int64_t M, int64_t N, float eps,
+                                   float offset, int dtype, const rmsnorm_options_t* opts,
+                                   void* stream) {
+    return forward(x, ldx, w, y, ldy, rstd, M, N, eps, offset, dtype, opts, stream);
 }
 
 extern "C" int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void* w,
@@ -241,7 +270,7 @@ extern "C" int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x,
     DeviceInfo d;
     cudaError_t e = device_info(&d);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
-    const Args a{x, w, const_cast<void*>(y), nullptr, M, N, 0.f, 0.f, dtype, nullptr};
+    const Args a{x, w, const_cast<void*>(y), nullptr, M, N, N, N, 0.f, 0.f, dtype, nullptr};
     Launch l;
     int chosen = 0;
     rc = plan(a, d, variant, k, l, &chosen);

@@ -77,7 +77,8 @@ __device__ __forceinline__ uint32_t ld_peer_u32(uint32_t local_addr, uint32_t ra
 template <int DT>
 __global__ void __launch_bounds__(kThreads)
 cluster_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
-                    int64_t M, int nvec, int slice_vecs, float n, float eps, float offset,
+                    int64_t M, int nvec, int64_t ldx, int64_t ldy, int slice_vecs, float n,
+                    float eps, float offset,
                     int stages, int slice_stride, long long limit_cycles, long long drain_cycles,
                     int mode) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -120,7 +121,7 @@ cluster_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float
         const int st = static_cast<int>(k % stages);
         const int64_t row = cluster + k * nclusters;
         mbar_arrive_expect_tx(bars + 8 * st, slice_bytes);
-        bulk_g2s(smem_u32(stage0 + static_cast<int64_t>(st) * slice_stride), x + row * nvec + v0,
+        bulk_g2s(smem_u32(stage0 + static_cast<int64_t>(st) * slice_stride), x + row * ldx + v0,
                  slice_bytes, bars + 8 * st);
     };
     if (tid == 0) {
@@ -182,11 +183,11 @@ cluster_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float
         }
         const int64_t row = cluster + k * nclusters;
         const float r = row_rstd(row_total, n, eps);
-        if (rank == 0 && tid == 0) rstd[row] = r;
+        if (rank == 0 && tid == 0 && rstd != nullptr) rstd[row] = r;
         for (int i = tid; i < my_vecs; i += kThreads) {
             float s[kVecElems];
             weights8<DT>(sw[i], offset, s);
-            st_stream(y + row * nvec + v0 + i, scale8<DT>(sx[i], r, s));
+            st_stream(y + row * ldy + v0 + i, scale8<DT>(sx[i], r, s));
         }
         pp ^= 1;
         __syncthreads();  // every thread is done reading this stage
@@ -206,8 +207,8 @@ cluster_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float
     cluster_sync();  // no CTA retires while a peer may still read its shared memory
 }
 
-using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, int, float, float,
-                    float, int, int, long long, long long, int);
+using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, int64_t, int64_t, int,
+                    float, float, float, int, int, long long, long long, int);
 
 // One-time per device and kernel: opt into the full dynamic shared memory and
 // into non-portable (16-CTA) clusters. Returns the dynamic smem limit, 0 on failure.
@@ -263,7 +264,7 @@ int max_clusters(const void* fn, int C, int smem) {
 }  // namespace
 
 bool cluster_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
-    if (a.N % kVecElems != 0 || !aligned16(a.x) || !aligned16(a.y) || !aligned16(a.w)) return false;
+    if (!vector_ok(a)) return false;
     const int64_t nvec = a.N / kVecElems;
     Fn fn = a.dtype == kBF16 ? cluster_rows_kernel<kBF16> : cluster_rows_kernel<kFP16>;
     const int max_dyn = prepare(reinterpret_cast<const void*>(fn), d.max_smem_optin);
@@ -323,7 +324,8 @@ cudaError_t cluster_run(const Args& a, const Launch& l) {
     cfg.numAttrs = l.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
-                              a.M, static_cast<int>(a.N / kVecElems), l.slice_vecs,
+                              a.M, static_cast<int>(a.N / kVecElems), a.ldx / kVecElems,
+                              a.ldy / kVecElems, l.slice_vecs,
                               static_cast<float>(a.N), a.eps, a.offset, l.stages, slice_stride,
                               limit < 1 ? 1LL : limit, drain, l.mode());
 }

@@ -18,7 +18,8 @@ namespace {
 template <int DT, int THREADS, int V>
 __global__ void __launch_bounds__(THREADS)
 cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
-                int64_t M, int nvec, float n, float eps, float offset, int mode) {
+                int64_t M, int nvec, int64_t ldx, int64_t ldy, float n, float eps, float offset,
+                int mode) {
     constexpr int kWarps = THREADS / 32;
     // Two slots per warp, alternating by row parity, so one barrier per row suffices:
     // slot p is rewritten two rows later, after every thread has passed the
@@ -51,7 +52,7 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     for (int v = 0; v < V; ++v) {
         const int c = v * THREADS + tid;
         cur[v] = make_uint4(0u, 0u, 0u, 0u);
-        if (row < r_end && c < nvec) cur[v] = ld_stream(x + row * nvec + c);
+        if (row < r_end && c < nvec) cur[v] = ld_stream(x + row * ldx + c);
     }
     if (early) pdl_wait();  // every store comes after the previous kernel completes
 
@@ -63,7 +64,7 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         for (int v = 0; v < V; ++v) {
             const int c = v * THREADS + tid;
             nxt[v] = make_uint4(0u, 0u, 0u, 0u);
-            if (nrow < r_end && c < nvec) nxt[v] = ld_stream(x + nrow * nvec + c);
+            if (nrow < r_end && c < nvec) nxt[v] = ld_stream(x + nrow * ldx + c);
         }
 
         float ss = 0.f;
@@ -77,11 +78,11 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
 #pragma unroll
         for (int k = 0; k < kWarps; ++k) tot += part[parity][k];
         const float r = row_rstd(tot, n, eps);
-        if (tid == 0) rstd[row] = r;
+        if (tid == 0 && rstd != nullptr) rstd[row] = r;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = v * THREADS + tid;
-            if (c < nvec) st_stream(y + row * nvec + c, scale8<DT>(cur[v], r, s[v]));
+            if (c < nvec) st_stream(y + row * ldy + c, scale8<DT>(cur[v], r, s[v]));
         }
 #pragma unroll
         for (int v = 0; v < V; ++v) cur[v] = nxt[v];
@@ -89,8 +90,8 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     }
 }
 
-using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, float, float, float,
-                    int);
+using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, int64_t, int64_t, float,
+                    float, float, int);
 
 template <int DT>
 Fn pick(int T, int V) {
@@ -108,7 +109,7 @@ Fn pick(int T, int V) {
 }  // namespace
 
 bool cta_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
-    if (a.N % kVecElems != 0 || !aligned16(a.x) || !aligned16(a.y) || !aligned16(a.w)) return false;
+    if (!vector_ok(a)) return false;
     const int64_t nvec = a.N / kVecElems;
     if (nvec > 1024 * 4) return false;
     int T = k.lanes_per_row;
@@ -139,8 +140,8 @@ cudaError_t cta_run(const Args& a, const Launch& l) {
     LaunchCfg c(l, a.stream, l.pdl);
     return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
-                              a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
-                              a.eps, a.offset, l.mode());
+                              a.M, static_cast<int>(a.N / kVecElems), a.ldx / kVecElems,
+                              a.ldy / kVecElems, static_cast<float>(a.N), a.eps, a.offset, l.mode());
 }
 
 }  // namespace rmsn

@@ -17,8 +17,8 @@ namespace {
 template <int DT, int THREADS>
 __global__ void __launch_bounds__(THREADS)
 generic_rows_kernel(const uint16_t* x, const uint16_t* __restrict__ w, uint16_t* y,
-                    float* __restrict__ rstd, int64_t M, int64_t N, float n, float eps,
-                    float offset) {
+                    float* __restrict__ rstd, int64_t M, int64_t N, int64_t ldx, int64_t ldy,
+                    float n, float eps, float offset) {
     constexpr int kWarps = THREADS / 32;
     __shared__ float part[2][kWarps];
     const int tid = threadIdx.x;
@@ -26,7 +26,7 @@ generic_rows_kernel(const uint16_t* x, const uint16_t* __restrict__ w, uint16_t*
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
-        const uint16_t* xr = x + row * N;
+        const uint16_t* xr = x + row * ldx;
         float ss = 0.f;
         for (int64_t j = tid; j < N; j += THREADS) {
             const float f = Codec<DT>::unpack1(xr[j]);
@@ -40,8 +40,8 @@ generic_rows_kernel(const uint16_t* x, const uint16_t* __restrict__ w, uint16_t*
 #pragma unroll
         for (int k = 0; k < kWarps; ++k) tot += part[parity][k];
         const float r = row_rstd(tot, n, eps);
-        if (tid == 0) rstd[row] = r;
-        uint16_t* yr = y + row * N;
+        if (tid == 0 && rstd != nullptr) rstd[row] = r;
+        uint16_t* yr = y + row * ldy;
         for (int64_t j = tid; j < N; j += THREADS) {
             const float f = Codec<DT>::unpack1(xr[j]);
             const float sw = offset + Codec<DT>::unpack1(__ldg(w + j));
@@ -51,8 +51,8 @@ generic_rows_kernel(const uint16_t* x, const uint16_t* __restrict__ w, uint16_t*
     }
 }
 
-using Fn = void (*)(const uint16_t*, const uint16_t*, uint16_t*, float*, int64_t, int64_t, float,
-                    float, float);
+using Fn = void (*)(const uint16_t*, const uint16_t*, uint16_t*, float*, int64_t, int64_t, int64_t,
+                    int64_t, float, float, float);
 
 template <int DT>
 Fn pick(int T) {
@@ -93,7 +93,8 @@ cudaError_t generic_run(const Args& a, const Launch& l) {
     LaunchCfg c(l, a.stream, l.pdl);
     return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint16_t*>(a.x),
                               static_cast<const uint16_t*>(a.w), static_cast<uint16_t*>(a.y),
-                              a.rstd, a.M, a.N, static_cast<float>(a.N), a.eps, a.offset);
+                              a.rstd, a.M, a.N, a.ldx, a.ldy, static_cast<float>(a.N), a.eps,
+                              a.offset);
 }
 
 }  // namespace rmsn

@@ -47,7 +47,8 @@ __device__ __forceinline__ void team_barrier(int id, int threads) {
 template <int DT, int THREADS, int TEAM, int V>
 __global__ void __launch_bounds__(THREADS)
 tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
-                int64_t M, int nvec, float n, float eps, float offset, int rows_per_stage,
+                int64_t M, int nvec, int64_t ldx, int64_t ldy, float n, float eps, float offset,
+                int rows_per_stage,
                 int stages, int stage_stride, long long limit_cycles, long long drain_cycles,
                 int mode) {
     constexpr int kTeams = THREADS / TEAM;
@@ -105,10 +106,16 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         const int st = static_cast<int>(k % stages);
         const int64_t r0 = chunk_row(k);
         const int64_t rows = (r_end - r0) < R ? (r_end - r0) : R;
-        const uint32_t bytes = static_cast<uint32_t>(rows * nvec * 16);
-        mbar_arrive_expect_tx(bars + 8 * st, bytes);
-        bulk_g2s(smem_u32(buf + static_cast<int64_t>(st) * stage_stride), x + r0 * nvec, bytes,
-                 bars + 8 * st);
+        const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
+        const uint32_t dst = smem_u32(buf + static_cast<int64_t>(st) * stage_stride);
+        mbar_arrive_expect_tx(bars + 8 * st, static_cast<uint32_t>(rows) * row_bytes);
+        if (ldx == nvec) {  // contiguous rows: the whole stage is one span of x
+            bulk_g2s(dst, x + r0 * nvec, static_cast<uint32_t>(rows) * row_bytes, bars + 8 * st);
+        } else {            // strided rows: one copy per row, all counted on the same barrier
+            for (int64_t q = 0; q < rows; ++q)
+                bulk_g2s(dst + static_cast<uint32_t>(q) * row_bytes, x + (r0 + q) * ldx, row_bytes,
+                         bars + 8 * st);
+        }
     };
     if (tid == 0) {
         for (int k = 0; k < stages; ++k) issue(k);
@@ -156,11 +163,11 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
             if (act) {
                 const int64_t row = r0 + rr;
                 const float r = row_rstd(ss, n, eps);
-                if (t == 0) rstd[row] = r;
+                if (t == 0 && rstd != nullptr) rstd[row] = r;
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const int c = v * TEAM + t;
-                    if (c < nvec) st_stream(y + row * nvec + c, scale8<DT>(xv[v], r, s[v]));
+                    if (c < nvec) st_stream(y + row * ldy + c, scale8<DT>(xv[v], r, s[v]));
                 }
             }
         }
@@ -179,8 +186,8 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     }
 }
 
-using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, float, float, float,
-                    int, int, int, long long, long long, int);
+using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, int64_t, int64_t, float,
+                    float, float, int, int, int, long long, long long, int);
 
 template <int DT>
 Fn pick(int team, int V) {
@@ -229,7 +236,7 @@ int next_pow2(int64_t v) {
 }  // namespace
 
 bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
-    if (a.N % kVecElems != 0 || !aligned16(a.x) || !aligned16(a.y) || !aligned16(a.w)) return false;
+    if (!vector_ok(a)) return false;
     const int64_t nvec = a.N / kVecElems;
     int team = k.lanes_per_row;
     if (team == 0) {
@@ -298,8 +305,9 @@ cudaError_t tma_run(const Args& a, const Launch& l) {
     LaunchCfg c(l, a.stream, l.pdl);
     return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
-                              a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
-                              a.eps, a.offset, l.rows_per_stage, l.stages,
+                              a.M, static_cast<int>(a.N / kVecElems), a.ldx / kVecElems,
+                              a.ldy / kVecElems, static_cast<float>(a.N), a.eps, a.offset,
+                              l.rows_per_stage, l.stages,
                               static_cast<int>(stage_stride), limit < 1 ? 1LL : limit, drain,
                               l.mode());
 }

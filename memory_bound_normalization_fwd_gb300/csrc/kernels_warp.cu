@@ -29,7 +29,8 @@ constexpr int kWarps = 8;  // 256 threads per CTA
 template <int DT, int G, int V, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
-                 int64_t M, int nvec, float n, float eps, float offset, int mode) {
+                 int64_t M, int nvec, int64_t ldx, int64_t ldy, float n, float eps, float offset,
+                 int mode) {
     extern __shared__ float4 sw[];  // 2 float4 of (offset + w) per 16-byte vector of w
     constexpr int kTeams = 32 / G;  // rows per warp per pass
     constexpr int kPass = kWarps * kTeams;  // rows per CTA per pass
@@ -72,7 +73,7 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
         for (int v = 0; v < V; ++v) {
             const int c = v * G + sub;
             buf[d][v] = make_uint4(0u, 0u, 0u, 0u);
-            if (row < r_end && c < nvec) buf[d][v] = ld_stream(x + row * nvec + c);
+            if (row < r_end && c < nvec) buf[d][v] = ld_stream(x + row * ldx + c);
         }
     }
     if (early) pdl_wait();  // every store comes after the previous kernel completes
@@ -93,12 +94,12 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
                     ss += __shfl_xor_sync(0xffffffffu, ss, off);
                 if (row < r_end) {
                     const float r = row_rstd(ss, n, eps);
-                    if (sub == 0) rstd[row] = r;
+                    if (sub == 0 && rstd != nullptr) rstd[row] = r;
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
                         const int c = v * G + sub;
                         if (c < nvec)
-                            st_stream(y + row * nvec + c,
+                            st_stream(y + row * ldy + c,
                                       scale8<DT>(buf[d][v], r, sw[2 * c], sw[2 * c + 1]));
                     }
                 }
@@ -107,15 +108,15 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
                 for (int v = 0; v < V; ++v) {
                     const int c = v * G + sub;
                     buf[d][v] = make_uint4(0u, 0u, 0u, 0u);
-                    if (nrow < r_end && c < nvec) buf[d][v] = ld_stream(x + nrow * nvec + c);
+                    if (nrow < r_end && c < nvec) buf[d][v] = ld_stream(x + nrow * ldx + c);
                 }
             }
         }
     }
 }
 
-using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, float, float, float,
-                    int);
+using Fn = void (*)(const uint4*, const uint4*, uint4*, float*, int64_t, int, int64_t, int64_t, float,
+                    float, float, int);
 
 template <int DT, int D>
 Fn pick_d(int G, int V) {
@@ -150,7 +151,7 @@ int next_pow2(int v) {
 }  // namespace
 
 bool warp_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
-    if (a.N % kVecElems != 0 || !aligned16(a.x) || !aligned16(a.y) || !aligned16(a.w)) return false;
+    if (!vector_ok(a)) return false;
     const int64_t nvec = a.N / kVecElems;
     if (nvec > 32 * 4) return false;
     int G, V;
@@ -187,8 +188,8 @@ cudaError_t warp_run(const Args& a, const Launch& l) {
     LaunchCfg c(l, a.stream, l.pdl);
     return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
-                              a.M, static_cast<int>(a.N / kVecElems), static_cast<float>(a.N),
-                              a.eps, a.offset, l.mode());
+                              a.M, static_cast<int>(a.N / kVecElems), a.ldx / kVecElems,
+                              a.ldy / kVecElems, static_cast<float>(a.N), a.eps, a.offset, l.mode());
 }
 
 }  // namespace rmsn

@@ -15,6 +15,8 @@ struct Args {
     float* rstd;
     int64_t M;
     int64_t N;
+    int64_t ldx;  // row stride of x in elements (>= N)
+    int64_t ldy;  // row stride of y in elements (>= N)
     float eps;
     float offset;
     int dtype;  // 0 bf16, 1 fp16
@@ -99,6 +101,14 @@ inline int persistent_grid(int64_t work_items, int64_t items_per_cta, int sm_cou
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The 16-byte-vector kernels need every row of x and y, and w, to start on a
+// 16-byte boundary and N to be a whole number of vectors.
+inline bool vector_ok(const Args& a) {
+    constexpr int64_t kElems = 8;
+    return a.N % kElems == 0 && a.ldx % kElems == 0 && a.ldy % kElems == 0 && aligned16(a.x) &&
+           aligned16(a.y) && aligned16(a.w);
+}
 
 // Launch configuration shared by every variant: programmatic stream
 // serialisation (PDL) unless the caller turned it off.

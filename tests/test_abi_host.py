@@ -69,7 +69,7 @@ def _call(lib, x=X, w=W_, y=Y, r=R, M=4, N=8, eps=1e-6, off=0.0, dt=0, opts=None
     (dict(M=-1), -2), (dict(N=0), -2), (dict(N=-5), -2), (dict(M=1 << 62, N=4), -2),
     (dict(eps=-1e-6), -4), (dict(eps=float("nan")), -4), (dict(eps=float("inf")), -4),
     (dict(off=float("nan")), -4), (dict(off=float("inf")), -4),
-    (dict(w=0), -1), (dict(x=0), -1), (dict(y=0), -1), (dict(r=0), -1),
+    (dict(w=0), -1), (dict(x=0), -1), (dict(y=0), -1),
     (dict(x=X + 1), -10), (dict(y=Y + 1), -10), (dict(w=W_ + 1), -10), (dict(r=R + 2), -10),
     (dict(y=X + 2), -5),            # y overlaps x without being equal to it
     (dict(r=X + 16), -5),           # rstd inside x
@@ -82,8 +82,26 @@ def test_validation_errors(lib, kw, code):
     assert B.rmsnorm_last_error() != ""
 
 
+def _call_strided(lib, x=X, ldx=8, w=W_, y=Y, ldy=8, r=R, M=4, N=8, opts=None):
+    return B.rmsnorm_fwd_strided(x, ldx, w, y, ldy, r, M, N, 1e-6, 0.0, 0, opts, 0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ldx=7), -2), (dict(ldy=4), -2), (dict(ldx=-8), -2),
+    (dict(ldx=1 << 45, M=1 << 3), -2),            # span beyond 2^48 bytes
+    (dict(y=X, ldx=16, ldy=8), -5),                # in place with different strides
+    (dict(y=X + 2 * 8, ldx=16, ldy=16), -5),       # interleaved rows: spans overlap
+    (dict(r=X + 3 * 16 * 2, ldx=16), -5),          # rstd inside the span of x
+    (dict(x=0), -1), (dict(w=X + 1), -10),
+])
+def test_strided_validation_errors(lib, kw, code):
+    assert _call_strided(lib, **kw) == code
+    assert B.rmsnorm_last_error() != ""
+
+
 def test_m_zero_is_ok_without_buffers(lib):
     assert _call(lib, x=0, y=0, r=0, M=0) == 0
+    assert _call_strided(lib, x=0, y=0, r=0, M=0, ldx=100, ldy=9) == 0
 
 
 @pytest.mark.parametrize("field,value", [("variant", 6), ("variant", -1), ("max_ctas", -1),

@@ -364,3 +364,76 @@ def test_cluster_bounded_wait_reports_timeout_and_recovers():
     y, r = case.results()
     yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "bf16")
     compare(y, r, yo, ro, "bf16")
+
+
+# ---------------------------------------------------------------- strided rows, no rstd
+
+def _strided_case(x, w, dtype, ldx, ldy, col0=0):
+    """x rows inside a wider [M, ldx] buffer (canaries in the gaps), y into a [M, ldy] one."""
+    M, N = x.shape
+    nan = 0x7FC1 if dtype == "bf16" else 0x7E01
+    xb = np.full((M, ldx + col0), nan, dtype=np.uint16)
+    xb[:, col0:col0 + N] = x
+    yb = np.full((M, ldy + col0), 0x5A5A, dtype=np.uint16)
+    xd = W.to_torch(xb, dtype).cuda()
+    yd = W.to_torch(yb, dtype).cuda()
+    return xb, yb, xd, yd
+
+
+@pytest.mark.parametrize("variant,N,ldx,ldy", [
+    ("warp", 512, 640, 520), ("warp", 1000, 1000, 1024), ("cta", 8192, 8200, 8192),
+    ("tma", 512, 520, 640), ("tma", 4096, 4104, 4096), ("tma", 8192, 16384, 8200),
+    ("cluster", 65536, 65544, 65536), ("generic", 512, 513, 517), ("auto", 512, 513, 512),
+    ("auto", 1000, 1008, 1000), ("auto", 8192, 8192, 8192)])
+def test_strided_rows(variant, N, ldx, ldy):
+    M = 300 if N < 65536 else 24
+    wl = W.custom(M, N, "bf16", seed=N + ldx, offset=1.0)
+    x, w = W.generate(wl)
+    xb, yb, xd, yd = _strided_case(x, w, "bf16", ldx, ldy)
+    wd = W.to_torch(w, "bf16").cuda()
+    rd = torch.full((M,), -1.0, dtype=torch.float32, device="cuda")
+    for early in (False, True):
+        o = B.make_options(variant=variant, early_loads=early)
+        rc = B.rmsnorm_fwd_strided(xd.data_ptr(), ldx, wd.data_ptr(), yd.data_ptr(), ldy,
+                                   rd.data_ptr(), M, N, wl.eps, wl.offset, B.BF16, o,
+                                   torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, B.rmsnorm_last_error()
+        torch.cuda.synchronize()
+        yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "bf16")
+        yg = W.from_torch(yd).reshape(M, ldy)
+        compare(yg[:, :N], rd.cpu().numpy(), yo, ro, "bf16", where=f"{variant} ld {ldx}/{ldy}")
+        assert np.all(yg[:, N:] == 0x5A5A), "y written between rows"
+        assert np.array_equal(W.from_torch(xd).reshape(M, ldx), xb), "x changed"
+
+
+def test_strided_in_place_and_torch_views():
+    M, N, K = 257, 1024, 1536
+    wl = W.custom(M, N, "fp16", seed=77, x_std=20.0)
+    x, w = W.generate(wl)
+    full = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    full[:, 256:256 + N] = W.to_torch(x, "fp16").cuda()
+    view = full[:, 256:256 + N]          # rows of a wider tensor, 16-byte aligned
+    wd = W.to_torch(w, "fp16").cuda()
+    y, r = B.fwd(view, wd, eps=wl.eps, offset=wl.offset, y=view)   # in place, strided
+    torch.cuda.synchronize()
+    yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "fp16")
+    compare(W.from_torch(full[:, 256:256 + N].contiguous()), r.cpu().numpy(), yo, ro, "fp16")
+    assert torch.count_nonzero(full[:, :256]) == 0 and torch.count_nonzero(full[:, 256 + N:]) == 0
+
+
+@pytest.mark.parametrize("variant,N", [("warp", 512), ("tma", 1000), ("cta", 8192),
+                                       ("cluster", 65536), ("generic", 777)])
+def test_rstd_null_skips_the_store(variant, N):
+    M = 200 if N < 65536 else 16
+    wl = W.custom(M, N, "bf16", seed=N + 3)
+    x, w = W.generate(wl)
+    case = DeviceCase(x, w, "bf16")
+    o = B.make_options(variant=variant)
+    rc = B.rmsnorm_fwd_ex(case.x.data_ptr(), case.w.data_ptr(), case.y.data_ptr(), 0, M, N,
+                          wl.eps, wl.offset, B.BF16, o, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, B.rmsnorm_last_error()
+    y, r = case.results()
+    assert np.all(r == -12345.0)          # the rstd buffer was never written
+    case.check_guards()
+    yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "bf16")
+    compare(y, ro, yo, ro, "bf16")
