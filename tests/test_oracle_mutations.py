@@ -1,0 +1,162 @@
+"""The oracle's pins are sensitive: each plausible slip, planted in a scratch
+copy of the oracle's C source, compiled on the CPU, must fail them.
+
+The mutants never touch the repository's oracle; they live in a temporary
+directory for the length of the test.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from exact import decode_exact, rmsnorm_row_exact, round_exact
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle",
+                   "rmsnorm_oracle.c")
+
+MUTATIONS = {
+    "eps outside the root": ("double r = 1.0 / sqrt(ms + e);", "double r = 1.0 / sqrt(ms) + e;"),
+    "eps dropped": ("double r = 1.0 / sqrt(ms + e);", "double r = 1.0 / sqrt(ms);"),
+    "divides by the padded width": ("double ms = s / (double)N;",
+                                    "double ms = s / (double)((N + 7) / 8 * 8);"),
+    "offset multiplied": ("double scale = off + dec(w[j]);",
+                          "double scale = (off == 0.0 ? 1.0 : off) * dec(w[j]);"),
+    "weight indexed by row": ("double scale = off + dec(w[j]);",
+                              "double scale = off + dec(w[(i + j) % N]);"),
+    "double rounding through fp32": ("if (y) y[i * N + j] = enc(v);",
+                                     "if (y) y[i * N + j] = enc((double)(float)v);"),
+    "ties rounded down": ("if (rem > 0.5 || (rem == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;",
+                          "if (rem > 0.5) n += 1.0;"),
+    "sign of x lost": ("double v = dec(xi[j]) * r * scale;",
+                       "double v = fabs(dec(xi[j])) * r * scale;"),
+    "sum of |x| instead of x^2": ("s += v * v;", "s += fabs(v);"),
+    "wrong row stride": ("const uint16_t* xi = x + i * N;",
+                         "const uint16_t* xi = x + i * (N > 1 ? N - 1 : N);"),
+    "subnormal quantum off by one": ("if (e < emin) e = emin;", "if (e < emin - 1) e = emin - 1;"),
+    "mean over N+1": ("double ms = s / (double)N;", "double ms = s / (double)(N + 1);"),
+}
+
+
+def _build(tmp, source: str) -> ctypes.CDLL:
+    c = os.path.join(tmp, "m.c")
+    so = os.path.join(tmp, f"m{abs(hash(source))}.so")
+    with open(c, "w") as f:
+        f.write(source)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", so,
+                    c, "-lm"], check=True)
+    L = ctypes.CDLL(so)
+    u16p, f64p = ctypes.POINTER(ctypes.c_uint16), ctypes.POINTER(ctypes.c_double)
+    L.oracle_rmsnorm_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int64,
+                                     ctypes.c_int64]
+    L.oracle_encode.argtypes = [ctypes.c_int, ctypes.c_int64, f64p, u16p]
+    return L
+
+
+def _fwd(L, x, w, eps, offset, dtype):
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    M, N = x.shape
+    y = np.zeros((M, N), dtype=np.uint16)
+    r = np.zeros(M, dtype=np.float64)
+    u16p, f64p = ctypes.POINTER(ctypes.c_uint16), ctypes.POINTER(ctypes.c_double)
+    rc = L.oracle_rmsnorm_fwd(x.ctypes.data_as(u16p), np.ascontiguousarray(w).ctypes.data_as(u16p),
+                              y.ctypes.data_as(u16p), r.ctypes.data_as(f64p), None, M, N, eps,
+                              offset, 0 if dtype == "bf16" else 1, 0, M)
+    assert rc == 0
+    return y, r
+
+
+def _bits(dtype, values):
+    return np.array([round_exact(dtype, Fraction(float(v))) for v in values], dtype=np.uint16)
+
+
+def _pins_hold(L) -> bool:
+    """A compact battery drawn from the oracle pins: exact rationals on random
+    tiny rows (both dtypes, both offsets, several eps), constant rows at
+    non-power-of-two N, and round-to-nearest-even at every bf16/fp16 midpoint
+    between 1 and 2."""
+    rng = np.random.default_rng(3)
+    for dtype in ("bf16", "fp16"):
+        for N in (1, 3, 7, 12, 33):
+            M = 3
+            x = _bits(dtype, rng.normal(0, 1.5, M * N).astype(np.float32)).reshape(M, N)
+            w = _bits(dtype, rng.normal(0, 0.7, N).astype(np.float32))
+            for eps, offset in ((0.0, 0.0), (1e-5, 1.0), (0.25, 0.0)):
+                y, r = _fwd(L, x, w, eps, offset, dtype)
+                wv = [decode_exact(dtype, int(b)) for b in w]
+                for i in range(M):
+                    xv = [decode_exact(dtype, int(b)) for b in x[i]]
+                    rr, ys = rmsnorm_row_exact(xv, wv, Fraction(float(np.float32(eps))),
+                                               Fraction(offset))
+                    if rr is None:
+                        continue
+                    if not math.isclose(r[i], float(rr), rel_tol=1e-14):
+                        return False
+                    for j, v in enumerate(ys):
+                        got = decode_exact(dtype, int(y[i, j]))
+                        if v == 0:
+                            if got != 0:
+                                return False
+                        elif int(y[i, j]) != round_exact(dtype, v):
+                            return False
+        # constant rows: r = 1/sqrt(c^2 + eps) at a non-power-of-two N
+        c = 0.5
+        x = np.full((1, 1000), _bits(dtype, [c])[0], dtype=np.uint16)
+        w = _bits(dtype, [1.0] * 1000)
+        _, r = _fwd(L, x, w, 1e-6, 0.0, dtype)
+        if not math.isclose(r[0], 1 / math.sqrt(c * c + float(np.float32(1e-6))), rel_tol=1e-14):
+            return False
+        # ties to even at every midpoint in [1, 2)
+        mbits = 7 if dtype == "bf16" else 10
+        k = np.arange(1 << mbits, dtype=np.float64)
+        mids = 1.0 + (k + 0.5) / (1 << mbits)
+        out = np.zeros(mids.size, dtype=np.uint16)
+        L.oracle_encode(0 if dtype == "bf16" else 1, mids.size,
+                        mids.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                        out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)))
+        want = [round_exact(dtype, Fraction(float(m))) for m in mids]
+        if out.tolist() != want:
+            return False
+        # every finite pattern round-trips through the encoder
+        pats = np.arange(0x7F80 if dtype == "bf16" else 0x7C00, dtype=np.uint16)
+        vals = np.array([float(decode_exact(dtype, int(b))) for b in pats])
+        back = np.zeros(pats.size, dtype=np.uint16)
+        L.oracle_encode(0 if dtype == "bf16" else 1, vals.size,
+                        vals.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                        back.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)))
+        if not np.array_equal(back, pats):
+            return False
+        # a product just below a tie rounds down (one rounding, not two)
+        if not _just_below_tie_rounds_down(L, dtype):
+            return False
+    return True
+
+
+def _just_below_tie_rounds_down(L, dtype) -> bool:
+    # x = (1, 1, 1, 1), eps = 2^-30: rstd = 1/sqrt(1 + 2^-30), just under 1. With
+    # offset 1 and w = 3 ulp/2 the exact y sits 2^-31 below the midpoint between
+    # 1 + 1 ulp (odd) and 1 + 2 ulp (even): it must round down to 1 + 1 ulp,
+    # while rounding through fp32 first lands on the midpoint and goes up.
+    ulp = 2.0 ** -7 if dtype == "bf16" else 2.0 ** -10
+    x = _bits(dtype, [1.0] * 4).reshape(1, 4)
+    w = _bits(dtype, [1.5 * ulp] * 4)
+    y, _ = _fwd(L, x, w, 2.0 ** -30, 1.0, dtype)
+    return y[0].tolist() == [round_exact(dtype, Fraction(1) + Fraction(ulp))] * 4
+
+
+def test_the_oracle_itself_passes_the_battery(tmp_path):
+    assert _pins_hold(_build(str(tmp_path), open(SRC).read()))
+
+
+@pytest.mark.parametrize("name", list(MUTATIONS))
+def test_each_planted_slip_fails_the_pins(tmp_path, name):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found: {old}"
+    assert not _pins_hold(_build(str(tmp_path), src.replace(old, new)))

@@ -338,3 +338,19 @@ def test_eps_is_taken_as_float32():
     w = _bits_of("bf16", [1, 1])
     _, r = oracle.rmsnorm_fwd(x[None, :], w, 1e-6, 0.0, "bf16")
     assert r[0] == 1.0 / math.sqrt(float(F32(1e-6)))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_single_rounding_just_below_a_tie(dtype):
+    # x = (1, 1, 1, 1), eps = 2^-30 (exact in fp32), offset 1, w = 1.5 ulp(1):
+    # y = (1 + 1.5 ulp) / sqrt(1 + 2^-30) lies about 2^-31 below the midpoint
+    # between 1 + ulp (odd significand) and 1 + 2 ulp, so the one rounding the
+    # pages' cast implies gives 1 + ulp. Rounding through fp32 first would land
+    # exactly on the midpoint and round up to the even neighbour instead.
+    ulp = 2.0 ** -7 if dtype == "bf16" else 2.0 ** -10
+    x = _bits_of(dtype, [1] * 4)[None, :]
+    w = _bits_of(dtype, [Fraction(3, 2) * Fraction(ulp)] * 4)
+    y, r, y64 = oracle.rmsnorm_fwd(x, w, 2.0 ** -30, 1.0, dtype, want_y64=True)
+    mid = 1 + 1.5 * ulp
+    assert y64[0, 0] < mid and mid - y64[0, 0] < 2.0 ** -30
+    assert [decode_exact(dtype, int(b)) for b in y[0]] == [1 + Fraction(ulp)] * 4
