@@ -52,6 +52,10 @@ def lib() -> ctypes.CDLL:
                                              ctypes.c_int64, ctypes.c_float, ctypes.c_float,
                                              ctypes.c_int, ctypes.c_int64, ctypes.c_int64]
             L.oracle_rmsnorm_fwd.restype = ctypes.c_int
+            L.oracle_rmsnorm_bwd.argtypes = [u16p, u16p, u16p, f64p, u16p, f64p, f64p,
+                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+                                             ctypes.c_float, ctypes.c_int]
+            L.oracle_rmsnorm_bwd.restype = ctypes.c_int
             L.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_int64, u16p, f64p]
             L.oracle_decode.restype = ctypes.c_int
             L.oracle_encode.argtypes = [ctypes.c_int, ctypes.c_int64, f64p, u16p]
@@ -125,3 +129,28 @@ def rmsnorm_fwd_into(x_bits: np.ndarray, w_bits: np.ndarray, y_out: np.ndarray,
                                   _ptr(y_out, ctypes.c_uint16), _ptr(rstd_out, ctypes.c_double),
                                   None, M, N, eps, offset, _DTYPES[dtype], row0, row1)
     assert rc == 0
+
+
+def rmsnorm_bwd(x_bits: np.ndarray, w_bits: np.ndarray, dy_bits: np.ndarray, offset: float,
+                dtype: str, rstd: np.ndarray | None = None, eps: float = 0.0):
+    """Backward of the forward above (derived by the chain rule; see the C file).
+
+    ``rstd`` (per row, any float array) is the saved rstd the backward consumes;
+    None recomputes it in fp64 from x and ``eps``. Returns ``(dx_bits, dx_f64,
+    dw_f64)``.
+    """
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    dy_bits = np.ascontiguousarray(dy_bits, dtype=np.uint16)
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    M, N = x_bits.shape
+    assert dy_bits.shape == (M, N) and w_bits.shape == (N,)
+    r = None if rstd is None else np.ascontiguousarray(rstd, dtype=np.float64)
+    dx = np.zeros((M, N), dtype=np.uint16)
+    dx64 = np.zeros((M, N), dtype=np.float64)
+    dw = np.zeros(N, dtype=np.float64)
+    rc = lib().oracle_rmsnorm_bwd(_ptr(x_bits, ctypes.c_uint16), _ptr(w_bits, ctypes.c_uint16),
+                                  _ptr(dy_bits, ctypes.c_uint16), _ptr(r, ctypes.c_double),
+                                  _ptr(dx, ctypes.c_uint16), _ptr(dx64, ctypes.c_double),
+                                  _ptr(dw, ctypes.c_double), M, N, eps, offset, _DTYPES[dtype])
+    assert rc == 0
+    return dx, dx64, dw

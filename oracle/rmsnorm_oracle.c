@@ -188,3 +188,56 @@ int oracle_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, double
     }
     return 0;
 }
+
+/* ---- the backward (derived; the pages only say rstd is kept for it) ----
+ *
+ * For y_ij = x_ij * r_i * s_j with s_j = offset + w_j and
+ * r_i = (sum_k x_ik^2 / N + eps)^(-1/2), the chain rule gives, for an
+ * upstream gradient dy:
+ *
+ *   c_i    = sum_j dy_ij * s_j * x_ij
+ *   dx_ij  = r_i * (dy_ij * s_j - x_ij * r_i^2 * c_i / N)
+ *   dw_j   = sum_i dy_ij * x_ij * r_i
+ *
+ * (d r_i / d x_ik = -r_i^3 x_ik / N.) r_i is the saved rstd: the caller passes
+ * it (as the CUDA backward receives it), or NULL to recompute it here in fp64
+ * from x and eps. dx is returned rounded to the dtype (one rounding) and in
+ * fp64; dw in fp64, summed over rows in index order.
+ */
+int oracle_rmsnorm_bwd(const uint16_t* x, const uint16_t* w, const uint16_t* dy,
+                       const double* rstd, uint16_t* dx, double* dx_f64, double* dw,
+                       int64_t M, int64_t N, float eps, float offset, int dtype)
+{
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16) return -1;
+    if (M < 0 || N <= 0) return -1;
+    double (*dec)(uint16_t) = dtype == ORACLE_BF16 ? oracle_bf16_to_f64 : oracle_f16_to_f64;
+    uint16_t (*enc)(double) = dtype == ORACLE_BF16 ? oracle_f64_to_bf16 : oracle_f64_to_f16;
+    const double off = (double)offset;
+    if (dw)
+        for (int64_t j = 0; j < N; ++j) dw[j] = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        const uint16_t* xi = x + i * N;
+        const uint16_t* gi = dy + i * N;
+        double r;
+        if (rstd) {
+            r = rstd[i];
+        } else {
+            double s = 0.0;
+            for (int64_t j = 0; j < N; ++j) {
+                double v = dec(xi[j]);
+                s += v * v;
+            }
+            r = 1.0 / sqrt(s / (double)N + (double)eps);
+        }
+        double c = 0.0;
+        for (int64_t j = 0; j < N; ++j) c += dec(gi[j]) * (off + dec(w[j])) * dec(xi[j]);
+        for (int64_t j = 0; j < N; ++j) {
+            double xv = dec(xi[j]), gv = dec(gi[j]), sv = off + dec(w[j]);
+            double v = r * (gv * sv - xv * r * r * c / (double)N);
+            if (dx_f64) dx_f64[i * N + j] = v;
+            if (dx) dx[i * N + j] = enc(v);
+            if (dw) dw[j] += gv * xv * r;
+        }
+    }
+    return 0;
+}
