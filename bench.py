@@ -35,7 +35,8 @@ sys.path.insert(0, ROOT)
 METRIC = "RMSNorm fwd achieved HBM GB/s and % of GB300 peak (1 GPU), per M×N×dtype"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["common.cuh", "async_copy.cuh", "launch.h", "kernels_warp.cu", "kernels_cta.cu",
-                  "kernels_tma.cu", "kernels_cluster.cu", "kernels_generic.cu", "api.cu"]
+                  "kernels_tma.cu", "kernels_cluster.cu", "kernels_generic.cu", "kernels_bwd.cu",
+                  "api.cu"]
 
 
 # ---------------------------------------------------------------- host-side helpers
@@ -61,6 +62,8 @@ def parse_args(argv=None):
     p.add_argument("--cluster-size", type=int, default=0)
     p.add_argument("--ablation", action="store_true",
                    help="time a matrix of kernel variants and knobs per workload, one JSON line each")
+    p.add_argument("--backward", action="store_true",
+                   help="time the backward (dx, dw) on the workload instead of the forward")
     return p.parse_args(argv)
 
 
@@ -496,6 +499,74 @@ def run_ablation(args, names):
         torch.cuda.empty_cache()
 
 
+# ---------------------------------------------------------------- backward
+
+def bench_backward(args, wl):
+    """Throughput of rmsnorm_bwd on the workload: algorithmic bytes per step =
+    x, dy read and dx written (6 M N) + rstd read (4 M) + w read (2 N) + dw
+    written (4 N); the dw partials in the workspace are not counted."""
+    import torch
+    from memory_bound_normalization_fwd_gb300 import binding as B
+    from memory_bound_normalization_fwd_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    dcode = B.BF16 if wl.dtype == "bf16" else B.FP16
+    x_bits, w_bits = W.generate(wl)
+    dy_bits, _ = W.generate(W.custom(wl.M, wl.N, wl.dtype, seed=99))
+    x0, dy0 = W.to_torch(x_bits, wl.dtype).to(dev), W.to_torch(dy_bits, wl.dtype).to(dev)
+    w = W.to_torch(w_bits, wl.dtype).to(dev)
+    r0 = torch.empty(wl.M, dtype=torch.float32, device=dev)
+    B.fwd(x0, w, eps=wl.eps, offset=wl.offset, y=torch.empty_like(x0), rstd=r0)
+    set_bytes = 6 * wl.M * wl.N + 4 * wl.M
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool = max(2, -(-3 * l2 // set_bytes))
+    xs = [x0.clone() for _ in range(pool)]
+    dys = [dy0.clone() for _ in range(pool)]
+    dxs = [torch.empty_like(x0) for _ in range(pool)]
+    rs = [r0.clone() for _ in range(pool)]
+    dw = torch.empty(wl.N, dtype=torch.float32, device=dev)
+    nbytes = B.rmsnorm_bwd_workspace_size(wl.M, wl.N, dcode)
+    ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+
+    def step(k):
+        i = k % pool
+        rc = B.rmsnorm_bwd(xs[i].data_ptr(), w.data_ptr(), rs[i].data_ptr(), dys[i].data_ptr(),
+                           dxs[i].data_ptr(), dw.data_ptr(), wl.M, wl.N, wl.offset, dcode,
+                           ws.data_ptr(), ws.numel() * 4, None, sh)
+        if rc != 0:
+            raise RuntimeError(B.rmsnorm_last_error())
+
+    with torch.cuda.stream(stream):
+        for k in range(8):
+            step(k)
+    torch.cuda.synchronize()
+    per = pool * max(1, 128 // pool)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for k in range(per):
+            step(k)
+    K = max(per, args.steps // per * per)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(K // per):
+            g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    sec = a.elapsed_time(b) / 1e3
+    step_bytes = 6 * wl.M * wl.N + 4 * wl.M + 2 * wl.N + 4 * wl.N
+    peak, _ = load_peaks()
+    gbs = step_bytes * K / sec / 1e9
+    return {"backward": wl.name, "value": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak, 4),
+            "steps": K, "ms_per_step": round(sec * 1e3 / K, 5), "bytes_per_step": step_bytes,
+            "workspace_bytes": nbytes,
+            "l2": f"rotating pool of {pool} sets ({pool * set_bytes / 1e6:.0f} MB) > 3x L2"}
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 
 def bench_reference(args, wl):
@@ -534,6 +605,11 @@ def main(argv=None):
     from memory_bound_normalization_fwd_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload or W.BENCH_WORKLOAD]
     rank, world, local_rank = dist_env()
+
+    if args.backward:
+        for name in ([args.workload] if args.workload else list(W.WORKLOADS)):
+            print(json.dumps(bench_backward(args, W.WORKLOADS[name])), flush=True)
+        return 0
 
     if args.ablation:
         run_ablation(args, [args.workload] if args.workload else list(W.WORKLOADS))

@@ -75,7 +75,8 @@ typedef enum rmsnorm_status {
     RMSNORM_ERR_DEVICE_TIMEOUT = -7, /* a kernel's bounded wait ran out (see rmsnorm_check_device_status) */
     RMSNORM_ERR_UNSUPPORTED = -8,    /* the forced variant cannot take these arguments */
     RMSNORM_ERR_OPTIONS = -9,        /* malformed rmsnorm_options_t */
-    RMSNORM_ERR_ALIGN = -10          /* x, w or y not 2-byte aligned, or rstd not 4-byte aligned */
+    RMSNORM_ERR_ALIGN = -10,         /* x, w or y not 2-byte aligned, or rstd not 4-byte aligned */
+    RMSNORM_ERR_WORKSPACE = -11      /* the backward's workspace is smaller than it needs */
 } rmsnorm_status_t;
 
 /* Kernel variants. RMSNORM_VARIANT_AUTO lets the planner choose. */
@@ -180,6 +181,37 @@ int rmsnorm_fwd_strided(const void* x, int64_t ldx, const void* w, void* y, int6
  * and may be any values with the alignment the real call will have. */
 int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void* w,
                       const void* y, const rmsnorm_options_t* opts, rmsnorm_plan_t* out);
+
+/*
+ * Backward, consuming the rstd the forward kept. The pages state only that
+ * rstd is kept "for backward"; the formulas are the chain rule of the forward
+ * above (s_j = offset + w_j):
+ *   c_i   = sum_j dy[i,j] * s_j * x[i,j]
+ *   dx    = rstd[i] * (dy[i,j] * s_j - x[i,j] * rstd[i]^2 * c_i / N)   (x's dtype)
+ *   dw[j] = sum_i dy[i,j] * x[i,j] * rstd[i]                              (fp32)
+ * fp32 arithmetic; dx rounded once to nearest even; dw summed per CTA over its
+ * rows, then over CTAs in index order (deterministic for a fixed device).
+ *   x, dy, dx  [M, N] x's dtype, contiguous; dx may equal x or dy exactly
+ *   w          [N]    x's dtype
+ *   rstd       [M]    fp32, as written by rmsnorm_fwd
+ *   dw         [N]    fp32 output (overwritten; zero when M == 0)
+ *   workspace  device scratch of at least rmsnorm_bwd_workspace_size() bytes,
+ *              16-byte aligned, owned by the caller; its contents are
+ *              overwritten. Calls sharing one workspace must not overlap on
+ *              the GPU (one stream, or ordered streams).
+ * Rows of up to 16384 columns (N % 8 == 0, 16-byte aligned buffers) take the
+ * vector kernel; others the general kernel, which keeps a row's dw partial in
+ * shared memory (N up to about 56K). Options: variant AUTO, CTA or GENERIC,
+ * lanes_per_row (threads per CTA), max_ctas, RMSNORM_FLAG_NO_PDL.
+ */
+int rmsnorm_bwd(const void* x, const void* w, const float* rstd, const void* dy, void* dx,
+                float* dw, int64_t M, int64_t N, float offset, int dtype, void* workspace,
+                int64_t workspace_bytes, const rmsnorm_options_t* opts, void* stream);
+
+/* Bytes of workspace rmsnorm_bwd needs for these sizes and options on the
+ * current device, for any buffer alignment (written to *bytes). */
+int rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype, const rmsnorm_options_t* opts,
+                               int64_t* bytes);
 
 /* Synchronises `stream`, then reads and clears the current device's status
  * word. Returns RMSNORM_OK, RMSNORM_ERR_DEVICE_TIMEOUT if any kernel since the

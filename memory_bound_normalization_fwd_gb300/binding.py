@@ -21,12 +21,12 @@ STATUS = {
     0: "RMSNORM_OK", -1: "RMSNORM_ERR_NULL", -2: "RMSNORM_ERR_SHAPE", -3: "RMSNORM_ERR_DTYPE",
     -4: "RMSNORM_ERR_SCALAR", -5: "RMSNORM_ERR_OVERLAP", -6: "RMSNORM_ERR_CUDA",
     -7: "RMSNORM_ERR_DEVICE_TIMEOUT", -8: "RMSNORM_ERR_UNSUPPORTED", -9: "RMSNORM_ERR_OPTIONS",
-    -10: "RMSNORM_ERR_ALIGN",
+    -10: "RMSNORM_ERR_ALIGN", -11: "RMSNORM_ERR_WORKSPACE",
 }
 # Every function include/rmsnorm.h declares.
-EXPORTS = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_strided", "rmsnorm_plan_info",
-           "rmsnorm_check_device_status", "rmsnorm_strerror", "rmsnorm_last_error",
-           "rmsnorm_version")
+EXPORTS = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_strided", "rmsnorm_bwd",
+           "rmsnorm_bwd_workspace_size", "rmsnorm_plan_info", "rmsnorm_check_device_status",
+           "rmsnorm_strerror", "rmsnorm_last_error", "rmsnorm_version")
 
 
 class RMSNormError(RuntimeError):
@@ -82,6 +82,12 @@ def lib() -> ctypes.CDLL:
             L.rmsnorm_fwd_strided.argtypes = [vp, i64, vp, vp, i64, vp, i64, i64, f32, f32, i32,
                                               ctypes.POINTER(Options), vp]
             L.rmsnorm_fwd_strided.restype = i32
+            L.rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp, i64,
+                                      ctypes.POINTER(Options), vp]
+            L.rmsnorm_bwd.restype = i32
+            L.rmsnorm_bwd_workspace_size.argtypes = [i64, i64, i32, ctypes.POINTER(Options),
+                                                     ctypes.POINTER(ctypes.c_int64)]
+            L.rmsnorm_bwd_workspace_size.restype = i32
             L.rmsnorm_plan_info.argtypes = [i64, i64, i32, vp, vp, vp, ctypes.POINTER(Options),
                                             ctypes.POINTER(Plan)]
             L.rmsnorm_plan_info.restype = i32
@@ -137,6 +143,22 @@ def rmsnorm_fwd_strided(x: int, ldx: int, w: int, y: int, ldy: int, rstd: int, M
                         stream: int) -> int:
     return lib().rmsnorm_fwd_strided(x, ldx, w, y, ldy, rstd, M, N, eps, offset, dtype,
                                      ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def rmsnorm_bwd(x: int, w: int, rstd: int, dy: int, dx: int, dw: int, M: int, N: int,
+                offset: float, dtype: int, workspace: int, workspace_bytes: int,
+                opts: Options | None, stream: int) -> int:
+    return lib().rmsnorm_bwd(x, w, rstd, dy, dx, dw, M, N, offset, dtype, workspace,
+                             workspace_bytes, ctypes.byref(opts) if opts is not None else None,
+                             stream)
+
+
+def rmsnorm_bwd_workspace_size(M: int, N: int, dtype: int, opts: Options | None = None) -> int:
+    out = ctypes.c_int64(0)
+    _check(lib().rmsnorm_bwd_workspace_size(M, N, dtype,
+                                            ctypes.byref(opts) if opts is not None else None,
+                                            ctypes.byref(out)))
+    return out.value
 
 
 def rmsnorm_plan_info(M: int, N: int, dtype: int, x: int = 0, w: int = 0, y: int = 0,
@@ -213,3 +235,26 @@ def fwd(x, w, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=None, stream=
         _check(rmsnorm_fwd_strided(x.data_ptr(), ldx, w.data_ptr(), y.data_ptr(), ldy, r_ptr, M,
                                    N, eps, offset, _dtype_code(x), opts, s.cuda_stream))
     return y, (None if rstd is False else rstd)
+
+
+def bwd(x, w, rstd, dy, offset: float = 0.0, dx=None, stream=None, **options):
+    """dx, dw = bwd(x, w, rstd, dy): backward of ``fwd`` for contiguous CUDA tensors.
+
+    The fp32 workspace for the dw partials is allocated here with torch (the C
+    library never allocates); dw comes back in fp32.
+    """
+    import torch
+    N = x.shape[-1]
+    M = x.numel() // N if N else 0
+    if dx is None:
+        dx = torch.empty_like(x)
+    dw = torch.empty(N, dtype=torch.float32, device=x.device)
+    opts = make_options(**options) if options else None
+    with torch.cuda.device(x.device):
+        nbytes = rmsnorm_bwd_workspace_size(M, N, _dtype_code(x), opts)
+        ws = torch.empty((nbytes + 15) // 16 * 4, dtype=torch.float32, device=x.device)
+        s = stream if stream is not None else torch.cuda.current_stream(x.device)
+        _check(rmsnorm_bwd(x.data_ptr(), w.data_ptr(), rstd.data_ptr(), dy.data_ptr(),
+                           dx.data_ptr(), dw.data_ptr(), M, N, offset, _dtype_code(x),
+                           ws.data_ptr(), ws.numel() * 4, opts, s.cuda_stream))
+    return dx, dw

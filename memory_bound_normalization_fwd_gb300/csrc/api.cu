@@ -255,6 +255,120 @@ extern "C" int rmsnorm_fwd_strided(const void* x, int64_t ldx, const void* w, vo
     return forward(x, ldx, w, y, ldy, rstd, M, N, eps, offset, dtype, opts, stream);
 }
 
+// ---- backward ---------------------------------------------------------------
+
+namespace {
+
+int bwd_validate(const void* x, const void* w, const float* rstd, const void* dy, void* dx,
+                 float* dw, int64_t M, int64_t N, float offset, int dtype, const void* ws) {
+    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16)
+        return fail(RMSNORM_ERR_DTYPE, "dtype %d is not RMSNORM_DTYPE_BF16 (0) or _FP16 (1)", dtype);
+    if (M < 0 || N <= 0)
+        return fail(RMSNORM_ERR_SHAPE, "need M >= 0 and N > 0 (got M=%lld N=%lld)",
+                    static_cast<long long>(M), static_cast<long long>(N));
+    if (M > 0 && (N > (int64_t(1) << 47) / M || M > (int64_t(1) << 46)))
+        return fail(RMSNORM_ERR_SHAPE, "x would exceed 2^48 bytes");
+    if (!std::isfinite(offset)) return fail(RMSNORM_ERR_SCALAR, "offset must be finite");
+    if (w == nullptr || dw == nullptr) return fail(RMSNORM_ERR_NULL, "w and dw must be non-NULL");
+    if (M > 0 && (x == nullptr || dy == nullptr || dx == nullptr || rstd == nullptr ||
+                  ws == nullptr))
+        return fail(RMSNORM_ERR_NULL, "x, rstd, dy, dx and the workspace must be non-NULL");
+    const uintptr_t a2 = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
+                         reinterpret_cast<uintptr_t>(dy) | reinterpret_cast<uintptr_t>(dx);
+    if (a2 & 1u) return fail(RMSNORM_ERR_ALIGN, "x, w, dy and dx must be 2-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(rstd) | reinterpret_cast<uintptr_t>(dw)) & 3u)
+        return fail(RMSNORM_ERR_ALIGN, "rstd and dw must be 4-byte aligned");
+    if (reinterpret_cast<uintptr_t>(ws) & 15u)
+        return fail(RMSNORM_ERR_ALIGN, "the workspace must be 16-byte aligned");
+    if (M == 0) {
+        if (overlaps(dw, N * 4, w, N * 2)) return fail(RMSNORM_ERR_OVERLAP, "dw overlaps w");
+        return RMSNORM_OK;
+    }
+    const int64_t tb = M * N * 2;
+    if (dx != x && overlaps(dx, tb, x, tb))
+        return fail(RMSNORM_ERR_OVERLAP, "dx overlaps x without being equal to it");
+    if (dx != dy && overlaps(dx, tb, dy, tb))
+        return fail(RMSNORM_ERR_OVERLAP, "dx overlaps dy without being equal to it");
+    if (overlaps(dx, tb, w, N * 2) || overlaps(dx, tb, rstd, M * 4) || overlaps(dx, tb, dw, N * 4))
+        return fail(RMSNORM_ERR_OVERLAP, "dx overlaps w, rstd or dw");
+    if (overlaps(dw, N * 4, x, tb) || overlaps(dw, N * 4, dy, tb) ||
+        overlaps(dw, N * 4, w, N * 2) || overlaps(dw, N * 4, rstd, M * 4))
+        return fail(RMSNORM_ERR_OVERLAP, "dw overlaps an input");
+    return RMSNORM_OK;
+}
+
+int bwd_plan(const BwdArgs& a, const rmsnorm_options_t* opts, DeviceInfo* d, Launch& l) {
+    int variant;
+    Knobs k;
+    int rc = read_knobs(opts, &variant, &k);
+    if (rc != RMSNORM_OK) return rc;
+    if (variant != RMSNORM_VARIANT_AUTO && variant != RMSNORM_VARIANT_CTA &&
+        variant != RMSNORM_VARIANT_GENERIC)
+        return fail(RMSNORM_ERR_UNSUPPORTED, "the backward has the CTA and GENERIC variants only");
+    cudaError_t e = device_info(d);
+    if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+    if (!bwd_choose(a, *d, k, variant, l))
+        return fail(RMSNORM_ERR_UNSUPPORTED, "no backward kernel takes N=%lld with these options",
+                    static_cast<long long>(a.N));
+    l.pdl = (k.flags & RMSNORM_FLAG_NO_PDL) == 0;
+    return RMSNORM_OK;
+}
+
+}  // namespace
+
+extern "C" int rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype,
+                                          const rmsnorm_options_t* opts, int64_t* bytes) {
+    if (bytes == nullptr) return fail(RMSNORM_ERR_NULL, "bytes is NULL");
+    *bytes = 0;
+    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16)
+        return fail(RMSNORM_ERR_DTYPE, "dtype %d is not a rmsnorm_dtype_t", dtype);
+    if (M < 0 || N <= 0) return fail(RMSNORM_ERR_SHAPE, "need M >= 0 and N > 0");
+    // The larger of the two kernels' needs (vector kernel with aligned
+    // buffers, general kernel), so the size holds for any alignment.
+    int64_t need = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        const void* p = reinterpret_cast<const void*>(static_cast<uintptr_t>(pass == 0 ? 256 : 2));
+        BwdArgs a{p, p, nullptr, p, const_cast<void*>(p), nullptr, M, N, 0.f, dtype, nullptr};
+        DeviceInfo d;
+        Launch l;
+        rmsnorm_options_t o = {};
+        if (opts) o = *opts;
+        else o.struct_size = sizeof(o);
+        if (pass == 1) o.variant = RMSNORM_VARIANT_GENERIC;
+        if (bwd_plan(a, &o, &d, l) == RMSNORM_OK) {
+            const int64_t b = static_cast<int64_t>(l.grid) * N * 4;
+            if (b > need) need = b;
+        }
+    }
+    if (need == 0) return fail(RMSNORM_ERR_UNSUPPORTED, "no backward kernel takes these arguments");
+    *bytes = need;
+    return RMSNORM_OK;
+}
+
+extern "C" int rmsnorm_bwd(const void* x, const void* w, const float* rstd, const void* dy,
+                           void* dx, float* dw, int64_t M, int64_t N, float offset, int dtype,
+                           void* workspace, int64_t workspace_bytes,
+                           const rmsnorm_options_t* opts, void* stream) {
+    int rc = bwd_validate(x, w, rstd, dy, dx, dw, M, N, offset, dtype, workspace);
+    if (rc != RMSNORM_OK) return rc;
+    const BwdArgs a{x, w, rstd, dy, dx, dw, M, N, offset, dtype, static_cast<cudaStream_t>(stream)};
+    DeviceInfo d;
+    Launch l;
+    rc = bwd_plan(a, opts, &d, l);
+    if (rc != RMSNORM_OK) return rc;
+    const int64_t need = M > 0 ? static_cast<int64_t>(l.grid) * N * 4 : 0;
+    if (workspace_bytes < need)
+        return fail(RMSNORM_ERR_WORKSPACE, "workspace of %lld bytes, %lld needed",
+                    static_cast<long long>(workspace_bytes), static_cast<long long>(need));
+    if (M > 0 && (overlaps(workspace, need, x, M * N * 2) || overlaps(workspace, need, dy, M * N * 2) ||
+                  overlaps(workspace, need, dx, M * N * 2) || overlaps(workspace, need, w, N * 2) ||
+                  overlaps(workspace, need, rstd, M * 4) || overlaps(workspace, need, dw, N * 4)))
+        return fail(RMSNORM_ERR_OVERLAP, "the workspace overlaps an argument");
+    cudaError_t e = bwd_run(a, l, static_cast<float*>(workspace));
+    if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return RMSNORM_OK;
+}
+
 extern "C" int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void* w,
                                  const void* y, const rmsnorm_options_t* opts,
                                  rmsnorm_plan_t* out) {
@@ -313,6 +427,7 @@ extern "C" const char* rmsnorm_strerror(int status) {
         case RMSNORM_ERR_UNSUPPORTED: return "variant unsupported for these arguments";
         case RMSNORM_ERR_OPTIONS: return "bad options";
         case RMSNORM_ERR_ALIGN: return "misaligned pointer";
+        case RMSNORM_ERR_WORKSPACE: return "workspace too small";
         default: return "unknown status";
     }
 }

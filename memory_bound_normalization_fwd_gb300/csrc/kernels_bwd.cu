@@ -1,0 +1,310 @@
+// Backward of the RMSNorm forward, consuming the per-row fp32 rstd the forward
+// keeps "for backward" (TileGym issue #169 kernel listing). The pages give no
+// backward formula; it is the chain rule of the forward's definition:
+//
+//   s_j   = offset + w_j
+//   c_i   = sum_j dy_ij * s_j * x_ij
+//   dx_ij = r_i * (dy_ij * s_j - x_ij * (r_i^2 * c_i / N))
+//   dw_j  = sum_i dy_ij * x_ij * r_i
+//
+// Kernel 1 (one CTA per row, persistent, rows strided over the grid): each
+// thread owns fixed columns (16-byte vectors), so its dw contribution stays in
+// fp32 registers across all the rows it sees; the row sum c goes through a
+// warp butterfly and a shared-memory step. At the end each CTA writes its dw
+// partial (fp32, N values) to row blockIdx.x of the caller's workspace.
+// Kernel 2 sums the partials over CTAs in index order (deterministic) into dw.
+// The general kernel takes any N and alignment with element accesses and a
+// shared-memory dw partial.
+#include "common.cuh"
+#include "launch.h"
+
+namespace rmsn {
+namespace {
+
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 p = Codec<DT>::unpack2(w[k]);
+        f[2 * k] = p.x;
+        f[2 * k + 1] = p.y;
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack8(const float* f) {
+    return make_uint4(Codec<DT>::pack2(f[0], f[1]), Codec<DT>::pack2(f[2], f[3]),
+                      Codec<DT>::pack2(f[4], f[5]), Codec<DT>::pack2(f[6], f[7]));
+}
+
+template <int DT, int THREADS, int V>
+__global__ void __launch_bounds__(THREADS)
+bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __restrict__ rstd,
+                const uint4* dy, uint4* dx, float* __restrict__ partial, int64_t M, int nvec,
+                float n, float offset) {
+    constexpr int kWarps = THREADS / 32;
+    extern __shared__ float4 sw[];  // (offset + w) in fp32, 2 float4 per 16-byte vector
+    __shared__ float part[2][kWarps];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int wid = tid >> 5;
+
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = tid; i < nvec; i += THREADS) {
+        float q[kVecElems];
+        weights8<DT>(__ldg(w + i), offset, q);
+        sw[2 * i] = make_float4(q[0], q[1], q[2], q[3]);
+        sw[2 * i + 1] = make_float4(q[4], q[5], q[6], q[7]);
+    }
+    __syncthreads();
+    float acc[V][kVecElems];
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+        for (int e = 0; e < kVecElems; ++e) acc[v][e] = 0.f;
+
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+        uint4 xv[V], gv[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * THREADS + tid;
+            xv[v] = gv[v] = make_uint4(0u, 0u, 0u, 0u);
+            if (c < nvec) {
+                xv[v] = ld_stream(x + row * nvec + c);
+                gv[v] = ld_stream(dy + row * nvec + c);
+            }
+        }
+        const float r = __ldg(rstd + row);
+        float cs = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * THREADS + tid;
+            if (c >= nvec) continue;
+            float xf[kVecElems], gf[kVecElems];
+            unpack8<DT>(xv[v], xf);
+            unpack8<DT>(gv[v], gf);
+            const float4 s0 = sw[2 * c], s1 = sw[2 * c + 1];
+            const float sv[kVecElems] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int e = 0; e < kVecElems; ++e) cs = fmaf(gf[e] * sv[e], xf[e], cs);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
+        if (lane == 0) part[parity][wid] = cs;
+        __syncthreads();
+        float c_row = 0.f;
+#pragma unroll
+        for (int q = 0; q < kWarps; ++q) c_row += part[parity][q];
+        const float k = (r * r) * c_row / n;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * THREADS + tid;
+            if (c >= nvec) continue;
+            float xf[kVecElems], gf[kVecElems], o[kVecElems];
+            unpack8<DT>(xv[v], xf);
+            unpack8<DT>(gv[v], gf);
+            const float4 s0 = sw[2 * c], s1 = sw[2 * c + 1];
+            const float sv[kVecElems] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int e = 0; e < kVecElems; ++e) {
+                o[e] = r * (gf[e] * sv[e] - xf[e] * k);
+                acc[v][e] = fmaf(gf[e] * xf[e], r, acc[v][e]);
+            }
+            st_stream(dx + row * nvec + c, pack8<DT>(o));
+        }
+        parity ^= 1;
+    }
+
+    float4* out = reinterpret_cast<float4*>(partial + static_cast<int64_t>(blockIdx.x) * nvec * 8);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * THREADS + tid;
+        if (c < nvec) {
+            out[2 * c] = make_float4(acc[v][0], acc[v][1], acc[v][2], acc[v][3]);
+            out[2 * c + 1] = make_float4(acc[v][4], acc[v][5], acc[v][6], acc[v][7]);
+        }
+    }
+}
+
+// General backward: any N and 2-byte alignment. dw partial in shared memory (N floats).
+template <int DT, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+bwd_generic_kernel(const uint16_t* x, const uint16_t* __restrict__ w,
+                   const float* __restrict__ rstd, const uint16_t* dy, uint16_t* dx,
+                   float* __restrict__ partial, int64_t M, int64_t N, float n, float offset) {
+    constexpr int kWarps = THREADS / 32;
+    extern __shared__ float sacc[];
+    __shared__ float part[2][kWarps];
+    const int tid = threadIdx.x;
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t j = tid; j < N; j += THREADS) sacc[j] = 0.f;
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+        const uint16_t* xr = x + row * N;
+        const uint16_t* gr = dy + row * N;
+        const float r = __ldg(rstd + row);
+        float cs = 0.f;
+        for (int64_t j = tid; j < N; j += THREADS) {
+            const float sj = offset + Codec<DT>::unpack1(__ldg(w + j));
+            cs = fmaf(Codec<DT>::unpack1(gr[j]) * sj, Codec<DT>::unpack1(xr[j]), cs);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
+        if ((tid & 31) == 0) part[parity][tid >> 5] = cs;
+        __syncthreads();  // also orders every read of this row before any write of dx
+        float c_row = 0.f;
+#pragma unroll
+        for (int q = 0; q < kWarps; ++q) c_row += part[parity][q];
+        const float k = (r * r) * c_row / n;
+        uint16_t* dr = dx + row * N;
+        for (int64_t j = tid; j < N; j += THREADS) {
+            const float sj = offset + Codec<DT>::unpack1(__ldg(w + j));
+            const float xf = Codec<DT>::unpack1(xr[j]), gf = Codec<DT>::unpack1(gr[j]);
+            dr[j] = Codec<DT>::pack1(r * (gf * sj - xf * k));
+            sacc[j] = fmaf(gf * xf, r, sacc[j]);
+        }
+        parity ^= 1;
+    }
+    __syncthreads();
+    for (int64_t j = tid; j < N; j += THREADS) partial[static_cast<int64_t>(blockIdx.x) * N + j] = sacc[j];
+}
+
+// dw_j = sum over g < G of partial[g][j], in g order; 32 columns per CTA, the
+// 8 warps take every 8th partial row and meet in shared memory in warp order.
+__global__ void __launch_bounds__(256)
+dw_reduce_kernel(const float* __restrict__ partial, float* __restrict__ dw, int G, int64_t N) {
+    __shared__ float red[8][32];
+    pdl_wait();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+    float a = 0.f;
+    if (j < N)
+        for (int g = wid; g < G; g += 8) a += partial[static_cast<int64_t>(g) * N + j];
+    red[wid][lane] = a;
+    __syncthreads();
+    if (wid == 0 && j < N) {
+        float t = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) t += red[q][lane];
+        dw[j] = t;
+    }
+}
+
+using VecFn = void (*)(const uint4*, const uint4*, const float*, const uint4*, uint4*, float*,
+                       int64_t, int, float, float);
+using GenFn = void (*)(const uint16_t*, const uint16_t*, const float*, const uint16_t*,
+                       uint16_t*, float*, int64_t, int64_t, float, float);
+
+template <int DT>
+VecFn pick_vec(int T, int V) {
+#define RMSN_CASE(t, v) \
+    if (T == t && V == v) return bwd_rows_kernel<DT, t, v>;
+    RMSN_CASE(64, 1) RMSN_CASE(64, 2) RMSN_CASE(64, 4)
+    RMSN_CASE(128, 1) RMSN_CASE(128, 2) RMSN_CASE(128, 4)
+    RMSN_CASE(256, 1) RMSN_CASE(256, 2) RMSN_CASE(256, 4)
+    RMSN_CASE(512, 1) RMSN_CASE(512, 2) RMSN_CASE(512, 4)
+    RMSN_CASE(1024, 1) RMSN_CASE(1024, 2)
+#undef RMSN_CASE
+    return nullptr;
+}
+
+template <int DT>
+GenFn pick_gen(int T) {
+    switch (T) {
+        case 64: return bwd_generic_kernel<DT, 64>;
+        case 256: return bwd_generic_kernel<DT, 256>;
+        case 1024: return bwd_generic_kernel<DT, 1024>;
+        default: return nullptr;
+    }
+}
+
+}  // namespace
+
+bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int variant, Launch& l) {
+    const int64_t nvec = a.N / kVecElems;
+    const bool vec = a.N % kVecElems == 0 && aligned16(a.x) && aligned16(a.w) &&
+                     aligned16(a.dy) && aligned16(a.dx);
+    if ((variant == 0 || variant == 2) && vec && nvec <= 2048) {
+        int T = k.lanes_per_row;
+        if (T == 0) {  // two vectors per thread (x, dy and the dw partial stay in registers)
+            T = 64;
+            while (T < 1024 && static_cast<int64_t>(T) * 2 < nvec) T <<= 1;
+        }
+        int V = 1;
+        while (static_cast<int64_t>(V) * T < nvec) V <<= 1;
+        VecFn fn = a.dtype == kBF16 ? pick_vec<kBF16>(T, V) : pick_vec<kFP16>(T, V);
+        const int smem = static_cast<int>(nvec * 32);
+        if (fn && smem > 48 * 1024 &&
+            cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            fn = nullptr;
+        if (fn) {
+            l.kernel = reinterpret_cast<const void*>(fn);
+            l.threads = T;
+            l.lanes_per_row = T;
+            l.vecs_per_lane = V;
+            l.smem = smem;
+            l.ctas_per_sm = occupancy(l.kernel, T, smem);
+            l.grid = persistent_grid(a.M > 0 ? a.M : 1, 1, d.sm_count, l.ctas_per_sm, k.max_ctas);
+            l.work_items = a.M;
+            return true;
+        }
+        if (variant == 2) return false;
+    }
+    if (variant == 2) return false;
+    // General kernel: dw partial for the whole row in shared memory.
+    if (a.N * 4 > d.max_smem_optin - 1024) return false;
+    int T = k.lanes_per_row > 0 ? k.lanes_per_row : (a.N >= 4096 ? 1024 : a.N >= 512 ? 256 : 64);
+    GenFn fn = a.dtype == kBF16 ? pick_gen<kBF16>(T) : pick_gen<kFP16>(T);
+    if (!fn) return false;
+    const int smem = static_cast<int>(a.N * 4);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return false;
+    l.kernel = reinterpret_cast<const void*>(fn);
+    l.threads = T;
+    l.lanes_per_row = T;
+    l.vecs_per_lane = 0;
+    l.smem = smem;
+    l.ctas_per_sm = occupancy(l.kernel, T, smem);
+    if (l.ctas_per_sm < 1) return false;
+    l.grid = persistent_grid(a.M > 0 ? a.M : 1, 1, d.sm_count, l.ctas_per_sm, k.max_ctas);
+    l.work_items = a.M;
+    return true;
+}
+
+cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial) {
+    if (a.M > 0) {
+        LaunchCfg c(l, a.stream, l.pdl);
+        cudaError_t e;
+        if (l.vecs_per_lane > 0) {  // the vector kernel (the general one has none)
+            VecFn fn = reinterpret_cast<VecFn>(const_cast<void*>(l.kernel));
+            e = cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
+                                   static_cast<const uint4*>(a.w), a.rstd,
+                                   static_cast<const uint4*>(a.dy), static_cast<uint4*>(a.dx),
+                                   partial, a.M, static_cast<int>(a.N / kVecElems),
+                                   static_cast<float>(a.N), a.offset);
+        } else {
+            GenFn fn = reinterpret_cast<GenFn>(const_cast<void*>(l.kernel));
+            e = cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint16_t*>(a.x),
+                                   static_cast<const uint16_t*>(a.w), a.rstd,
+                                   static_cast<const uint16_t*>(a.dy), static_cast<uint16_t*>(a.dx),
+                                   partial, a.M, a.N, static_cast<float>(a.N), a.offset);
+        }
+        if (e != cudaSuccess) return e;
+    }
+    Launch r;
+    r.threads = 256;
+    r.grid = static_cast<int>((a.N + 31) / 32);
+    r.smem = 0;
+    LaunchCfg c2(r, a.stream, l.pdl);
+    return cudaLaunchKernelEx(&c2.cfg, dw_reduce_kernel, static_cast<const float*>(partial),
+                              a.dw, a.M > 0 ? l.grid : 0, a.N);
+}
+
+}  // namespace rmsn

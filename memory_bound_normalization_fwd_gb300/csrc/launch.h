@@ -85,6 +85,26 @@ cudaError_t cluster_run(const Args& a, const Launch& l);
 bool generic_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l);
 cudaError_t generic_run(const Args& a, const Launch& l);
 
+// Backward (dx and dw from x, w, the saved rstd and dy), validated by the front end.
+struct BwdArgs {
+    const void* x;
+    const void* w;
+    const float* rstd;
+    const void* dy;
+    void* dx;
+    float* dw;
+    int64_t M;
+    int64_t N;
+    float offset;
+    int dtype;
+    cudaStream_t stream;
+};
+// variant: 0 automatic, 2 the vector (CTA per row) kernel, 4 the general kernel.
+bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int variant, Launch& l);
+// Launches the row kernel (writing one fp32 dw partial row per CTA into `partial`,
+// l.grid rows of N floats) and the reduction of the partials into dw.
+cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial);
+
 // Device status words (bounded-wait timeouts) of the staged variants: read and
 // clear on the current device.
 cudaError_t status_read_and_clear(unsigned int* value);

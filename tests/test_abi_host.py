@@ -113,3 +113,19 @@ def test_bad_options(lib, field, value):
     o = B.make_options()
     setattr(o, field, value)
     assert _call(lib, opts=o) == -9
+
+
+def test_bwd_validation_errors(lib):
+    ws = 0x50000000
+    call = lambda **k: B.rmsnorm_bwd(k.get("x", X), k.get("w", W_), k.get("r", R), k.get("dy", 0x60000000),
+                                     k.get("dx", Y), k.get("dw", 0x70000000), k.get("M", 4), k.get("N", 8),
+                                     0.0, k.get("dt", 0), k.get("ws", ws), 1 << 20, None, 0)
+    assert call(dt=3) == -3
+    assert call(M=-1) == -2
+    assert call(w=0) == -1
+    assert call(dw=0) == -1
+    assert call(ws=0) == -1
+    assert call(ws=ws + 8) == -10
+    assert call(dx=X + 2) == -5          # partial overlap with x
+    assert call(dw=W_) == -5             # dw over w
+    assert call(r=R + 1) == -10

@@ -1,0 +1,159 @@
+"""GPU parity of the backward (dx, dw) against the oracle's fp64 backward, on the
+same seeded inputs and the same fp32 rstd (the oracle forward's, rounded to
+fp32: the value a forward keeps for the backward).
+
+Tolerance, derived from the arithmetic: dx = r (dy s - x r^2 c / N) is a
+difference of two fp32 terms, each with relative error of a few 1e-7 (c is a
+fp32 sum over the row), so |dx_gpu - dx| <= 1 ulp(dx) + 1e-5 * r (|dy s| +
+|x| r^2 sum|dy s x| / N); dw is an fp32 sum over rows (per CTA, then over
+CTAs), so |dw_gpu - dw| <= 1e-5 * sum_i |dy x r|.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_normalization_fwd_gb300 import binding as B
+from memory_bound_normalization_fwd_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+TAU = 1e-5
+DT = {"bf16": B.BF16, "fp16": B.FP16}
+
+
+def _ulp(dtype, v):
+    mbits, emin = (7, -126) if dtype == "bf16" else (10, -14)
+    e = np.floor(np.log2(np.maximum(np.abs(v), 1e-300)))
+    return np.exp2(np.maximum(e, emin) - mbits)
+
+
+def _inputs(M, N, dtype, seed, offset=0.0):
+    wl = W.custom(M, N, dtype, seed=seed, offset=offset)
+    x, w = W.generate(wl)
+    g = W.custom(M, N, dtype, seed=seed + 1000)
+    dy, _ = W.generate(g)
+    _, r64 = oracle.rmsnorm_fwd(x, w, wl.eps, offset, dtype)
+    rstd = r64.astype(np.float32)
+    return x, w, dy, rstd
+
+
+def _check(x, w, dy, rstd, dx_bits, dw, offset, dtype, where=""):
+    _, dx64, dw64 = oracle.rmsnorm_bwd(x, w, dy, offset, dtype, rstd=rstd.astype(np.float64))
+    xv, gv = oracle.decode(dtype, x), oracle.decode(dtype, dy)
+    sv = offset + oracle.decode(dtype, w)
+    r = rstd.astype(np.float64)[:, None]
+    cabs = np.abs(gv * sv * xv).sum(axis=1, keepdims=True)
+    bound = _ulp(dtype, dx64) + TAU * r * (np.abs(gv * sv) + np.abs(xv) * r * r * cabs / x.shape[1])
+    err = np.abs(oracle.decode(dtype, dx_bits) - dx64)
+    assert np.all(err <= bound), f"{where}: dx off by {np.max(err / bound):.3g} of the bound"
+    dwb = TAU * (np.abs(gv * xv) * r).sum(axis=0) + 1e-30
+    errw = np.abs(dw.astype(np.float64) - dw64)
+    assert np.all(errw <= dwb), f"{where}: dw off by {np.max(errw / dwb):.3g} of the bound"
+
+
+def _run(x, w, dy, rstd, offset, dtype, inplace=None, **opts):
+    M, N = x.shape
+    xd = W.to_torch(x, dtype).cuda()
+    wd = W.to_torch(w, dtype).cuda()
+    gd = W.to_torch(dy, dtype).cuda()
+    rd = torch.from_numpy(rstd).cuda()
+    dxd = xd if inplace == "x" else gd if inplace == "dy" else torch.empty_like(xd)
+    dwd = torch.full((N,), -7.0, dtype=torch.float32, device="cuda")
+    o = B.make_options(**opts) if opts else None
+    nbytes = B.rmsnorm_bwd_workspace_size(M, N, DT[dtype], o)
+    ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device="cuda")
+    rc = B.rmsnorm_bwd(xd.data_ptr(), wd.data_ptr(), rd.data_ptr(), gd.data_ptr(), dxd.data_ptr(),
+                       dwd.data_ptr(), M, N, offset, DT[dtype], ws.data_ptr(), ws.numel() * 4, o,
+                       torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, B.rmsnorm_last_error()
+    torch.cuda.synchronize()
+    return W.from_torch(dxd), dwd.cpu().numpy()
+
+
+SHAPES = [(1, 8), (37, 512), (300, 1000), (64, 4096), (33, 8192), (17, 16384), (9, 777),
+          (5, 20000), (130, 520)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("M,N", SHAPES)
+@pytest.mark.parametrize("variant", ["auto", "cta", "generic"])
+def test_bwd_parity(dtype, M, N, variant):
+    offset = float((M + N) % 2)
+    x, w, dy, rstd = _inputs(M, N, dtype, seed=M * 7 + N, offset=offset)
+    try:
+        B.rmsnorm_bwd_workspace_size(M, N, DT[dtype], B.make_options(variant=variant))
+    except B.RMSNormError as e:
+        assert e.status == -8
+        pytest.skip("variant does not take this shape")
+    for max_ctas in (0, 3):
+        try:
+            dx, dw = _run(x, w, dy, rstd, offset, dtype, variant=variant, max_ctas=max_ctas)
+        except AssertionError:
+            if variant == "cta" and (N % 8 or N > 16384):
+                pytest.skip("vector kernel does not take this shape")
+            raise
+        _check(x, w, dy, rstd, dx, dw, offset, dtype, where=f"{variant} {M}x{N} {max_ctas}")
+
+
+@pytest.mark.parametrize("inplace", ["x", "dy"])
+@pytest.mark.parametrize("N", [512, 777])
+def test_bwd_in_place(inplace, N):
+    x, w, dy, rstd = _inputs(200, N, "bf16", seed=N + 1, offset=1.0)
+    dx, dw = _run(x, w, dy, rstd, 1.0, "bf16", inplace=inplace)
+    _check(x, w, dy, rstd, dx, dw, 1.0, "bf16")
+
+
+@pytest.mark.parametrize("name", ["rmsnorm_16384x512_bf16", "rmsnorm_32768x1000_bf16_gemma"])
+def test_bwd_full_size_workloads(name):
+    wl = W.WORKLOADS[name]
+    x, w = W.generate(wl)
+    dy, _ = W.generate(W.custom(wl.M, wl.N, wl.dtype, seed=99))
+    _, r64 = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, wl.dtype)
+    rstd = r64.astype(np.float32)
+    dx, dw = _run(x, w, dy, rstd, wl.offset, wl.dtype)
+    _check(x, w, dy, rstd, dx, dw, wl.offset, wl.dtype, where=name)
+
+
+def test_bwd_is_deterministic_and_m_zero_zeroes_dw():
+    x, w, dy, rstd = _inputs(3000, 1024, "fp16", seed=5)
+    a = _run(x, w, dy, rstd, 0.0, "fp16")
+    b = _run(x, w, dy, rstd, 0.0, "fp16")
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    wd = W.to_torch(w, "fp16").cuda()
+    dwd = torch.full((1024,), 3.0, dtype=torch.float32, device="cuda")
+    assert B.rmsnorm_bwd(0, wd.data_ptr(), 0, 0, 0, dwd.data_ptr(), 0, 1024, 0.0, B.FP16, 0, 0, None,
+                         torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dwd) == 0
+
+
+def test_bwd_rejects_a_small_workspace():
+    M, N = 64, 512
+    xd = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    wd = torch.zeros(N, dtype=torch.bfloat16, device="cuda")
+    rd = torch.ones(M, dtype=torch.float32, device="cuda")
+    dwd = torch.zeros(N, dtype=torch.float32, device="cuda")
+    need = B.rmsnorm_bwd_workspace_size(M, N, B.BF16)
+    ws = torch.empty(need // 4, dtype=torch.float32, device="cuda")
+    rc = B.rmsnorm_bwd(xd.data_ptr(), wd.data_ptr(), rd.data_ptr(), xd.data_ptr(), xd.data_ptr(),
+                       dwd.data_ptr(), M, N, 0.0, B.BF16, ws.data_ptr(), 16, None,
+                       torch.cuda.current_stream().cuda_stream)
+    assert rc == -11
+
+
+def test_torch_convenience_forward_then_backward():
+    x, w, dy, _ = _inputs(500, 2048, "bf16", seed=8, offset=1.0)
+    xd, wd, gd = (W.to_torch(a, "bf16").cuda() for a in (x, w, dy))
+    y, rstd = B.fwd(xd, wd, eps=1e-6, offset=1.0)
+    dx, dw = B.bwd(xd, wd, rstd, gd, offset=1.0)
+    torch.cuda.synchronize()
+    # The GPU forward's rstd is within 1e-5 of the oracle's: check the backward
+    # against the oracle fed the oracle's own rstd, with the tolerance widened by
+    # that difference (dx and dw are first order in r).
+    _, r64 = oracle.rmsnorm_fwd(x, w, 1e-6, 1.0, "bf16")
+    _, dx64, dw64 = oracle.rmsnorm_bwd(x, w, dy, 1.0, "bf16", rstd=r64)
+    got = oracle.decode("bf16", W.from_torch(dx))
+    assert np.all(np.abs(got - dx64) <= _ulp("bf16", dx64) + 3e-5 * np.abs(dx64).max())
+    assert np.allclose(dw.cpu().numpy(), dw64, rtol=1e-4, atol=1e-4 * np.abs(dw64).max())
