@@ -208,6 +208,27 @@ int rmsnorm_bwd(const void* x, const void* w, const float* rstd, const void* dy,
                 float* dw, int64_t M, int64_t N, float offset, int dtype, void* workspace,
                 int64_t workspace_bytes, const rmsnorm_options_t* opts, void* stream);
 
+/*
+ * rmsnorm_bwd without a workspace; allocates nothing. (The pages have no
+ * counterpart: this entry point exists for callers, not for the method.)
+ * Some callers cannot allocate device memory at the point of the call: a
+ * plugin inside a host framework that owns every device allocation, or a
+ * real-time path whose memory plan is fixed at start-up. Here the dw partials
+ * go to a fixed 8 MiB fp32 array built into the library, which every GPU that
+ * loads the library holds until the process exits. The grid is capped so that
+ * grid * N fits in it; N above 2^21 is rejected with RMSNORM_ERR_WORKSPACE.
+ * The first call on a device looks up the array's device address (a CUDA
+ * runtime call, with that device current); make that first call before any
+ * stream capture. All calls on a device share the array, and each call
+ * overwrites the part it uses before reading it, so nothing carries over
+ * between calls; calls that overlap on the GPU (concurrent streams) race on it.
+ * Same arguments as rmsnorm_bwd otherwise; callers who can allocate should
+ * prefer rmsnorm_bwd.
+ */
+int rmsnorm_bwd_noalloc(const void* x, const void* w, const float* rstd, const void* dy, void* dx,
+                        float* dw, int64_t M, int64_t N, float offset, int dtype,
+                        const rmsnorm_options_t* opts, void* stream);
+
 /* Bytes of workspace rmsnorm_bwd needs for these sizes and options on the
  * current device, for any buffer alignment (written to *bytes). */
 int rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype, const rmsnorm_options_t* opts,

@@ -25,7 +25,7 @@ STATUS = {
 }
 # Every function include/rmsnorm.h declares.
 EXPORTS = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_strided", "rmsnorm_bwd",
-           "rmsnorm_bwd_workspace_size", "rmsnorm_plan_info", "rmsnorm_check_device_status",
+           "rmsnorm_bwd_noalloc", "rmsnorm_bwd_workspace_size", "rmsnorm_plan_info", "rmsnorm_check_device_status",
            "rmsnorm_strerror", "rmsnorm_last_error", "rmsnorm_version")
 
 
@@ -85,6 +85,9 @@ def lib() -> ctypes.CDLL:
             L.rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp, i64,
                                       ctypes.POINTER(Options), vp]
             L.rmsnorm_bwd.restype = i32
+            L.rmsnorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, f32, i32,
+                                              ctypes.POINTER(Options), vp]
+            L.rmsnorm_bwd_noalloc.restype = i32
             L.rmsnorm_bwd_workspace_size.argtypes = [i64, i64, i32, ctypes.POINTER(Options),
                                                      ctypes.POINTER(ctypes.c_int64)]
             L.rmsnorm_bwd_workspace_size.restype = i32
@@ -151,6 +154,14 @@ def rmsnorm_bwd(x: int, w: int, rstd: int, dy: int, dx: int, dw: int, M: int, N:
     return lib().rmsnorm_bwd(x, w, rstd, dy, dx, dw, M, N, offset, dtype, workspace,
                              workspace_bytes, ctypes.byref(opts) if opts is not None else None,
                              stream)
+
+
+def rmsnorm_bwd_noalloc(x: int, w: int, rstd: int, dy: int, dx: int, dw: int, M: int, N: int,
+                        offset: float, dtype: int, opts: Options | None, stream: int) -> int:
+    """rmsnorm_bwd with the library's built-in scratch instead of a workspace
+    (for callers that cannot allocate device memory at the call)."""
+    return lib().rmsnorm_bwd_noalloc(x, w, rstd, dy, dx, dw, M, N, offset, dtype,
+                                     ctypes.byref(opts) if opts is not None else None, stream)
 
 
 def rmsnorm_bwd_workspace_size(M: int, N: int, dtype: int, opts: Options | None = None) -> int:

@@ -369,6 +369,34 @@ extern "C" int rmsnorm_bwd(const void* x, const void* w, const float* rstd, cons
     return RMSNORM_OK;
 }
 
+extern "C" int rmsnorm_bwd_noalloc(const void* x, const void* w, const float* rstd,
+                                   const void* dy, void* dx, float* dw, int64_t M, int64_t N,
+                                   float offset, int dtype, const rmsnorm_options_t* opts,
+                                   void* stream) {
+    // The built-in scratch stands in for the workspace argument of the checks.
+    int rc = bwd_validate(x, w, rstd, dy, dx, dw, M, N, offset, dtype,
+                          reinterpret_cast<const void*>(static_cast<uintptr_t>(256)));
+    if (rc != RMSNORM_OK) return rc;
+    float* scratch = nullptr;
+    int64_t cap = 0;
+    cudaError_t e = bwd_builtin_scratch(&scratch, &cap);
+    if (e != cudaSuccess)
+        return fail(RMSNORM_ERR_CUDA, "built-in scratch: %s", cudaGetErrorString(e));
+    if (N > cap)
+        return fail(RMSNORM_ERR_WORKSPACE,
+                    "N=%lld exceeds the built-in scratch (%lld fp32 values per device)",
+                    static_cast<long long>(N), static_cast<long long>(cap));
+    const BwdArgs a{x, w, rstd, dy, dx, dw, M, N, offset, dtype, static_cast<cudaStream_t>(stream)};
+    DeviceInfo d;
+    Launch l;
+    rc = bwd_plan(a, opts, &d, l);
+    if (rc != RMSNORM_OK) return rc;
+    if (static_cast<int64_t>(l.grid) * N > cap) l.grid = static_cast<int>(cap / N);  // one partial row per CTA
+    e = bwd_run(a, l, scratch);
+    if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return RMSNORM_OK;
+}
+
 extern "C" int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void* w,
                                  const void* y, const rmsnorm_options_t* opts,
                                  rmsnorm_plan_t* out) {

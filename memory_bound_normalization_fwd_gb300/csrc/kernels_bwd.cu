@@ -308,3 +308,43 @@ cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial) {
 }
 
 }  // namespace rmsn
+
+// ---- built-in scratch for rmsnorm_bwd_noalloc ---------------------------------
+//
+// Some callers cannot allocate device memory when they call the backward: a
+// plugin running inside a host framework that owns every device allocation, or
+// a real-time path whose memory plan is fixed at start-up. For them the dw
+// partials go to this array instead of a caller workspace. It is a file-scope
+// device array of fixed size, so every GPU that loads the library holds it
+// (8 MiB) until the process exits, and every call on a device shares it.
+#include <mutex>
+
+namespace rmsn {
+
+constexpr int64_t kBuiltinScratchFloats = int64_t(1) << 21;  // 8 MiB of fp32 per device
+static __device__ __align__(256) float g_bwd_scratch[kBuiltinScratchFloats];
+
+// Device address of this device's scratch array. The host-side name of the
+// array is only a stand-in; the address is looked up once per device, with
+// that device current, by the first call on it.
+cudaError_t bwd_builtin_scratch(float** ptr, int64_t* floats) {
+    constexpr int kMaxDevices = 64;
+    static std::once_flag once[kMaxDevices];
+    static float* addr[kMaxDevices];
+    static cudaError_t err[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        void* p = nullptr;
+        err[dev] = cudaGetSymbolAddress(&p, g_bwd_scratch);
+        addr[dev] = static_cast<float*>(p);
+    });
+    if (err[dev] != cudaSuccess) return err[dev];
+    *ptr = addr[dev];
+    *floats = kBuiltinScratchFloats;
+    return cudaSuccess;
+}
+
+}  // namespace rmsn

@@ -104,6 +104,8 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
 // Launches the row kernel (writing one fp32 dw partial row per CTA into `partial`,
 // l.grid rows of N floats) and the reduction of the partials into dw.
 cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial);
+// The backward's built-in scratch on the current device (set up on first use).
+cudaError_t bwd_builtin_scratch(float** ptr, int64_t* floats);
 
 // Device status words (bounded-wait timeouts) of the staged variants: read and
 // clear on the current device.
