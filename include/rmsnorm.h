@@ -199,10 +199,11 @@ int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void
  *              16-byte aligned, owned by the caller; its contents are
  *              overwritten. Calls sharing one workspace must not overlap on
  *              the GPU (one stream, or ordered streams).
- * Rows of up to 16384 columns (N % 8 == 0, 16-byte aligned buffers) take the
- * vector kernel; others the general kernel, which keeps a row's dw partial in
- * shared memory (N up to about 56K). Options: variant AUTO, CTA or GENERIC,
- * lanes_per_row (threads per CTA), max_ctas, RMSNORM_FLAG_NO_PDL.
+ * With N % 8 == 0 and 16-byte aligned buffers, rows of up to 1024 columns take
+ * a warp-per-row kernel and rows of up to 16384 columns a CTA-per-row kernel;
+ * others the general kernel, which keeps a row's dw partial in shared memory
+ * (N up to about 56K). Options: variant AUTO, WARP, CTA or GENERIC,
+ * lanes_per_row (CTA: threads per CTA), max_ctas, RMSNORM_FLAG_NO_PDL.
  */
 int rmsnorm_bwd(const void* x, const void* w, const float* rstd, const void* dy, void* dx,
                 float* dw, int64_t M, int64_t N, float offset, int dtype, void* workspace,

@@ -302,9 +302,10 @@ int bwd_plan(const BwdArgs& a, const rmsnorm_options_t* opts, DeviceInfo* d, Lau
     Knobs k;
     int rc = read_knobs(opts, &variant, &k);
     if (rc != RMSNORM_OK) return rc;
-    if (variant != RMSNORM_VARIANT_AUTO && variant != RMSNORM_VARIANT_CTA &&
-        variant != RMSNORM_VARIANT_GENERIC)
-        return fail(RMSNORM_ERR_UNSUPPORTED, "the backward has the CTA and GENERIC variants only");
+    if (variant != RMSNORM_VARIANT_AUTO && variant != RMSNORM_VARIANT_WARP &&
+        variant != RMSNORM_VARIANT_CTA && variant != RMSNORM_VARIANT_GENERIC)
+        return fail(RMSNORM_ERR_UNSUPPORTED,
+                    "the backward has the WARP, CTA and GENERIC variants only");
     cudaError_t e = device_info(d);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
     if (!bwd_choose(a, *d, k, variant, l))

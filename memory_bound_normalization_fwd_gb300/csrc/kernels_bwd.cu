@@ -129,6 +129,100 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
     }
 }
 
+// Warp-per-row backward for rows of up to 1024 columns: 8 warps per CTA, each
+// warp takes rows blockIdx.x * 8 + warp, + 8 * gridDim.x, ...; lane l owns
+// vectors v * 32 + l. At the end the 8 warps' dw contributions meet in shared
+// memory (summed in warp order) and the CTA writes one partial row, so the
+// number of partial rows is the grid, not the row count.
+template <int DT, int V>
+__global__ void __launch_bounds__(256)
+bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __restrict__ rstd,
+                const uint4* dy, uint4* dx, float* __restrict__ partial, int64_t M, int nvec,
+                float n, float offset) {
+    extern __shared__ float4 sw[];  // (offset + w): 2 float4 per vector; then 8 x N floats of dw
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int wid = tid >> 5;
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = tid; i < nvec; i += 256) {
+        float q[kVecElems];
+        weights8<DT>(__ldg(w + i), offset, q);
+        sw[2 * i] = make_float4(q[0], q[1], q[2], q[3]);
+        sw[2 * i + 1] = make_float4(q[4], q[5], q[6], q[7]);
+    }
+    __syncthreads();
+    float acc[V][kVecElems];
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+        for (int e = 0; e < kVecElems; ++e) acc[v][e] = 0.f;
+
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * 8;
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + wid; row < M; row += stride) {
+        uint4 xv[V], gv[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * 32 + lane;
+            xv[v] = gv[v] = make_uint4(0u, 0u, 0u, 0u);
+            if (c < nvec) {
+                xv[v] = ld_stream(x + row * nvec + c);
+                gv[v] = ld_stream(dy + row * nvec + c);
+            }
+        }
+        const float r = __ldg(rstd + row);
+        float cs = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * 32 + lane;
+            if (c >= nvec) continue;
+            float xf[kVecElems], gf[kVecElems];
+            unpack8<DT>(xv[v], xf);
+            unpack8<DT>(gv[v], gf);
+            const float4 s0 = sw[2 * c], s1 = sw[2 * c + 1];
+            const float sv[kVecElems] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int e = 0; e < kVecElems; ++e) cs = fmaf(gf[e] * sv[e], xf[e], cs);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
+        const float k = (r * r) * cs / n;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * 32 + lane;
+            if (c >= nvec) continue;
+            float xf[kVecElems], gf[kVecElems], o[kVecElems];
+            unpack8<DT>(xv[v], xf);
+            unpack8<DT>(gv[v], gf);
+            const float4 s0 = sw[2 * c], s1 = sw[2 * c + 1];
+            const float sv[kVecElems] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int e = 0; e < kVecElems; ++e) {
+                o[e] = r * (gf[e] * sv[e] - xf[e] * k);
+                acc[v][e] = fmaf(gf[e] * xf[e], r, acc[v][e]);
+            }
+            st_stream(dx + row * nvec + c, pack8<DT>(o));
+        }
+    }
+
+    float* red = reinterpret_cast<float*>(sw + 2 * nvec);  // [8][nvec * 8]
+    const int N8 = nvec * kVecElems;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * 32 + lane;
+        if (c < nvec)
+#pragma unroll
+            for (int e = 0; e < kVecElems; ++e) red[wid * N8 + c * kVecElems + e] = acc[v][e];
+    }
+    __syncthreads();
+    for (int j = tid; j < N8; j += 256) {
+        float t = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) t += red[q * N8 + j];
+        partial[static_cast<int64_t>(blockIdx.x) * N8 + j] = t;
+    }
+}
+
 // General backward: any N and 2-byte alignment. dw partial in shared memory (N floats).
 template <int DT, int THREADS>
 __global__ void __launch_bounds__(THREADS)
@@ -173,23 +267,24 @@ bwd_generic_kernel(const uint16_t* x, const uint16_t* __restrict__ w,
     for (int64_t j = tid; j < N; j += THREADS) partial[static_cast<int64_t>(blockIdx.x) * N + j] = sacc[j];
 }
 
-// dw_j = sum over g < G of partial[g][j], in g order; 32 columns per CTA, the
-// 8 warps take every 8th partial row and meet in shared memory in warp order.
-__global__ void __launch_bounds__(256)
+// dw_j = sum over g < G of partial[g][j]: 32 columns per CTA; the 32 warps take
+// every 32nd partial row and meet in shared memory, summed in warp order
+// (deterministic for a given G).
+__global__ void __launch_bounds__(1024)
 dw_reduce_kernel(const float* __restrict__ partial, float* __restrict__ dw, int G, int64_t N) {
-    __shared__ float red[8][32];
+    __shared__ float red[32][33];
     pdl_wait();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int64_t j = static_cast<int64_t>(blockIdx.x) * 32 + lane;
     float a = 0.f;
     if (j < N)
-        for (int g = wid; g < G; g += 8) a += partial[static_cast<int64_t>(g) * N + j];
+        for (int g = wid; g < G; g += 32) a += partial[static_cast<int64_t>(g) * N + j];
     red[wid][lane] = a;
     __syncthreads();
     if (wid == 0 && j < N) {
         float t = 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) t += red[q][lane];
+        for (int q = 0; q < 32; ++q) t += red[q][lane];
         dw[j] = t;
     }
 }
@@ -228,6 +323,24 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
     const int64_t nvec = a.N / kVecElems;
     const bool vec = a.N % kVecElems == 0 && aligned16(a.x) && aligned16(a.w) &&
                      aligned16(a.dy) && aligned16(a.dx);
+    if ((variant == 0 || variant == 1) && vec && nvec <= 128) {
+        const int V = nvec <= 32 ? 1 : nvec <= 64 ? 2 : 4;
+        VecFn fn = nullptr;
+        if (a.dtype == kBF16)
+            fn = V == 1 ? bwd_warp_kernel<kBF16, 1> : V == 2 ? bwd_warp_kernel<kBF16, 2> : bwd_warp_kernel<kBF16, 4>;
+        else
+            fn = V == 1 ? bwd_warp_kernel<kFP16, 1> : V == 2 ? bwd_warp_kernel<kFP16, 2> : bwd_warp_kernel<kFP16, 4>;
+        l.kernel = reinterpret_cast<const void*>(fn);
+        l.threads = 256;
+        l.lanes_per_row = 32;
+        l.vecs_per_lane = V;
+        l.smem = static_cast<int>(nvec * 32 + 8 * nvec * kVecElems * 4);
+        l.ctas_per_sm = occupancy(l.kernel, 256, l.smem);
+        l.grid = persistent_grid(a.M > 0 ? a.M : 1, 8, d.sm_count, l.ctas_per_sm, k.max_ctas);
+        l.work_items = a.M;
+        return true;
+    }
+    if (variant == 1) return false;
     if ((variant == 0 || variant == 2) && vec && nvec <= 2048) {
         int T = k.lanes_per_row;
         if (T == 0) {  // two vectors per thread (x, dy and the dw partial stay in registers)
@@ -299,7 +412,7 @@ cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial) {
         if (e != cudaSuccess) return e;
     }
     Launch r;
-    r.threads = 256;
+    r.threads = 1024;
     r.grid = static_cast<int>((a.N + 31) / 32);
     r.smem = 0;
     LaunchCfg c2(r, a.stream, l.pdl);

@@ -99,7 +99,7 @@ struct BwdArgs {
     int dtype;
     cudaStream_t stream;
 };
-// variant: 0 automatic, 2 the vector (CTA per row) kernel, 4 the general kernel.
+// variant: 0 automatic, 1 warp per row (N <= 1024), 2 CTA per row, 4 the general kernel.
 bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int variant, Launch& l);
 // Launches the row kernel (writing one fp32 dw partial row per CTA into `partial`,
 // l.grid rows of N floats) and the reduction of the partials into dw.
