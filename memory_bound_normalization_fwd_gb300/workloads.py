@@ -8,7 +8,8 @@ Recipe (every workload): one ``torch.Generator('cpu')`` seeded with the
 workload's seed; x is drawn first, in blocks of rows (block = max(1, 2**22 // N)
 rows, each block drawn in full before the next), then w. Values are drawn in
 fp32 and rounded to the activation dtype by torch's ``.to()`` (round to nearest
-even). Arrays come back as raw uint16 bit patterns.
+even). Arrays come back as raw bit patterns: uint16 for bf16/fp16, uint32 for
+fp32 (drawn in fp32, so no rounding at all).
 
 The five named workloads reproduce the shapes and distributions the method is
 benchmarked on: the 16384x512 bf16 shape reported for the persistent cuTile
@@ -24,8 +25,11 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-DTYPES = ("bf16", "fp16")
-_TORCH = {"bf16": torch.bfloat16, "fp16": torch.float16}
+DTYPES = ("bf16", "fp16", "fp32")
+_TORCH = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
+_INT = {"bf16": (torch.int16, np.uint16), "fp16": (torch.int16, np.uint16),
+        "fp32": (torch.int32, np.uint32)}
+ELEM_BYTES = {"bf16": 2, "fp16": 2, "fp32": 4}
 
 
 @dataclass(frozen=True)
@@ -48,7 +52,8 @@ class Workload:
     @property
     def algorithmic_bytes(self) -> int:
         """Bytes one forward must move: x read, y written, w read, rstd written."""
-        return 2 * self.M * self.N + 2 * self.M * self.N + 2 * self.N + 4 * self.M
+        e = ELEM_BYTES[self.dtype]
+        return e * self.M * self.N + e * self.M * self.N + e * self.N + 4 * self.M
 
 
 WORKLOADS = {
@@ -69,15 +74,16 @@ BENCH_WORKLOAD = "rmsnorm_16384x512_bf16"
 
 
 def _bits(t: torch.Tensor, dtype: str) -> np.ndarray:
-    return t.to(_TORCH[dtype]).view(torch.int16).numpy().view(np.uint16)
+    ti, ni = _INT[dtype]
+    return t.to(_TORCH[dtype]).view(ti).numpy().view(ni)
 
 
 def generate(wl: Workload) -> tuple[np.ndarray, np.ndarray]:
-    """Return ``(x_bits [M, N] uint16, w_bits [N] uint16)`` for the workload."""
+    """Return ``(x_bits [M, N], w_bits [N])`` for the workload (uint16, or uint32 for fp32)."""
     M = wl.M
     g = torch.Generator(device="cpu")
     g.manual_seed(wl.seed)
-    x = np.empty((M, wl.N), dtype=np.uint16)
+    x = np.empty((M, wl.N), dtype=_INT[wl.dtype][1])
     block = max(1, (1 << 22) // wl.N)
     for r0 in range(0, M, block):
         r1 = min(M, r0 + block)
@@ -102,10 +108,14 @@ def custom(M: int, N: int, dtype: str = "bf16", seed: int = 0, **kw) -> Workload
 
 
 def to_torch(bits: np.ndarray, dtype: str) -> torch.Tensor:
-    """uint16 bit patterns -> a CPU torch tensor of the activation dtype (no copy of values)."""
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(_TORCH[dtype])
+    """Bit patterns -> a CPU torch tensor of the activation dtype (no copy of values)."""
+    signed = np.int32 if dtype == "fp32" else np.int16
+    return torch.from_numpy(np.ascontiguousarray(bits).view(signed)).view(_TORCH[dtype])
 
 
 def from_torch(t: torch.Tensor) -> np.ndarray:
-    """A bf16/fp16 torch tensor (any device) -> uint16 bit patterns on the host."""
-    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    """A bf16/fp16/fp32 torch tensor (any device) -> its bit patterns on the host."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.float32:
+        return t.view(torch.int32).numpy().view(np.uint32)
+    return t.view(torch.int16).numpy().view(np.uint16)

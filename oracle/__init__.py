@@ -23,7 +23,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "rmsnorm_oracle.c")
 _LIB = os.path.join(_HERE, "librmsnorm_oracle.so")
-_DTYPES = {"bf16": 0, "fp16": 1}
+_DTYPES = {"bf16": 0, "fp16": 1, "fp32": 2}
+# Bit-pattern container per dtype: 16-bit formats in uint16, fp32 in uint32.
+_BITS = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.uint32}
 _lock = threading.Lock()
 _lib = None
 
@@ -46,19 +48,19 @@ def lib() -> ctypes.CDLL:
         if _lib is None:
             build()
             L = ctypes.CDLL(_LIB)
-            u16p = ctypes.POINTER(ctypes.c_uint16)
+            vp = ctypes.c_void_p
             f64p = ctypes.POINTER(ctypes.c_double)
-            L.oracle_rmsnorm_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p, ctypes.c_int64,
+            L.oracle_rmsnorm_fwd.argtypes = [vp, vp, vp, f64p, f64p, ctypes.c_int64,
                                              ctypes.c_int64, ctypes.c_float, ctypes.c_float,
                                              ctypes.c_int, ctypes.c_int64, ctypes.c_int64]
             L.oracle_rmsnorm_fwd.restype = ctypes.c_int
-            L.oracle_rmsnorm_bwd.argtypes = [u16p, u16p, u16p, f64p, u16p, f64p, f64p,
+            L.oracle_rmsnorm_bwd.argtypes = [vp, vp, vp, f64p, vp, f64p, f64p,
                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
                                              ctypes.c_float, ctypes.c_int]
             L.oracle_rmsnorm_bwd.restype = ctypes.c_int
-            L.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_int64, u16p, f64p]
+            L.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_int64, vp, f64p]
             L.oracle_decode.restype = ctypes.c_int
-            L.oracle_encode.argtypes = [ctypes.c_int, ctypes.c_int64, f64p, u16p]
+            L.oracle_encode.argtypes = [ctypes.c_int, ctypes.c_int64, f64p, vp]
             L.oracle_encode.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -71,48 +73,57 @@ def _ptr(a: np.ndarray | None, ctype):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
 
+def _vp(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def bits_dtype(dtype: str):
+    """numpy container of the bit patterns of ``dtype`` (uint16 or uint32)."""
+    return _BITS[dtype]
+
+
 def decode(dtype: str, bits: np.ndarray) -> np.ndarray:
-    """bf16/fp16 bit patterns (uint16) -> exact float64 values."""
-    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    """bf16/fp16 (uint16) or fp32 (uint32) bit patterns -> exact float64 values."""
+    bits = np.ascontiguousarray(bits, dtype=_BITS[dtype])
     out = np.empty(bits.shape, dtype=np.float64)
-    rc = lib().oracle_decode(_DTYPES[dtype], bits.size, _ptr(bits, ctypes.c_uint16),
-                             _ptr(out, ctypes.c_double))
+    rc = lib().oracle_decode(_DTYPES[dtype], bits.size, _vp(bits), _ptr(out, ctypes.c_double))
     assert rc == 0
     return out
 
 
 def encode(dtype: str, values: np.ndarray) -> np.ndarray:
-    """float64 -> nearest bf16/fp16 bit pattern, ties to even."""
+    """float64 -> nearest bf16/fp16/fp32 bit pattern, ties to even."""
     values = np.ascontiguousarray(values, dtype=np.float64)
-    out = np.empty(values.shape, dtype=np.uint16)
-    rc = lib().oracle_encode(_DTYPES[dtype], values.size, _ptr(values, ctypes.c_double),
-                             _ptr(out, ctypes.c_uint16))
+    out = np.empty(values.shape, dtype=_BITS[dtype])
+    rc = lib().oracle_encode(_DTYPES[dtype], values.size, _ptr(values, ctypes.c_double), _vp(out))
     assert rc == 0
     return out
 
 
 def rmsnorm_fwd(x_bits: np.ndarray, w_bits: np.ndarray, eps: float, offset: float, dtype: str,
                 rows: tuple[int, int] | None = None, want_y64: bool = False):
-    """RMSNorm forward over rows ``[r0, r1)`` of ``x_bits`` ([M, N] uint16).
+    """RMSNorm forward over rows ``[r0, r1)`` of ``x_bits`` ([M, N] bit patterns).
 
     Returns ``(y_bits, rstd_f64)`` for those rows, plus the unrounded fp64 y
     when ``want_y64``. ``eps`` and ``offset`` are taken as fp32, as the CUDA
     entry point takes them.
     """
-    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
-    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    x_bits = np.ascontiguousarray(x_bits, dtype=_BITS[dtype])
+    w_bits = np.ascontiguousarray(w_bits, dtype=_BITS[dtype])
     M, N = x_bits.shape
     assert w_bits.shape == (N,)
     r0, r1 = (0, M) if rows is None else rows
-    y = np.zeros((M, N), dtype=np.uint16) if rows is None else None
+    y = np.zeros((M, N), dtype=_BITS[dtype]) if rows is None else None
     rstd = np.zeros(M, dtype=np.float64)
     y64 = np.zeros((M, N), dtype=np.float64) if want_y64 else None
     if rows is not None:
         # Work on the slice only, so a row range costs only its own rows.
         xs = np.ascontiguousarray(x_bits[r0:r1])
         return rmsnorm_fwd(xs, w_bits, eps, offset, dtype, None, want_y64)
-    rc = lib().oracle_rmsnorm_fwd(_ptr(x_bits, ctypes.c_uint16), _ptr(w_bits, ctypes.c_uint16),
-                                  _ptr(y, ctypes.c_uint16), _ptr(rstd, ctypes.c_double),
+    rc = lib().oracle_rmsnorm_fwd(_vp(x_bits), _vp(w_bits), _vp(y), _ptr(rstd, ctypes.c_double),
                                   _ptr(y64, ctypes.c_double), M, N, eps, offset, _DTYPES[dtype],
                                   r0, r1)
     assert rc == 0
@@ -125,9 +136,11 @@ def rmsnorm_fwd_into(x_bits: np.ndarray, w_bits: np.ndarray, y_out: np.ndarray,
     """Rows ``[row0, row1)`` written into caller-owned arrays (used for threaded runs:
     ctypes releases the GIL for the duration of the C call)."""
     M, N = x_bits.shape
-    rc = lib().oracle_rmsnorm_fwd(_ptr(x_bits, ctypes.c_uint16), _ptr(w_bits, ctypes.c_uint16),
-                                  _ptr(y_out, ctypes.c_uint16), _ptr(rstd_out, ctypes.c_double),
-                                  None, M, N, eps, offset, _DTYPES[dtype], row0, row1)
+    for a in (x_bits, w_bits, y_out):
+        assert a.dtype == _BITS[dtype]
+    rc = lib().oracle_rmsnorm_fwd(_vp(x_bits), _vp(w_bits), _vp(y_out),
+                                  _ptr(rstd_out, ctypes.c_double), None, M, N, eps, offset,
+                                  _DTYPES[dtype], row0, row1)
     assert rc == 0
 
 
@@ -139,18 +152,17 @@ def rmsnorm_bwd(x_bits: np.ndarray, w_bits: np.ndarray, dy_bits: np.ndarray, off
     None recomputes it in fp64 from x and ``eps``. Returns ``(dx_bits, dx_f64,
     dw_f64)``.
     """
-    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
-    dy_bits = np.ascontiguousarray(dy_bits, dtype=np.uint16)
-    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    x_bits = np.ascontiguousarray(x_bits, dtype=_BITS[dtype])
+    dy_bits = np.ascontiguousarray(dy_bits, dtype=_BITS[dtype])
+    w_bits = np.ascontiguousarray(w_bits, dtype=_BITS[dtype])
     M, N = x_bits.shape
     assert dy_bits.shape == (M, N) and w_bits.shape == (N,)
     r = None if rstd is None else np.ascontiguousarray(rstd, dtype=np.float64)
-    dx = np.zeros((M, N), dtype=np.uint16)
+    dx = np.zeros((M, N), dtype=_BITS[dtype])
     dx64 = np.zeros((M, N), dtype=np.float64)
     dw = np.zeros(N, dtype=np.float64)
-    rc = lib().oracle_rmsnorm_bwd(_ptr(x_bits, ctypes.c_uint16), _ptr(w_bits, ctypes.c_uint16),
-                                  _ptr(dy_bits, ctypes.c_uint16), _ptr(r, ctypes.c_double),
-                                  _ptr(dx, ctypes.c_uint16), _ptr(dx64, ctypes.c_double),
-                                  _ptr(dw, ctypes.c_double), M, N, eps, offset, _DTYPES[dtype])
+    rc = lib().oracle_rmsnorm_bwd(_vp(x_bits), _vp(w_bits), _vp(dy_bits), _ptr(r, ctypes.c_double),
+                                  _vp(dx), _ptr(dx64, ctypes.c_double), _ptr(dw, ctypes.c_double),
+                                  M, N, eps, offset, _DTYPES[dtype])
     assert rc == 0
     return dx, dx64, dw

@@ -4,8 +4,12 @@
  * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the CPU
  * baseline leg of the benchmark load this file's library; the product path
  * never does. It shares no code, header, table or constant with the CUDA
- * library: it has its own bf16/fp16 decoders and its own round-to-nearest-even
- * encoders, written from the IEEE-754 binary16 and bfloat16 formats.
+ * library: it has its own bf16/fp16/fp32 decoders and its own
+ * round-to-nearest-even encoders, written from the IEEE-754 binary16, binary32
+ * and bfloat16 formats.
+ *
+ * Activations and weights are bf16, fp16 or fp32 (x, w and y share one
+ * dtype; the kernel listing casts y back to the dtype of X, whatever it is).
  *
  * What it computes, for each row i of a row-major [M, N] activation x and a
  * weight vector w[N]:
@@ -29,11 +33,14 @@
  * round-to-nearest-even, applied once to the exact-as-possible fp64 value.
  *
  * Parity pins (tests that tie this file to something other than itself):
- * decoders against torch/numpy for all 65536 bit patterns; encoders against
- * exact rational rounding; the constant-row closed form; power-of-two scale
- * invariance; the textbook expression in torch float64; the Gemma identity;
- * hand-derived closed-form fixtures; and brute force in 60-digit decimal on
- * tiny shapes. No function here is "parity unpinned".
+ * 16-bit decoders against torch/numpy for all 65536 bit patterns and the fp32
+ * decoder against numpy's float32 on every exponent and a million patterns;
+ * encoders against exact rational rounding and numpy's float64 -> float16 and
+ * float64 -> float32 conversions; the constant-row closed form; power-of-two
+ * scale invariance; the textbook expression in torch float64; the Gemma
+ * identity; hand-derived closed-form fixtures; brute force in 60-digit decimal
+ * on tiny shapes; and the backward against torch float64 autograd and central
+ * differences. No function here is "parity unpinned".
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math, no
  * fused multiply-add contraction, so x86-64 and aarch64 give the same bits).
@@ -44,6 +51,7 @@
 
 #define ORACLE_BF16 0
 #define ORACLE_FP16 1
+#define ORACLE_FP32 2
 
 /* ---- decoders: exact bit pattern -> double ------------------------------ */
 
@@ -81,21 +89,40 @@ double oracle_f16_to_f64(uint16_t h)
     return sign ? -mag : mag;
 }
 
+/* IEEE binary32: 1 sign bit, 8 exponent bits (bias 127), 23 fraction bits. */
+double oracle_f32_to_f64(uint32_t b)
+{
+    int sign = (int)((b >> 31) & 1u);
+    int expo = (int)((b >> 23) & 0xFFu);
+    int32_t frac = (int32_t)(b & 0x7FFFFFu);
+    double mag;
+    if (expo == 0xFF) {
+        mag = frac ? NAN : INFINITY;
+    } else if (expo == 0) {
+        mag = ldexp((double)frac, -126 - 23);
+    } else {
+        mag = ldexp((double)((1 << 23) + frac), expo - 127 - 23);
+    }
+    return sign ? -mag : mag;
+}
+
 /* ---- encoders: double -> nearest representable, ties to even ------------ */
 
 /*
  * Generic binary-float rounding for a format with `mbits` fraction bits,
- * minimum normal exponent `emin`, and all-ones exponent field `emax_field`.
- * Returns the bit pattern (sign, exponent field, fraction).
+ * minimum normal exponent `emin`, and all-ones exponent field `emax_field`,
+ * whose sign is bit `sign_bit`. Returns the bit pattern (sign, exponent
+ * field, fraction).
  */
-static uint16_t round_to_small_float(double v, int mbits, int emin, int bias, int emax_field)
+static uint32_t round_to_binary(double v, int mbits, int emin, int bias, int emax_field,
+                                int sign_bit)
 {
-    uint16_t sign = signbit(v) ? (uint16_t)(1u << 15) : 0;
-    uint16_t quiet_nan = (uint16_t)((emax_field << mbits) | (1u << (mbits - 1)));
-    uint16_t inf = (uint16_t)(emax_field << mbits);
-    if (isnan(v)) return (uint16_t)(sign | quiet_nan);
+    uint32_t sign = signbit(v) ? (1u << sign_bit) : 0u;
+    uint32_t quiet_nan = ((uint32_t)emax_field << mbits) | (1u << (mbits - 1));
+    uint32_t inf = (uint32_t)emax_field << mbits;
+    if (isnan(v)) return sign | quiet_nan;
     double a = fabs(v);
-    if (isinf(a)) return (uint16_t)(sign | inf);
+    if (isinf(a)) return sign | inf;
     if (a == 0.0) return sign;
 
     int e2;
@@ -123,27 +150,51 @@ static uint16_t round_to_small_float(double v, int mbits, int emin, int bias, in
         field = e + bias;
         k -= hidden;
     }
-    if (field >= emax_field) return (uint16_t)(sign | inf);
-    return (uint16_t)(sign | (uint16_t)(field << mbits) | (uint16_t)k);
+    if (field >= emax_field) return sign | inf;
+    return sign | ((uint32_t)field << mbits) | (uint32_t)k;
 }
 
-uint16_t oracle_f64_to_bf16(double v) { return round_to_small_float(v, 7, -126, 127, 0xFF); }
-uint16_t oracle_f64_to_f16(double v) { return round_to_small_float(v, 10, -14, 15, 0x1F); }
+uint16_t oracle_f64_to_bf16(double v) { return (uint16_t)round_to_binary(v, 7, -126, 127, 0xFF, 15); }
+uint16_t oracle_f64_to_f16(double v) { return (uint16_t)round_to_binary(v, 10, -14, 15, 0x1F, 15); }
+uint32_t oracle_f64_to_f32(double v) { return round_to_binary(v, 23, -126, 127, 0xFF, 31); }
 
-/* Array forms, so tests can sweep whole bit spaces in one call. */
-int oracle_decode(int dtype, int64_t n, const uint16_t* bits, double* out)
+static int dtype_ok(int dtype)
 {
-    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16) return -1;
-    for (int64_t i = 0; i < n; ++i)
-        out[i] = dtype == ORACLE_BF16 ? oracle_bf16_to_f64(bits[i]) : oracle_f16_to_f64(bits[i]);
+    return dtype == ORACLE_BF16 || dtype == ORACLE_FP16 || dtype == ORACLE_FP32;
+}
+
+/* Element k of an array of `dtype` bit patterns, widened exactly to double. */
+static double load_elem(int dtype, const void* p, int64_t k)
+{
+    if (dtype == ORACLE_FP32) return oracle_f32_to_f64(((const uint32_t*)p)[k]);
+    if (dtype == ORACLE_BF16) return oracle_bf16_to_f64(((const uint16_t*)p)[k]);
+    return oracle_f16_to_f64(((const uint16_t*)p)[k]);
+}
+
+/* Stores the `dtype` value nearest to v (ties to even) as element k. */
+static void store_elem(int dtype, void* p, int64_t k, double v)
+{
+    if (dtype == ORACLE_FP32)
+        ((uint32_t*)p)[k] = oracle_f64_to_f32(v);
+    else if (dtype == ORACLE_BF16)
+        ((uint16_t*)p)[k] = oracle_f64_to_bf16(v);
+    else
+        ((uint16_t*)p)[k] = oracle_f64_to_f16(v);
+}
+
+/* Array forms, so tests can sweep whole bit spaces in one call. Bit patterns
+ * are uint16 for bf16/fp16 and uint32 for fp32. */
+int oracle_decode(int dtype, int64_t n, const void* bits, double* out)
+{
+    if (!dtype_ok(dtype)) return -1;
+    for (int64_t i = 0; i < n; ++i) out[i] = load_elem(dtype, bits, i);
     return 0;
 }
 
-int oracle_encode(int dtype, int64_t n, const double* v, uint16_t* out)
+int oracle_encode(int dtype, int64_t n, const double* v, void* out)
 {
-    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16) return -1;
-    for (int64_t i = 0; i < n; ++i)
-        out[i] = dtype == ORACLE_BF16 ? oracle_f64_to_bf16(v[i]) : oracle_f64_to_f16(v[i]);
+    if (!dtype_ok(dtype)) return -1;
+    for (int64_t i = 0; i < n; ++i) store_elem(dtype, out, i, v[i]);
     return 0;
 }
 
@@ -158,32 +209,30 @@ int oracle_encode(int dtype, int64_t n, const double* v, uint16_t* out)
  * eps and offset arrive as the fp32 values the CUDA entry point receives and
  * are widened exactly. Returns 0, or -1 on a bad argument.
  */
-int oracle_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, double* rstd,
-                       double* y_f64, int64_t M, int64_t N, float eps, float offset, int dtype,
-                       int64_t row0, int64_t row1)
+int oracle_rmsnorm_fwd(const void* x, const void* w, void* y, double* rstd, double* y_f64,
+                       int64_t M, int64_t N, float eps, float offset, int dtype, int64_t row0,
+                       int64_t row1)
 {
-    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16) return -1;
+    if (!dtype_ok(dtype)) return -1;
     if (M < 0 || N <= 0 || row0 < 0 || row1 > M || row0 > row1) return -1;
-    double (*dec)(uint16_t) = dtype == ORACLE_BF16 ? oracle_bf16_to_f64 : oracle_f16_to_f64;
-    uint16_t (*enc)(double) = dtype == ORACLE_BF16 ? oracle_f64_to_bf16 : oracle_f64_to_f16;
     const double e = (double)eps;
     const double off = (double)offset;
 
     for (int64_t i = row0; i < row1; ++i) {
-        const uint16_t* xi = x + i * N;
+        const int64_t xi = i * N; /* first element of row i */
         double s = 0.0;
         for (int64_t j = 0; j < N; ++j) {
-            double v = dec(xi[j]);
+            double v = load_elem(dtype, x, xi + j);
             s += v * v;
         }
         double ms = s / (double)N;
         double r = 1.0 / sqrt(ms + e);
         if (rstd) rstd[i] = r;
         for (int64_t j = 0; j < N; ++j) {
-            double scale = off + dec(w[j]);
-            double v = dec(xi[j]) * r * scale;
+            double scale = off + load_elem(dtype, w, j);
+            double v = load_elem(dtype, x, xi + j) * r * scale;
             if (y_f64) y_f64[i * N + j] = v;
-            if (y) y[i * N + j] = enc(v);
+            if (y) store_elem(dtype, y, i * N + j, v);
         }
     }
     return 0;
@@ -204,38 +253,38 @@ int oracle_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, double
  * from x and eps. dx is returned rounded to the dtype (one rounding) and in
  * fp64; dw in fp64, summed over rows in index order.
  */
-int oracle_rmsnorm_bwd(const uint16_t* x, const uint16_t* w, const uint16_t* dy,
-                       const double* rstd, uint16_t* dx, double* dx_f64, double* dw,
-                       int64_t M, int64_t N, float eps, float offset, int dtype)
+int oracle_rmsnorm_bwd(const void* x, const void* w, const void* dy, const double* rstd,
+                       void* dx, double* dx_f64, double* dw, int64_t M, int64_t N, float eps,
+                       float offset, int dtype)
 {
-    if (dtype != ORACLE_BF16 && dtype != ORACLE_FP16) return -1;
+    if (!dtype_ok(dtype)) return -1;
     if (M < 0 || N <= 0) return -1;
-    double (*dec)(uint16_t) = dtype == ORACLE_BF16 ? oracle_bf16_to_f64 : oracle_f16_to_f64;
-    uint16_t (*enc)(double) = dtype == ORACLE_BF16 ? oracle_f64_to_bf16 : oracle_f64_to_f16;
     const double off = (double)offset;
     if (dw)
         for (int64_t j = 0; j < N; ++j) dw[j] = 0.0;
     for (int64_t i = 0; i < M; ++i) {
-        const uint16_t* xi = x + i * N;
-        const uint16_t* gi = dy + i * N;
+        const int64_t base = i * N; /* first element of row i of x, dy and dx */
         double r;
         if (rstd) {
             r = rstd[i];
         } else {
             double s = 0.0;
             for (int64_t j = 0; j < N; ++j) {
-                double v = dec(xi[j]);
+                double v = load_elem(dtype, x, base + j);
                 s += v * v;
             }
             r = 1.0 / sqrt(s / (double)N + (double)eps);
         }
         double c = 0.0;
-        for (int64_t j = 0; j < N; ++j) c += dec(gi[j]) * (off + dec(w[j])) * dec(xi[j]);
+        for (int64_t j = 0; j < N; ++j)
+            c += load_elem(dtype, dy, base + j) * (off + load_elem(dtype, w, j)) *
+                 load_elem(dtype, x, base + j);
         for (int64_t j = 0; j < N; ++j) {
-            double xv = dec(xi[j]), gv = dec(gi[j]), sv = off + dec(w[j]);
+            double xv = load_elem(dtype, x, base + j), gv = load_elem(dtype, dy, base + j);
+            double sv = off + load_elem(dtype, w, j);
             double v = r * (gv * sv - xv * r * r * c / (double)N);
-            if (dx_f64) dx_f64[i * N + j] = v;
-            if (dx) dx[i * N + j] = enc(v);
+            if (dx_f64) dx_f64[base + j] = v;
+            if (dx) store_elem(dtype, dx, base + j, v);
             if (dw) dw[j] += gv * xv * r;
         }
     }

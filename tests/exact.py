@@ -10,7 +10,10 @@ import decimal
 from fractions import Fraction
 
 # (fraction bits, minimum normal exponent, bias, all-ones exponent field)
-FORMATS = {"bf16": (7, -126, 127, 0xFF), "fp16": (10, -14, 15, 0x1F)}
+FORMATS = {"bf16": (7, -126, 127, 0xFF), "fp16": (10, -14, 15, 0x1F),
+           "fp32": (23, -126, 127, 0xFF)}
+# Position of the sign bit.
+SIGN_BIT = {"bf16": 15, "fp16": 15, "fp32": 31}
 
 _CTX = decimal.Context(prec=60)
 
@@ -18,7 +21,7 @@ _CTX = decimal.Context(prec=60)
 def decode_exact(dtype: str, bits: int) -> Fraction | None:
     """Bit pattern -> exact rational value (None for inf/NaN)."""
     mbits, emin, bias, emax_field = FORMATS[dtype]
-    sign = -1 if bits >> 15 else 1
+    sign = -1 if bits >> SIGN_BIT[dtype] else 1
     field = (bits >> mbits) & emax_field
     frac = bits & ((1 << mbits) - 1)
     if field == emax_field:
@@ -33,7 +36,7 @@ def decode_exact(dtype: str, bits: int) -> Fraction | None:
 def round_exact(dtype: str, v: Fraction, negative_zero: bool = False) -> int:
     """Nearest representable value of ``dtype`` to the rational ``v``, ties to even."""
     mbits, emin, bias, emax_field = FORMATS[dtype]
-    sign = 0x8000 if (v < 0 or (v == 0 and negative_zero)) else 0
+    sign = (1 << SIGN_BIT[dtype]) if (v < 0 or (v == 0 and negative_zero)) else 0
     a = abs(v)
     if a == 0:
         return sign

@@ -25,21 +25,27 @@ MUTATIONS = {
     "eps dropped": ("double r = 1.0 / sqrt(ms + e);", "double r = 1.0 / sqrt(ms);"),
     "divides by the padded width": ("double ms = s / (double)N;",
                                     "double ms = s / (double)((N + 7) / 8 * 8);"),
-    "offset multiplied": ("double scale = off + dec(w[j]);",
-                          "double scale = (off == 0.0 ? 1.0 : off) * dec(w[j]);"),
-    "weight indexed by row": ("double scale = off + dec(w[j]);",
-                              "double scale = off + dec(w[(i + j) % N]);"),
-    "double rounding through fp32": ("if (y) y[i * N + j] = enc(v);",
-                                     "if (y) y[i * N + j] = enc((double)(float)v);"),
+    "offset multiplied": ("double scale = off + load_elem(dtype, w, j);",
+                          "double scale = (off == 0.0 ? 1.0 : off) * load_elem(dtype, w, j);"),
+    "weight indexed by row": ("double scale = off + load_elem(dtype, w, j);",
+                              "double scale = off + load_elem(dtype, w, (i + j) % N);"),
+    "double rounding through fp32": ("if (y) store_elem(dtype, y, i * N + j, v);",
+                                     "if (y) store_elem(dtype, y, i * N + j, (double)(float)v);"),
     "ties rounded down": ("if (rem > 0.5 || (rem == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;",
                           "if (rem > 0.5) n += 1.0;"),
-    "sign of x lost": ("double v = dec(xi[j]) * r * scale;",
-                       "double v = fabs(dec(xi[j])) * r * scale;"),
+    "sign of x lost": ("double v = load_elem(dtype, x, xi + j) * r * scale;",
+                       "double v = fabs(load_elem(dtype, x, xi + j)) * r * scale;"),
     "sum of |x| instead of x^2": ("s += v * v;", "s += fabs(v);"),
-    "wrong row stride": ("const uint16_t* xi = x + i * N;",
-                         "const uint16_t* xi = x + i * (N > 1 ? N - 1 : N);"),
+    "wrong row stride": ("const int64_t xi = i * N;",
+                         "const int64_t xi = i * (N > 1 ? N - 1 : N);"),
     "subnormal quantum off by one": ("if (e < emin) e = emin;", "if (e < emin - 1) e = emin - 1;"),
     "mean over N+1": ("double ms = s / (double)N;", "double ms = s / (double)(N + 1);"),
+    "fp32 exponent bias off by one": ("mag = ldexp((double)((1 << 23) + frac), expo - 127 - 23);",
+                                      "mag = ldexp((double)((1 << 23) + frac), expo - 126 - 23);"),
+    "fp32 subnormal scale": ("mag = ldexp((double)frac, -126 - 23);",
+                             "mag = ldexp((double)frac, -127 - 23);"),
+    "fp32 encoder fraction bits": ("return round_to_binary(v, 23, -126, 127, 0xFF, 31);",
+                                   "return round_to_binary(v, 22, -126, 127, 0xFF, 31);"),
 }
 
 
@@ -51,29 +57,62 @@ def _build(tmp, source: str) -> ctypes.CDLL:
     subprocess.run(["gcc", "-O1", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", so,
                     c, "-lm"], check=True)
     L = ctypes.CDLL(so)
-    u16p, f64p = ctypes.POINTER(ctypes.c_uint16), ctypes.POINTER(ctypes.c_double)
-    L.oracle_rmsnorm_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p, ctypes.c_int64, ctypes.c_int64,
+    vp, f64p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_double)
+    L.oracle_rmsnorm_fwd.argtypes = [vp, vp, vp, f64p, f64p, ctypes.c_int64, ctypes.c_int64,
                                      ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int64,
                                      ctypes.c_int64]
-    L.oracle_encode.argtypes = [ctypes.c_int, ctypes.c_int64, f64p, u16p]
+    L.oracle_encode.argtypes = [ctypes.c_int, ctypes.c_int64, f64p, vp]
+    L.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_int64, vp, f64p]
     return L
 
 
+CODE = {"bf16": 0, "fp16": 1, "fp32": 2}
+BITS = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.uint32}
+
+
 def _fwd(L, x, w, eps, offset, dtype):
-    x = np.ascontiguousarray(x, dtype=np.uint16)
+    x = np.ascontiguousarray(x, dtype=BITS[dtype])
+    w = np.ascontiguousarray(w, dtype=BITS[dtype])
     M, N = x.shape
-    y = np.zeros((M, N), dtype=np.uint16)
+    y = np.zeros((M, N), dtype=BITS[dtype])
     r = np.zeros(M, dtype=np.float64)
-    u16p, f64p = ctypes.POINTER(ctypes.c_uint16), ctypes.POINTER(ctypes.c_double)
-    rc = L.oracle_rmsnorm_fwd(x.ctypes.data_as(u16p), np.ascontiguousarray(w).ctypes.data_as(u16p),
-                              y.ctypes.data_as(u16p), r.ctypes.data_as(f64p), None, M, N, eps,
-                              offset, 0 if dtype == "bf16" else 1, 0, M)
+    rc = L.oracle_rmsnorm_fwd(x.ctypes.data, w.ctypes.data, y.ctypes.data,
+                              r.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), None, M, N, eps,
+                              offset, CODE[dtype], 0, M)
     assert rc == 0
     return y, r
 
 
+def _encode(L, dtype, vals):
+    vals = np.ascontiguousarray(vals, dtype=np.float64)
+    out = np.zeros(vals.size, dtype=BITS[dtype])
+    L.oracle_encode(CODE[dtype], vals.size, vals.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                    out.ctypes.data)
+    return out
+
+
+def _decode(L, dtype, bits):
+    bits = np.ascontiguousarray(bits, dtype=BITS[dtype])
+    out = np.zeros(bits.size, dtype=np.float64)
+    L.oracle_decode(CODE[dtype], bits.size, bits.ctypes.data,
+                    out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return out
+
+
 def _bits(dtype, values):
-    return np.array([round_exact(dtype, Fraction(float(v))) for v in values], dtype=np.uint16)
+    return np.array([round_exact(dtype, Fraction(float(v))) for v in values], dtype=BITS[dtype])
+
+
+def _patterns(dtype):
+    """Finite non-negative patterns: all of them for 16-bit formats; for fp32,
+    every exponent with a few fractions plus the subnormal ends."""
+    if dtype != "fp32":
+        return np.arange(0x7F80 if dtype == "bf16" else 0x7C00, dtype=np.uint16)
+    expo = np.arange(255, dtype=np.uint32) << 23
+    fr = np.array([0, 1, 3, 0x2AAAAA, 0x400000, 0x7FFFFF], dtype=np.uint32)
+    sub = np.concatenate([np.arange(0, 512, dtype=np.uint32),
+                          np.arange((1 << 23) - 512, 1 << 23, dtype=np.uint32)])
+    return np.unique(np.concatenate([(expo[:, None] | fr[None, :]).ravel(), sub]))
 
 
 def _pins_hold(L) -> bool:
@@ -82,7 +121,7 @@ def _pins_hold(L) -> bool:
     non-power-of-two N, and round-to-nearest-even at every bf16/fp16 midpoint
     between 1 and 2."""
     rng = np.random.default_rng(3)
-    for dtype in ("bf16", "fp16"):
+    for dtype in ("bf16", "fp16", "fp32"):
         for N in (1, 3, 7, 12, 33):
             M = 3
             x = _bits(dtype, rng.normal(0, 1.5, M * N).astype(np.float32)).reshape(M, N)
@@ -107,30 +146,25 @@ def _pins_hold(L) -> bool:
                             return False
         # constant rows: r = 1/sqrt(c^2 + eps) at a non-power-of-two N
         c = 0.5
-        x = np.full((1, 1000), _bits(dtype, [c])[0], dtype=np.uint16)
+        x = np.full((1, 1000), _bits(dtype, [c])[0], dtype=BITS[dtype])
         w = _bits(dtype, [1.0] * 1000)
         _, r = _fwd(L, x, w, 1e-6, 0.0, dtype)
         if not math.isclose(r[0], 1 / math.sqrt(c * c + float(np.float32(1e-6))), rel_tol=1e-14):
             return False
-        # ties to even at every midpoint in [1, 2)
-        mbits = 7 if dtype == "bf16" else 10
-        k = np.arange(1 << mbits, dtype=np.float64)
+        # ties to even at midpoints in [1, 2) (every one for 16-bit formats)
+        mbits = {"bf16": 7, "fp16": 10, "fp32": 23}[dtype]
+        k = np.arange(1 << mbits, dtype=np.float64) if mbits < 16 else \
+            np.unique(rng.integers(0, 1 << mbits, 4096)).astype(np.float64)
         mids = 1.0 + (k + 0.5) / (1 << mbits)
-        out = np.zeros(mids.size, dtype=np.uint16)
-        L.oracle_encode(0 if dtype == "bf16" else 1, mids.size,
-                        mids.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
-                        out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)))
         want = [round_exact(dtype, Fraction(float(m))) for m in mids]
-        if out.tolist() != want:
+        if _encode(L, dtype, mids).tolist() != want:
             return False
-        # every finite pattern round-trips through the encoder
-        pats = np.arange(0x7F80 if dtype == "bf16" else 0x7C00, dtype=np.uint16)
+        # finite patterns decode to their exact values and round-trip through the encoder
+        pats = _patterns(dtype)
         vals = np.array([float(decode_exact(dtype, int(b))) for b in pats])
-        back = np.zeros(pats.size, dtype=np.uint16)
-        L.oracle_encode(0 if dtype == "bf16" else 1, vals.size,
-                        vals.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
-                        back.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)))
-        if not np.array_equal(back, pats):
+        if not np.array_equal(_decode(L, dtype, pats), vals):
+            return False
+        if not np.array_equal(_encode(L, dtype, vals), pats):
             return False
         # a product just below a tie rounds down (one rounding, not two)
         if not _just_below_tie_rounds_down(L, dtype):
@@ -143,7 +177,7 @@ def _just_below_tie_rounds_down(L, dtype) -> bool:
     # offset 1 and w = 3 ulp/2 the exact y sits 2^-31 below the midpoint between
     # 1 + 1 ulp (odd) and 1 + 2 ulp (even): it must round down to 1 + 1 ulp,
     # while rounding through fp32 first lands on the midpoint and goes up.
-    ulp = 2.0 ** -7 if dtype == "bf16" else 2.0 ** -10
+    ulp = {"bf16": 2.0 ** -7, "fp16": 2.0 ** -10, "fp32": 2.0 ** -23}[dtype]
     x = _bits(dtype, [1.0] * 4).reshape(1, 4)
     w = _bits(dtype, [1.5 * ulp] * 4)
     y, _ = _fwd(L, x, w, 2.0 ** -30, 1.0, dtype)
