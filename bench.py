@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "RMSNorm fwd achieved HBM GB/s and % of GB300 peak (1 GPU), per M×N×dtype"
+DCODE = {"bf16": 0, "fp16": 1, "fp32": 2}  # rmsnorm_dtype_t
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["common.cuh", "async_copy.cuh", "launch.h", "kernels_warp.cu", "kernels_cta.cu",
                   "kernels_tma.cu", "kernels_cluster.cu", "kernels_generic.cu", "kernels_bwd.cu",
@@ -202,10 +203,10 @@ class PoolBench:
         from memory_bound_normalization_fwd_gb300 import binding as B
         from memory_bound_normalization_fwd_gb300 import workloads as W
         self.wl, self.dev = wl, dev
-        self.dcode = B.BF16 if wl.dtype == "bf16" else B.FP16
+        self.dcode = DCODE[wl.dtype]
         self.x_host = W.to_torch(x_bits, wl.dtype)
         self.w_dev = W.to_torch(w_bits, wl.dtype).to(dev)
-        self.set_bytes = 4 * wl.M * wl.N + 4 * wl.M
+        self.set_bytes = 2 * W.ELEM_BYTES[wl.dtype] * wl.M * wl.N + 4 * wl.M
         self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         self.pool = max(2, -(-3 * self.l2 // self.set_bytes))
         self.xs = [self.x_host.to(dev) for _ in range(self.pool)]
@@ -286,7 +287,7 @@ def run_oracle_threaded(x, w, wl, rows: int, threads: int):
     `threads` Python threads (ctypes releases the GIL in the C call). Returns seconds."""
     import numpy as np
     import oracle
-    y = np.empty((rows, wl.N), dtype=np.uint16)
+    y = np.empty((rows, wl.N), dtype=oracle.bits_dtype(wl.dtype))
     r = np.empty(rows, dtype=np.float64)
     xs = np.ascontiguousarray(x[:rows])
     bounds = [rows * i // threads for i in range(threads + 1)]
@@ -322,7 +323,8 @@ def bench_ours(args, wl, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    dcode = B.BF16 if wl.dtype == "bf16" else B.FP16
+    dcode = DCODE[wl.dtype]
+    eb = W.ELEM_BYTES[wl.dtype]
     x_bits, w_bits = W.generate(wl)
     pb = PoolBench(wl, x_bits, w_bits, dev)
     x_host, w_dev, xs, ys, rs = pb.x_host, pb.w_dev, pb.xs, pb.ys, pb.rs
@@ -426,8 +428,8 @@ def bench_ours(args, wl, rank, world, local_rank):
                      else "fallback 6.8 TB/s", "algorithmic_bytes": wl.algorithmic_bytes,
                      "kernel_hash": kernel_hash()},
         "e2e": {"value": round(whole_job_gbs(wl.algorithmic_bytes, Ke, world, e2e_s), 2),
-                "unit": "GB/s", "h2d_bytes_per_step": 2 * wl.M * wl.N,
-                "d2h_bytes_per_step": 2 * wl.M * wl.N + 4 * wl.M, "steps": Ke,
+                "unit": "GB/s", "h2d_bytes_per_step": eb * wl.M * wl.N,
+                "d2h_bytes_per_step": eb * wl.M * wl.N + 4 * wl.M, "steps": Ke,
                 "ms_per_step": round(e2e_s * 1e3 / Ke, 4),
                 "path": "pinned host x -> device, rmsnorm_fwd, y and rstd -> pinned host, one stream"},
         "gpu_launches": K,
@@ -447,7 +449,8 @@ def ablation_configs(wl):
     """Kernel variants and knobs to compare on one workload (the pages' knobs:
     TMA staging on or off, prefetch depth, rows per warp, registers and
     occupancy; plus launch overlap and row order)."""
-    nvec, row = wl.N // 8, 2 * wl.N
+    eb = 4 if wl.dtype == "fp32" else 2
+    nvec, row = wl.N * eb // 16, eb * wl.N
     cfgs = [dict(), dict(early_loads=True), dict(pdl=False), dict(blocked=True)]
     if nvec <= 128:
         for G in (8, 16, 32):
@@ -477,13 +480,14 @@ def run_ablation(args, names):
     peak, _ = load_peaks()
     dev = torch.device("cuda", 0)
     for name in names:
-        wl = W.WORKLOADS[name]
+        wl = W.get(name)
         x_bits, w_bits = W.generate(wl)
         pb = PoolBench(wl, x_bits, w_bits, dev)
         K = args.steps if wl.M * wl.N < (1 << 26) else max(200, args.steps // 20)
         s, _, _, _ = pb.copy_timed(K, 3)
         print(json.dumps({"ablation": name, "config": "device copy x -> y (torch)",
-                          "gbs": round(4 * wl.M * wl.N * K / s / 1e9, 1)}), flush=True)
+                          "gbs": round(2 * pb.x_host.element_size() * wl.M * wl.N * K / s / 1e9,
+                                       1)}), flush=True)
         for cfg in ablation_configs(wl):
             opts = B.make_options(**cfg)
             try:
@@ -579,7 +583,8 @@ def bench_reference(args, wl):
     rows_per_s = probe / max(t, 1e-6)
     total = args.steps + max(3, args.warmup)
     rows = int(max(cores, min(wl.M, rows_per_s * 60.0 / total)))
-    step_bytes = 4 * rows * wl.N + 2 * wl.N + 4 * rows
+    eb = 4 if wl.dtype == "fp32" else 2
+    step_bytes = 2 * eb * rows * wl.N + eb * wl.N + 4 * rows
     for _ in range(max(3, args.warmup) if total * rows / rows_per_s < 120 else 3):
         run_oracle_threaded(x, w, wl, rows, cores)
     secs = sum(run_oracle_threaded(x, w, wl, rows, cores) for _ in range(args.steps))
@@ -603,7 +608,7 @@ def bench_reference(args, wl):
 def main(argv=None):
     args = parse_args(argv)
     from memory_bound_normalization_fwd_gb300 import workloads as W
-    wl = W.WORKLOADS[args.workload or W.BENCH_WORKLOAD]
+    wl = W.get(args.workload or W.BENCH_WORKLOAD)
     rank, world, local_rank = dist_env()
 
     if args.backward:

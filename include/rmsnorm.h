@@ -12,18 +12,20 @@
  * register" (TileGym issue #169): x is widened to fp32 before squaring, the
  * row sum of squares is divided by the true N, eps is added inside the rsqrt,
  * the fp32 rstd is stored "for backward", the normalised row is scaled by
- * (offset + w) in fp32 and cast once to x's dtype. The same formula, with
+ * (offset + w) in fp32 and cast once to x's dtype (the listing's cast to the
+ * dtype of X, whatever that dtype is: bf16, fp16 or fp32). The same formula, with
  * offset 0, is the Overview and Verification formula of "RMSNorm Kernel
  * Optimization" (skillmd): out = x / sqrt(mean(x^2) + eps) * weight.
  * Arithmetic is fp32 throughout (sum of squares, mean, rsqrt, products); y is
- * rounded to nearest-even once. Results are deterministic: the same inputs and
+ * rounded to nearest-even once (for fp32 y, the products are fp32 products).
+ * Results are deterministic: the same inputs and
  * launch shape always give the same bits.
  *
  * Memory. Every pointer is a DEVICE pointer on the calling thread's current
  * CUDA device (cudaSetDevice), allocated by the caller. The library never
  * allocates, frees or copies caller memory, and never synchronises except in
  * rmsnorm_check_device_status().
- *   x     [M, N] bf16 or fp16, contiguous row-major (row i at x + i*N)
+ *   x     [M, N] bf16, fp16 or fp32, contiguous row-major (row i at x + i*N)
  *   w     [N]    same dtype as x
  *   y     [M, N] same dtype as x; may equal x exactly (in place), must not
  *                otherwise overlap x, w or rstd
@@ -33,9 +35,10 @@
  * of y at y + i*ldy, in elements, each >= N), for rows that are slices of
  * wider tensors; the overlap rules then apply to the spans from the first to
  * the last element of each array.
- * x, w, y need only their element alignment (2 bytes) and rstd 4 bytes.
- * 16-byte-aligned x, w, y with N a multiple of 8 take the vectorised kernels;
- * anything else takes the general kernel.
+ * x, w, y need only their element alignment (2 bytes; 4 for fp32) and rstd
+ * 4 bytes. 16-byte-aligned x, w, y whose rows are whole 16-byte vectors (N a
+ * multiple of 8; of 4 for fp32) take the vectorised kernels; anything else
+ * takes the general kernel.
  *
  * Streams and errors. Work is enqueued on `stream` (a cudaStream_t; NULL is the
  * legacy default stream) and the call returns at once. Kernels are launched
@@ -61,7 +64,8 @@ extern "C" {
 
 typedef enum rmsnorm_dtype {
     RMSNORM_DTYPE_BF16 = 0,
-    RMSNORM_DTYPE_FP16 = 1
+    RMSNORM_DTYPE_FP16 = 1,
+    RMSNORM_DTYPE_FP32 = 2 /* forward only; the backward takes bf16 and fp16 */
 } rmsnorm_dtype_t;
 
 typedef enum rmsnorm_status {
@@ -75,7 +79,8 @@ typedef enum rmsnorm_status {
     RMSNORM_ERR_DEVICE_TIMEOUT = -7, /* a kernel's bounded wait ran out (see rmsnorm_check_device_status) */
     RMSNORM_ERR_UNSUPPORTED = -8,    /* the forced variant cannot take these arguments */
     RMSNORM_ERR_OPTIONS = -9,        /* malformed rmsnorm_options_t */
-    RMSNORM_ERR_ALIGN = -10,         /* x, w or y not 2-byte aligned, or rstd not 4-byte aligned */
+    RMSNORM_ERR_ALIGN = -10,         /* x, w or y not aligned to their element size, or rstd not
+                                        4-byte aligned */
     RMSNORM_ERR_WORKSPACE = -11      /* the backward's workspace is smaller than it needs */
 } rmsnorm_status_t;
 
@@ -84,22 +89,23 @@ typedef enum rmsnorm_variant {
     RMSNORM_VARIANT_AUTO = 0,
     /* A team of 1..32 lanes of one warp per row, row held in registers,
      * several rows per warp when N is small (warp-per-row and
-     * multi-row-per-warp). Needs 16-byte alignment and N % 8 == 0, N <= 1024. */
+     * multi-row-per-warp). Needs 16-byte alignment and rows of whole 16-byte
+     * vectors, at most 2 KB per row (N <= 1024 bf16/fp16, 512 fp32). */
     RMSNORM_VARIANT_WARP = 1,
     /* One CTA per row, row held in registers across the CTA, cross-warp sum
-     * through shared memory. Needs 16-byte alignment and N % 8 == 0,
-     * N <= 32768. */
+     * through shared memory. Needs 16-byte alignment and rows of whole 16-byte
+     * vectors, at most 64 KB per row (N <= 32768 bf16/fp16, 16384 fp32). */
     RMSNORM_VARIANT_CTA = 2,
     /* Rows staged in shared memory by TMA bulk copies (cp.async.bulk with an
      * mbarrier), multi-stage pipeline, bounded waits. Needs 16-byte alignment
-     * and N % 8 == 0; rows up to the shared-memory limit. */
+     * and rows of whole 16-byte vectors; rows up to the shared-memory limit. */
     RMSNORM_VARIANT_TMA = 3,
     /* Any alignment and any N: one CTA per row, two passes over the row. */
     RMSNORM_VARIANT_GENERIC = 4,
     /* Rows longer than one CTA's shared memory: a row split over a thread-block
      * cluster of 2..16 CTAs, each staging its column slice by TMA bulk copy; the
      * slice sums meet through distributed shared memory. Needs 16-byte alignment
-     * and N % 8 == 0; rows up to 16 slices of about 70 KB. */
+     * and rows of whole 16-byte vectors; rows up to 16 slices of about 70 KB. */
     RMSNORM_VARIANT_CLUSTER = 5
 } rmsnorm_variant_t;
 

@@ -14,7 +14,7 @@ import threading
 
 from . import build as _build
 
-BF16, FP16 = 0, 1
+BF16, FP16, FP32 = 0, 1, 2
 VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "tma": 3, "generic": 4, "cluster": 5}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 STATUS = {
@@ -205,7 +205,9 @@ def _dtype_code(t) -> int:
         return BF16
     if t.dtype == torch.float16:
         return FP16
-    raise TypeError(f"RMSNorm forward takes bf16 or fp16 activations, got {t.dtype}")
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"RMSNorm takes bf16, fp16 or fp32 activations, got {t.dtype}")
 
 
 def fwd(x, w, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=None, stream=None,

@@ -57,8 +57,9 @@ bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
 
 int validate(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, float* rstd,
              int64_t M, int64_t N, float eps, float offset, int dtype) {
-    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16)
-        return fail(RMSNORM_ERR_DTYPE, "dtype %d is not RMSNORM_DTYPE_BF16 (0) or _FP16 (1)", dtype);
+    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16 && dtype != RMSNORM_DTYPE_FP32)
+        return fail(RMSNORM_ERR_DTYPE, "dtype %d is not RMSNORM_DTYPE_BF16 (0), _FP16 (1) or _FP32 (2)",
+                    dtype);
     if (M < 0 || N <= 0)
         return fail(RMSNORM_ERR_SHAPE, "need M >= 0 and N > 0 (got M=%lld N=%lld)",
                     static_cast<long long>(M), static_cast<long long>(N));
@@ -68,7 +69,8 @@ int validate(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, fl
                     static_cast<long long>(N));
     // 2^48 bytes bounds any array a GPU can hold and keeps the kernels' 64-bit
     // index arithmetic (row block bounds are CTA index * M) far from overflow.
-    const int64_t lim = int64_t(1) << 47;
+    const int64_t eb = elem_bytes(dtype);
+    const int64_t lim = (int64_t(1) << 48) / eb;
     if (M > 0 && (M > (int64_t(1) << 46) || ldx > lim / M || ldy > lim / M))
         return fail(RMSNORM_ERR_SHAPE, "x or y would span more than 2^48 bytes (M=%lld)",
                     static_cast<long long>(M));
@@ -81,13 +83,14 @@ int validate(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, fl
     if (x == nullptr || y == nullptr)
         return fail(RMSNORM_ERR_NULL, "x and y must be non-NULL when M > 0");
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
-         reinterpret_cast<uintptr_t>(w)) & 1u)
-        return fail(RMSNORM_ERR_ALIGN, "x, w and y must be 2-byte aligned");
+         reinterpret_cast<uintptr_t>(w)) & static_cast<uintptr_t>(eb - 1))
+        return fail(RMSNORM_ERR_ALIGN, "x, w and y must be aligned to the element size (%d bytes)",
+                    static_cast<int>(eb));
     if (reinterpret_cast<uintptr_t>(rstd) & 3u)
         return fail(RMSNORM_ERR_ALIGN, "rstd must be 4-byte aligned");
     // Byte spans from the first element of row 0 to the last element of row M-1.
-    const int64_t xb = ((M - 1) * ldx + N) * 2, yb = ((M - 1) * ldy + N) * 2;
-    const int64_t wb = N * 2, rb = M * 4;
+    const int64_t xb = ((M - 1) * ldx + N) * eb, yb = ((M - 1) * ldy + N) * eb;
+    const int64_t wb = N * eb, rb = M * 4;
     if (x == y) {
         if (ldx != ldy) return fail(RMSNORM_ERR_OVERLAP, "in place (y == x) needs ldy == ldx");
     } else if (overlaps(x, xb, y, yb)) {
@@ -126,13 +129,15 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
 }
 
 // Chooses the variant. The automatic choice, when x, w and y are 16-byte
-// aligned and N % 8 == 0 (measured on GB300, bf16):
-//   rows of up to 768 columns under strict stream order: the warp-team kernel
-//     (ahead of the TMA kernel at N = 512; with early loads the TMA kernel is
-//     ahead at every N measured);
-//   rows of up to 8192 columns: the TMA-staged kernel (ahead from N = 1000 to 8192);
-//   rows of up to 32768 columns: the register CTA kernel (6.4 TB/s at N = 16384
-//     against 5.4 for the TMA kernel, 5.8 against 5.3 at N = 32768);
+// aligned and rows are whole 16-byte vectors (measured on GB300, bf16; the
+// limits are row bytes, so fp32 rows switch at half the column count):
+//   rows of up to 1536 bytes (768 bf16 columns) under strict stream order: the
+//     warp-team kernel (ahead of the TMA kernel at N = 512; with early loads
+//     the TMA kernel is ahead at every N measured);
+//   rows of up to 16 KB (8192 columns): the TMA-staged kernel (ahead from
+//     N = 1000 to 8192);
+//   rows of up to 64 KB (32768 columns): the register CTA kernel (6.4 TB/s at
+//     N = 16384 against 5.4 for the TMA kernel, 5.8 against 5.3 at N = 32768);
 //   longer rows: the cluster kernel, while 16 slices fit in shared memory.
 // Anything else takes the general kernel.
 int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch& l,
@@ -147,12 +152,13 @@ int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch
         default:
             const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) &&
                                !(k.flags & RMSNORM_FLAG_NO_PDL);
-            if (!early && a.N <= 768 && warp_choose(a, d, k, l)) {
+            const int64_t row_bytes = a.N * elem_bytes(a.dtype);
+            if (!early && row_bytes <= 1536 && warp_choose(a, d, k, l)) {
                 variant = RMSNORM_VARIANT_WARP;
-            } else if (a.N <= 8192 && (l = Launch{}, tma_choose(a, d, k, l)) &&
+            } else if (row_bytes <= 16384 && (l = Launch{}, tma_choose(a, d, k, l)) &&
                        (l.stages >= 2 || k.stages > 0)) {
                 variant = RMSNORM_VARIANT_TMA;
-            } else if (a.N <= 32768 && (l = Launch{}, cta_choose(a, d, k, l))) {
+            } else if (row_bytes <= 65536 && (l = Launch{}, cta_choose(a, d, k, l))) {
                 variant = RMSNORM_VARIANT_CTA;
             } else if ((l = Launch{}, cluster_choose(a, d, k, l))) {
                 variant = RMSNORM_VARIANT_CLUSTER;
@@ -262,7 +268,7 @@ namespace {
 int bwd_validate(const void* x, const void* w, const float* rstd, const void* dy, void* dx,
                  float* dw, int64_t M, int64_t N, float offset, int dtype, const void* ws) {
     if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16)
-        return fail(RMSNORM_ERR_DTYPE, "dtype %d is not RMSNORM_DTYPE_BF16 (0) or _FP16 (1)", dtype);
+        return fail(RMSNORM_ERR_DTYPE, "the backward takes bf16 (0) or fp16 (1), not dtype %d", dtype);
     if (M < 0 || N <= 0)
         return fail(RMSNORM_ERR_SHAPE, "need M >= 0 and N > 0 (got M=%lld N=%lld)",
                     static_cast<long long>(M), static_cast<long long>(N));
@@ -403,7 +409,7 @@ extern "C" int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x,
                                  rmsnorm_plan_t* out) {
     if (out == nullptr) return fail(RMSNORM_ERR_NULL, "out is NULL");
     std::memset(out, 0, sizeof(*out));
-    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16)
+    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16 && dtype != RMSNORM_DTYPE_FP32)
         return fail(RMSNORM_ERR_DTYPE, "dtype %d is not a rmsnorm_dtype_t", dtype);
     if (M < 1 || N <= 0) return fail(RMSNORM_ERR_SHAPE, "plan needs M >= 1 and N > 0");
     int variant;

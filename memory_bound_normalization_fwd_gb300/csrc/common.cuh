@@ -13,7 +13,7 @@
 
 namespace rmsn {
 
-enum DType : int { kBF16 = 0, kFP16 = 1 };
+enum DType : int { kBF16 = 0, kFP16 = 1, kFP32 = 2 };
 
 // Element codecs. A 32-bit word holds two elements, element 0 in the low half
 // (little-endian memory order).
@@ -59,8 +59,15 @@ struct Codec<kFP16> {
     }
 };
 
-// 16-byte vector = 8 elements.
+// 16-byte vector = 8 elements of a 16-bit format (the backward's kernels use
+// this constant; the forward's use VecElems<DT>).
 constexpr int kVecElems = 8;
+
+// Elements per 16-byte vector: 8 for bf16/fp16, 4 for fp32.
+template <int DT>
+struct VecElems {
+    static constexpr int value = DT == kFP32 ? 4 : 8;
+};
 
 // Sum of squares of the 8 elements of a vector, accumulated into acc.
 template <int DT>
@@ -98,6 +105,89 @@ __device__ __forceinline__ void weights8(const uint4& v, float offset, float* s)
         s[2 * k] = offset + f.x;
         s[2 * k + 1] = offset + f.y;
     }
+}
+
+// One element in memory, for the element-wise kernel: its storage type, the
+// widening to fp32 and the single rounding back.
+template <int DT>
+struct Elem {
+    using T = uint16_t;
+    static __device__ __forceinline__ float load(T u) { return Codec<DT>::unpack1(u); }
+    static __device__ __forceinline__ T store(float f) { return Codec<DT>::pack1(f); }
+};
+
+template <>
+struct Elem<kFP32> {
+    using T = float;
+    static __device__ __forceinline__ float load(T u) { return u; }
+    static __device__ __forceinline__ T store(float f) { return f; }
+};
+
+// The forward's per-vector steps for any dtype: fp32 vectors are four floats
+// (no conversion); 16-bit vectors go through the codecs above.
+template <int DT>
+__device__ __forceinline__ float sumsq_vec(const uint4& v, float acc) {
+    if constexpr (DT == kFP32) {
+        const float f[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                            __uint_as_float(v.w)};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc = fmaf(f[k], f[k], acc);
+        return acc;
+    } else {
+        return sumsq8<DT>(v, acc);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 scale_vec(const uint4& v, float r, const float* s) {
+    if constexpr (DT == kFP32) {
+        return make_uint4(__float_as_uint((__uint_as_float(v.x) * r) * s[0]),
+                          __float_as_uint((__uint_as_float(v.y) * r) * s[1]),
+                          __float_as_uint((__uint_as_float(v.z) * r) * s[2]),
+                          __float_as_uint((__uint_as_float(v.w) * r) * s[3]));
+    } else {
+        return scale8<DT>(v, r, s);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void weights_vec(const uint4& v, float offset, float* s) {
+    if constexpr (DT == kFP32) {
+        s[0] = offset + __uint_as_float(v.x);
+        s[1] = offset + __uint_as_float(v.y);
+        s[2] = offset + __uint_as_float(v.z);
+        s[3] = offset + __uint_as_float(v.w);
+    } else {
+        weights8<DT>(v, offset, s);
+    }
+}
+
+// (offset + w) of vector c kept in shared memory as VecElems floats (float4
+// reads), and the scale step with those weights.
+template <int DT>
+__device__ __forceinline__ uint4 scale_vec_smem(const uint4& v, float r, const float4* sw, int c) {
+    constexpr int kE = VecElems<DT>::value;
+    float s[kE];
+#pragma unroll
+    for (int q = 0; q < kE / 4; ++q) {
+        const float4 t = sw[c * (kE / 4) + q];
+        s[4 * q] = t.x;
+        s[4 * q + 1] = t.y;
+        s[4 * q + 2] = t.z;
+        s[4 * q + 3] = t.w;
+    }
+    return scale_vec<DT>(v, r, s);
+}
+
+template <int DT>
+__device__ __forceinline__ void weights_vec_to_smem(const uint4& wv, float offset, float4* sw,
+                                                    int c) {
+    constexpr int kE = VecElems<DT>::value;
+    float s[kE];
+    weights_vec<DT>(wv, offset, s);
+#pragma unroll
+    for (int q = 0; q < kE / 4; ++q)
+        sw[c * (kE / 4) + q] = make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
 }
 
 // Streaming global accesses: x and y are touched once, so they are loaded and

@@ -145,7 +145,7 @@ cluster_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float
 
         float ss = 0.f;
         if (ok)
-            for (int i = tid; i < my_vecs; i += kThreads) ss = sumsq8<DT>(sx[i], ss);
+            for (int i = tid; i < my_vecs; i += kThreads) ss = sumsq_vec<DT>(sx[i], ss);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         if (lane == 0) part[wid] = ss;
@@ -185,9 +185,9 @@ cluster_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float
         const float r = row_rstd(row_total, n, eps);
         if (rank == 0 && tid == 0 && rstd != nullptr) rstd[row] = r;
         for (int i = tid; i < my_vecs; i += kThreads) {
-            float s[kVecElems];
-            weights8<DT>(sw[i], offset, s);
-            st_stream(y + row * ldy + v0 + i, scale8<DT>(sx[i], r, s));
+            float s[VecElems<DT>::value];
+            weights_vec<DT>(sw[i], offset, s);
+            st_stream(y + row * ldy + v0 + i, scale_vec<DT>(sx[i], r, s));
         }
         pp ^= 1;
         __syncthreads();  // every thread is done reading this stage
@@ -265,8 +265,10 @@ int max_clusters(const void* fn, int C, int smem) {
 
 bool cluster_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     if (!vector_ok(a)) return false;
-    const int64_t nvec = a.N / kVecElems;
-    Fn fn = a.dtype == kBF16 ? cluster_rows_kernel<kBF16> : cluster_rows_kernel<kFP16>;
+    const int64_t nvec = a.N / vec_elems(a.dtype);
+    Fn fn = a.dtype == kBF16   ? cluster_rows_kernel<kBF16>
+            : a.dtype == kFP16 ? cluster_rows_kernel<kFP16>
+                               : cluster_rows_kernel<kFP32>;
     const int max_dyn = prepare(reinterpret_cast<const void*>(fn), d.max_smem_optin);
     if (max_dyn <= 0) return false;
     const int S = k.stages > 0 ? k.stages : 2;
@@ -308,6 +310,7 @@ cudaError_t cluster_run(const Args& a, const Launch& l) {
     const long long limit = static_cast<long long>(l.wait_limit_ns * 21 / 10);
     const long long drain = kDrainLimitNs * 21 / 10;
     const int slice_stride = (l.slice_vecs * 16 + 127) / 128 * 128;
+    const int64_t e = vec_elems(a.dtype);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -324,8 +327,7 @@ cudaError_t cluster_run(const Args& a, const Launch& l) {
     cfg.numAttrs = l.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
-                              a.M, static_cast<int>(a.N / kVecElems), a.ldx / kVecElems,
-                              a.ldy / kVecElems, l.slice_vecs,
+                              a.M, static_cast<int>(a.N / e), a.ldx / e, a.ldy / e, l.slice_vecs,
                               static_cast<float>(a.N), a.eps, a.offset, l.stages, slice_stride,
                               limit < 1 ? 1LL : limit, drain, l.mode());
 }

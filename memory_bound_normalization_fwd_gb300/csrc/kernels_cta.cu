@@ -33,13 +33,13 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     const bool early = (mode & kModeEarlyLoads) != 0;
     if (!early) pdl_wait();
     pdl_launch_dependents();
-    float s[V][kVecElems];
+    float s[V][VecElems<DT>::value];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = v * THREADS + tid;
         uint4 wv = make_uint4(0u, 0u, 0u, 0u);
         if (c < nvec) wv = __ldg(w + c);
-        weights8<DT>(wv, offset, s[v]);
+        weights_vec<DT>(wv, offset, s[v]);
     }
 
     // Row order. Strided (default): rows blockIdx.x, + gridDim.x, ... Blocked: one
@@ -69,7 +69,7 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
 
         float ss = 0.f;
 #pragma unroll
-        for (int v = 0; v < V; ++v) ss = sumsq8<DT>(cur[v], ss);
+        for (int v = 0; v < V; ++v) ss = sumsq_vec<DT>(cur[v], ss);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         if (lane == 0) part[parity][wid] = ss;
@@ -82,7 +82,7 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = v * THREADS + tid;
-            if (c < nvec) st_stream(y + row * ldy + c, scale8<DT>(cur[v], r, s[v]));
+            if (c < nvec) st_stream(y + row * ldy + c, scale_vec<DT>(cur[v], r, s[v]));
         }
 #pragma unroll
         for (int v = 0; v < V; ++v) cur[v] = nxt[v];
@@ -110,7 +110,7 @@ Fn pick(int T, int V) {
 
 bool cta_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     if (!vector_ok(a)) return false;
-    const int64_t nvec = a.N / kVecElems;
+    const int64_t nvec = a.N / vec_elems(a.dtype);
     if (nvec > 1024 * 4) return false;
     int T = k.lanes_per_row;
     if (T == 0) {
@@ -122,7 +122,9 @@ bool cta_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     int V = 1;
     while (static_cast<int64_t>(V) * T < nvec) V <<= 1;
     if (V > 4) return false;
-    Fn fn = a.dtype == kBF16 ? pick<kBF16>(T, V) : pick<kFP16>(T, V);
+    Fn fn = a.dtype == kBF16   ? pick<kBF16>(T, V)
+            : a.dtype == kFP16 ? pick<kFP16>(T, V)
+                               : pick<kFP32>(T, V);
     if (!fn) return false;
     l.kernel = reinterpret_cast<const void*>(fn);
     l.threads = T;
@@ -137,11 +139,12 @@ bool cta_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
 
 cudaError_t cta_run(const Args& a, const Launch& l) {
     Fn fn = reinterpret_cast<Fn>(const_cast<void*>(l.kernel));
+    const int64_t e = vec_elems(a.dtype);
     LaunchCfg c(l, a.stream, l.pdl);
     return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
-                              a.M, static_cast<int>(a.N / kVecElems), a.ldx / kVecElems,
-                              a.ldy / kVecElems, static_cast<float>(a.N), a.eps, a.offset, l.mode());
+                              a.M, static_cast<int>(a.N / e), a.ldx / e, a.ldy / e,
+                              static_cast<float>(a.N), a.eps, a.offset, l.mode());
 }
 
 }  // namespace rmsn

@@ -1,4 +1,4 @@
-// General variant: any N, any 2-byte alignment. One CTA per row, persistent.
+// General variant: any N, any element alignment (2 bytes; 4 for fp32). One CTA per row, persistent.
 // Pass 1 reads the row element by element (consecutive threads on consecutive
 // elements, so each warp access is one contiguous 64-byte span) and sums the
 // squares in fp32; a warp butterfly plus a shared-memory step gives the row
@@ -16,9 +16,14 @@ namespace {
 
 template <int DT, int THREADS>
 __global__ void __launch_bounds__(THREADS)
-generic_rows_kernel(const uint16_t* x, const uint16_t* __restrict__ w, uint16_t* y,
+generic_rows_kernel(const void* xv, const void* __restrict__ wv, void* yv,
                     float* __restrict__ rstd, int64_t M, int64_t N, int64_t ldx, int64_t ldy,
                     float n, float eps, float offset) {
+    using E = Elem<DT>;
+    using T = typename E::T;
+    const T* x = static_cast<const T*>(xv);
+    const T* __restrict__ w = static_cast<const T*>(wv);
+    T* y = static_cast<T*>(yv);
     constexpr int kWarps = THREADS / 32;
     __shared__ float part[2][kWarps];
     const int tid = threadIdx.x;
@@ -26,10 +31,10 @@ generic_rows_kernel(const uint16_t* x, const uint16_t* __restrict__ w, uint16_t*
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
-        const uint16_t* xr = x + row * ldx;
+        const T* xr = x + row * ldx;
         float ss = 0.f;
         for (int64_t j = tid; j < N; j += THREADS) {
-            const float f = Codec<DT>::unpack1(xr[j]);
+            const float f = E::load(xr[j]);
             ss = fmaf(f, f, ss);
         }
 #pragma unroll
@@ -41,18 +46,18 @@ generic_rows_kernel(const uint16_t* x, const uint16_t* __restrict__ w, uint16_t*
         for (int k = 0; k < kWarps; ++k) tot += part[parity][k];
         const float r = row_rstd(tot, n, eps);
         if (tid == 0 && rstd != nullptr) rstd[row] = r;
-        uint16_t* yr = y + row * ldy;
+        T* yr = y + row * ldy;
         for (int64_t j = tid; j < N; j += THREADS) {
-            const float f = Codec<DT>::unpack1(xr[j]);
-            const float sw = offset + Codec<DT>::unpack1(__ldg(w + j));
-            yr[j] = Codec<DT>::pack1((f * r) * sw);
+            const float f = E::load(xr[j]);
+            const float sw = offset + E::load(__ldg(w + j));
+            yr[j] = E::store((f * r) * sw);
         }
         parity ^= 1;
     }
 }
 
-using Fn = void (*)(const uint16_t*, const uint16_t*, uint16_t*, float*, int64_t, int64_t, int64_t,
-                    int64_t, float, float, float);
+using Fn = void (*)(const void*, const void*, void*, float*, int64_t, int64_t, int64_t, int64_t,
+                    float, float, float);
 
 template <int DT>
 Fn pick(int T) {
@@ -75,7 +80,9 @@ bool generic_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& 
         T = 32;  // about four elements per thread, 32..512 threads
         while (T < 512 && static_cast<int64_t>(T) * 4 < a.N) T <<= 1;
     }
-    Fn fn = a.dtype == kBF16 ? pick<kBF16>(T) : pick<kFP16>(T);
+    Fn fn = a.dtype == kBF16   ? pick<kBF16>(T)
+            : a.dtype == kFP16 ? pick<kFP16>(T)
+                               : pick<kFP32>(T);
     if (!fn) return false;
     l.kernel = reinterpret_cast<const void*>(fn);
     l.threads = T;
@@ -91,10 +98,8 @@ bool generic_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& 
 cudaError_t generic_run(const Args& a, const Launch& l) {
     Fn fn = reinterpret_cast<Fn>(const_cast<void*>(l.kernel));
     LaunchCfg c(l, a.stream, l.pdl);
-    return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint16_t*>(a.x),
-                              static_cast<const uint16_t*>(a.w), static_cast<uint16_t*>(a.y),
-                              a.rstd, a.M, a.N, a.ldx, a.ldy, static_cast<float>(a.N), a.eps,
-                              a.offset);
+    return cudaLaunchKernelEx(&c.cfg, fn, a.x, a.w, a.y, a.rstd, a.M, a.N, a.ldx, a.ldy,
+                              static_cast<float>(a.N), a.eps, a.offset);
 }
 
 }  // namespace rmsn

@@ -96,13 +96,13 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     // No global memory is touched before the previous kernel completes, unless the
     // caller promised x and w are ready: then only the stores wait (below).
     if (!early) pdl_wait();
-    float s[V][kVecElems];
+    float s[V][VecElems<DT>::value];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = v * TEAM + t;
         uint4 wv = make_uint4(0u, 0u, 0u, 0u);
         if (c < nvec) wv = __ldg(w + c);
-        weights8<DT>(wv, offset, s[v]);
+        weights_vec<DT>(wv, offset, s[v]);
     }
     __syncthreads();
 
@@ -154,7 +154,7 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
                 const int c = v * TEAM + t;
                 xv[v] = make_uint4(0u, 0u, 0u, 0u);
                 if (act && c < nvec) xv[v] = sx[rr * nvec + c];
-                ss = sumsq8<DT>(xv[v], ss);
+                ss = sumsq_vec<DT>(xv[v], ss);
             }
 #pragma unroll
             for (int off = kLanes / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -175,7 +175,7 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
                     const int c = v * TEAM + t;
                     if (c < nvec)
                         st_stream(y + row * (CONTIG ? static_cast<int64_t>(nvec) : ldy) + c,
-                                  scale8<DT>(xv[v], r, s[v]));
+                                  scale_vec<DT>(xv[v], r, s[v]));
                 }
             }
         }
@@ -250,7 +250,7 @@ int next_pow2(int64_t v) {
 
 bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     if (!vector_ok(a)) return false;
-    const int64_t nvec = a.N / kVecElems;
+    const int64_t nvec = a.N / vec_elems(a.dtype);
     int team = k.lanes_per_row;
     if (team == 0) {
         // Four vectors per thread (two for rows of 8192+ columns), 16..1024
@@ -263,7 +263,9 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     const int V = next_pow2((nvec + team - 1) / team);
     if (V > 4) return false;
     const bool contig = a.ldx == a.N && a.ldy == a.N;
-    Fn fn = a.dtype == kBF16 ? pick<kBF16>(team, V, contig) : pick<kFP16>(team, V, contig);
+    Fn fn = a.dtype == kBF16   ? pick<kBF16>(team, V, contig)
+            : a.dtype == kFP16 ? pick<kFP16>(team, V, contig)
+                               : pick<kFP32>(team, V, contig);
     if (!fn) return false;
     const int threads = team < 256 ? 256 : team;
     const int teams = threads / team;
@@ -317,13 +319,14 @@ cudaError_t tma_run(const Args& a, const Launch& l) {
     // (2070 MHz), so the wait lasts at least the requested time at any clock.
     const long long limit = static_cast<long long>(l.wait_limit_ns * 21 / 10);
     const long long drain = kDrainLimitNs * 21 / 10;
+    const int64_t e = vec_elems(a.dtype);
     const int64_t stage_stride =
-        (static_cast<int64_t>(l.rows_per_stage) * (a.N / kVecElems) * 16 + 127) / 128 * 128;
+        (static_cast<int64_t>(l.rows_per_stage) * (a.N / e) * 16 + 127) / 128 * 128;
     LaunchCfg c(l, a.stream, l.pdl);
     return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
-                              a.M, static_cast<int>(a.N / kVecElems), a.ldx / kVecElems,
-                              a.ldy / kVecElems, static_cast<float>(a.N), a.eps, a.offset,
+                              a.M, static_cast<int>(a.N / e), a.ldx / e, a.ldy / e,
+                              static_cast<float>(a.N), a.eps, a.offset,
                               l.rows_per_stage, l.stages,
                               static_cast<int>(stage_stride), limit < 1 ? 1LL : limit, drain,
                               l.mode());

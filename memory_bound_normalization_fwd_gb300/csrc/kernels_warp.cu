@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
                  int64_t M, int nvec, int64_t ldx, int64_t ldy, float n, float eps, float offset,
                  int mode) {
-    extern __shared__ float4 sw[];  // 2 float4 of (offset + w) per 16-byte vector of w
+    extern __shared__ float4 sw[];  // (offset + w) in fp32, one float per element of w
     constexpr int kTeams = 32 / G;  // rows per warp per pass
     constexpr int kPass = kWarps * kTeams;  // rows per CTA per pass
     const int lane = threadIdx.x & 31;
@@ -56,12 +56,8 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
     }
 
     if (!early) pdl_wait();
-    for (int i = threadIdx.x; i < nvec; i += kWarps * 32) {
-        float s[kVecElems];
-        weights8<DT>(__ldg(w + i), offset, s);
-        sw[2 * i] = make_float4(s[0], s[1], s[2], s[3]);
-        sw[2 * i + 1] = make_float4(s[4], s[5], s[6], s[7]);
-    }
+    for (int i = threadIdx.x; i < nvec; i += kWarps * 32)
+        weights_vec_to_smem<DT>(__ldg(w + i), offset, sw, i);
     __syncthreads();
     pdl_launch_dependents();
 
@@ -88,7 +84,7 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
                 const int64_t row = row0 + team;
                 float ss = 0.f;
 #pragma unroll
-                for (int v = 0; v < V; ++v) ss = sumsq8<DT>(buf[d][v], ss);
+                for (int v = 0; v < V; ++v) ss = sumsq_vec<DT>(buf[d][v], ss);
 #pragma unroll
                 for (int off = G / 2; off > 0; off >>= 1)
                     ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -99,8 +95,7 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
                     for (int v = 0; v < V; ++v) {
                         const int c = v * G + sub;
                         if (c < nvec)
-                            st_stream(y + row * ldy + c,
-                                      scale8<DT>(buf[d][v], r, sw[2 * c], sw[2 * c + 1]));
+                            st_stream(y + row * ldy + c, scale_vec_smem<DT>(buf[d][v], r, sw, c));
                     }
                 }
                 const int64_t nrow = row + D * stride;
@@ -134,12 +129,14 @@ Fn pick_d(int G, int V) {
 
 template <int DT>
 Fn pick(int G, int V, int D) {
-    switch (D) {
-        case 1: return pick_d<DT, 1>(G, V);
-        case 2: return pick_d<DT, 2>(G, V);
-        case 4: return pick_d<DT, 4>(G, V);
-        default: return nullptr;
+    if (D == 1) return pick_d<DT, 1>(G, V);
+    // Deeper rings are measured slower on GB300 (kept as a knob for the 16-bit
+    // formats only, which keeps the fp32 build small).
+    if constexpr (DT != kFP32) {
+        if (D == 2) return pick_d<DT, 2>(G, V);
+        if (D == 4) return pick_d<DT, 4>(G, V);
     }
+    return nullptr;
 }
 
 int next_pow2(int v) {
@@ -152,7 +149,7 @@ int next_pow2(int v) {
 
 bool warp_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     if (!vector_ok(a)) return false;
-    const int64_t nvec = a.N / kVecElems;
+    const int64_t nvec = a.N / vec_elems(a.dtype);
     if (nvec > 32 * 4) return false;
     int G, V;
     if (k.lanes_per_row > 0) {
@@ -168,14 +165,16 @@ bool warp_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) 
         V = nvec <= 64 ? 2 : 4;
     }
     const int D = k.stages > 0 ? k.stages : 1;
-    Fn fn = a.dtype == kBF16 ? pick<kBF16>(G, V, D) : pick<kFP16>(G, V, D);
+    Fn fn = a.dtype == kBF16   ? pick<kBF16>(G, V, D)
+            : a.dtype == kFP16 ? pick<kFP16>(G, V, D)
+                               : pick<kFP32>(G, V, D);
     if (!fn) return false;
     l.kernel = reinterpret_cast<const void*>(fn);
     l.threads = kWarps * 32;
     l.lanes_per_row = G;
     l.vecs_per_lane = V;
     l.stages = D;
-    l.smem = static_cast<int>(nvec * 32);
+    l.smem = static_cast<int>(a.N * 4);  // (offset + w) in fp32
     l.ctas_per_sm = occupancy(l.kernel, l.threads, l.smem);
     l.work_items = a.M;
     l.grid = persistent_grid(a.M, static_cast<int64_t>(kWarps) * (32 / G), d.sm_count,
@@ -185,11 +184,12 @@ bool warp_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) 
 
 cudaError_t warp_run(const Args& a, const Launch& l) {
     Fn fn = reinterpret_cast<Fn>(const_cast<void*>(l.kernel));
+    const int64_t e = vec_elems(a.dtype);
     LaunchCfg c(l, a.stream, l.pdl);
     return cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                               static_cast<const uint4*>(a.w), static_cast<uint4*>(a.y), a.rstd,
-                              a.M, static_cast<int>(a.N / kVecElems), a.ldx / kVecElems,
-                              a.ldy / kVecElems, static_cast<float>(a.N), a.eps, a.offset, l.mode());
+                              a.M, static_cast<int>(a.N / e), a.ldx / e, a.ldy / e,
+                              static_cast<float>(a.N), a.eps, a.offset, l.mode());
 }
 
 }  // namespace rmsn

@@ -19,9 +19,13 @@ struct Args {
     int64_t ldy;  // row stride of y in elements (>= N)
     float eps;
     float offset;
-    int dtype;  // 0 bf16, 1 fp16
+    int dtype;  // 0 bf16, 1 fp16, 2 fp32
     cudaStream_t stream;
 };
+
+// Bytes per element, and elements per 16-byte vector, of a dtype.
+inline int elem_bytes(int dtype) { return dtype == 2 ? 4 : 2; }
+inline int vec_elems(int dtype) { return 16 / elem_bytes(dtype); }
 
 // Kernel `mode` argument bits.
 constexpr int kModeBlocked = 1;     // one contiguous block of rows per CTA
@@ -127,9 +131,9 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // The 16-byte-vector kernels need every row of x and y, and w, to start on a
 // 16-byte boundary and N to be a whole number of vectors.
 inline bool vector_ok(const Args& a) {
-    constexpr int64_t kElems = 8;
-    return a.N % kElems == 0 && a.ldx % kElems == 0 && a.ldy % kElems == 0 && aligned16(a.x) &&
-           aligned16(a.y) && aligned16(a.w);
+    const int64_t e = vec_elems(a.dtype);
+    return a.N % e == 0 && a.ldx % e == 0 && a.ldy % e == 0 && aligned16(a.x) && aligned16(a.y) &&
+           aligned16(a.w);
 }
 
 // Launch configuration shared by every variant: programmatic stream

@@ -72,6 +72,28 @@ WORKLOADS = {
 }
 BENCH_WORKLOAD = "rmsnorm_16384x512_bf16"
 
+# fp32 activations (x, w, y in fp32) at the benchmark shapes: not among the
+# named workloads above, which are the method's own; measured and tested as a
+# boundary variant of the same forward.
+EXTRA_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("rmsnorm_16384x512_fp32", 16384, 512, dtype="fp32"),
+        Workload("rmsnorm_32768x1000_fp32_gemma", 32768, 1000, dtype="fp32", w_kind="normal",
+                 w_a=0.0, w_b=0.1, offset=1.0),
+        Workload("rmsnorm_16384x8192_fp32_heavytail", 16384, 8192, dtype="fp32", outlier_p=0.01,
+                 outlier_std=100.0, eps=1e-5),
+        Workload("rmsnorm_65536x4096_fp32", 65536, 4096, dtype="fp32", x_std=64.0),
+    ]
+}
+
+
+def get(name: str) -> Workload:
+    """A named workload, or one of the fp32 ones."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    return EXTRA_WORKLOADS[name]
+
 
 def _bits(t: torch.Tensor, dtype: str) -> np.ndarray:
     ti, ni = _INT[dtype]

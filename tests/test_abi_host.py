@@ -65,7 +65,7 @@ def _call(lib, x=X, w=W_, y=Y, r=R, M=4, N=8, eps=1e-6, off=0.0, dt=0, opts=None
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(dt=2), -3), (dict(dt=-1), -3),
+    (dict(dt=3), -3), (dict(dt=-1), -3),
     (dict(M=-1), -2), (dict(N=0), -2), (dict(N=-5), -2), (dict(M=1 << 62, N=4), -2),
     (dict(eps=-1e-6), -4), (dict(eps=float("nan")), -4), (dict(eps=float("inf")), -4),
     (dict(off=float("nan")), -4), (dict(off=float("inf")), -4),
@@ -97,6 +97,25 @@ def _call_strided(lib, x=X, ldx=8, w=W_, y=Y, ldy=8, r=R, M=4, N=8, opts=None):
 def test_strided_validation_errors(lib, kw, code):
     assert _call_strided(lib, **kw) == code
     assert B.rmsnorm_last_error() != ""
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=X + 2), -10), (dict(y=Y + 2), -10), (dict(w=W_ + 2), -10),  # fp32: 4-byte alignment
+    (dict(y=X + 4 * 8 * 4 - 4), -5),      # y starts on x's last element
+    (dict(w=Y + 4 * 8 * 4 - 4), -5),      # w on y's last element (4-byte elements)
+    (dict(r=X + 4 * 8 * 4 - 4), -5),
+    (dict(M=1 << 44, N=8), -2),           # 2^46 elements of 4 bytes: 2^48 bytes
+])
+def test_fp32_validation_uses_four_byte_elements(lib, kw, code):
+    assert _call(lib, dt=2, **kw) == code
+    assert B.rmsnorm_last_error() != ""
+
+
+def test_backward_rejects_fp32(lib):
+    assert B.rmsnorm_bwd(X, W_, R, 0x60000000, Y, 0x70000000, 4, 8, 0.0, 2, 0x50000000, 1 << 20,
+                         None, 0) == -3
+    with pytest.raises(B.RMSNormError):
+        B.rmsnorm_bwd_workspace_size(4, 8, 2)
 
 
 def test_m_zero_is_ok_without_buffers(lib):
