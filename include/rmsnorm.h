@@ -22,9 +22,10 @@
  * launch shape always give the same bits.
  *
  * Memory. Every pointer is a DEVICE pointer on the calling thread's current
- * CUDA device (cudaSetDevice), allocated by the caller. The library never
- * allocates, frees or copies caller memory, and never synchronises except in
- * rmsnorm_check_device_status().
+ * CUDA device (cudaSetDevice), allocated by the caller, except the host
+ * buffers of rmsnorm_fwd_host(). The library never allocates or frees caller
+ * memory, copies it only in rmsnorm_fwd_host(), and never synchronises except
+ * in rmsnorm_check_device_status().
  *   x     [M, N] bf16, fp16 or fp32, contiguous row-major (row i at x + i*N)
  *   w     [N]    same dtype as x
  *   y     [M, N] same dtype as x; may equal x exactly (in place), must not
@@ -120,6 +121,13 @@ typedef enum rmsnorm_variant {
  * for that kernel to complete. Without the promise every access waits. Ignored
  * with RMSNORM_FLAG_NO_PDL and by the general kernel. */
 #define RMSNORM_FLAG_EARLY_LOADS 4
+/* rmsnorm_fwd_host only: no ring and no copies; the kernel reads x and writes
+ * y and rstd in page-locked host memory through their device addresses (the
+ * GPU's own loads and stores cross the host link). Needs every host buffer to
+ * be page-locked (cudaHostAlloc / cudaHostRegister), else
+ * RMSNORM_ERR_UNSUPPORTED; takes no workspace; only the plain-load kernels
+ * (WARP, CTA, GENERIC) run. Ignored by the device-memory calls. */
+#define RMSNORM_FLAG_HOST_DIRECT 8
 
 typedef struct rmsnorm_options {
     int32_t struct_size;     /* sizeof(rmsnorm_options_t) */
@@ -181,6 +189,49 @@ int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M
 int rmsnorm_fwd_strided(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy,
                         float* rstd, int64_t M, int64_t N, float eps, float offset, int dtype,
                         const rmsnorm_options_t* opts, void* stream);
+
+/*
+ * The forward over activations in HOST memory. The pages' kernels take device
+ * tensors and have no counterpart for this; it is the library's data path for
+ * activations that live in host memory (offloaded or served from host RAM).
+ * Same operation and arguments as rmsnorm_fwd_ex, except:
+ *   x_host, y_host  [M, N] contiguous, in host memory (pinned with
+ *                   cudaHostAlloc/cudaHostRegister for the copies to run
+ *                   asynchronously and overlap; pageable memory is correct but
+ *                   slower); y_host may equal x_host exactly
+ *   rstd_host       [M] fp32 in host memory, or NULL
+ *   w               [N] DEVICE pointer (weights stay resident)
+ *   chunk_rows      rows moved per chunk (> 0), or 0 for about 4 MiB of x
+ *   workspace       DEVICE memory, 16-byte aligned, of workspace_bytes >=
+ *                   rmsnorm_fwd_host_workspace_size(M, N, dtype, chunk_rows);
+ *                   owned by the caller, used by this call until it completes
+ *                   on `stream`, and not to be shared with work running at the
+ *                   same time
+ * Unless RMSNORM_FLAG_HOST_DIRECT is set (see there; then the workspace may be
+ * NULL), rows move in chunks through a ring of up to four slots of the workspace:
+ * host->device copies of x on a copy-in stream, the forward kernel in place on
+ * each slot on `stream`, device->host copies of y and rstd on a copy-out
+ * stream, chained by events. The two copy streams are the library's, one pair
+ * per device (made on first use, with that device current, and kept for the
+ * life of the process). Both directions of the host link thus run at once.
+ * The copy-in stream first waits for the work already on `stream`, and before
+ * returning `stream` is made to wait for the last copy-out, so work enqueued
+ * on `stream` after this call sees y and rstd in host memory; the host must
+ * not read them before that work (or a stream synchronisation) completes.
+ * RMSNORM_FLAG_EARLY_LOADS is ignored.
+ * Errors: as rmsnorm_fwd_ex, plus RMSNORM_ERR_NULL (workspace), _ALIGN
+ * (workspace), _WORKSPACE (too small), _OVERLAP (workspace against x, y, rstd
+ * or w), _CUDA. Argument errors are found before anything is enqueued.
+ */
+int rmsnorm_fwd_host(const void* x_host, const void* w, void* y_host, float* rstd_host, int64_t M,
+                     int64_t N, float eps, float offset, int dtype, int64_t chunk_rows,
+                     void* workspace, int64_t workspace_bytes, const rmsnorm_options_t* opts,
+                     void* stream);
+
+/* Device workspace bytes rmsnorm_fwd_host needs for these sizes and chunk rows
+ * (written to *bytes; 0 when M == 0). No CUDA call. */
+int rmsnorm_fwd_host_workspace_size(int64_t M, int64_t N, int dtype, int64_t chunk_rows,
+                                    int64_t* bytes);
 
 /* Fills *out with the launch rmsnorm_fwd_ex would make for these arguments on
  * the current device (no launch). x, w, y are used only for their alignment

@@ -24,8 +24,9 @@ STATUS = {
     -10: "RMSNORM_ERR_ALIGN", -11: "RMSNORM_ERR_WORKSPACE",
 }
 # Every function include/rmsnorm.h declares.
-EXPORTS = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_strided", "rmsnorm_bwd",
-           "rmsnorm_bwd_noalloc", "rmsnorm_bwd_workspace_size", "rmsnorm_plan_info", "rmsnorm_check_device_status",
+EXPORTS = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_strided", "rmsnorm_fwd_host",
+           "rmsnorm_fwd_host_workspace_size", "rmsnorm_bwd", "rmsnorm_bwd_noalloc",
+           "rmsnorm_bwd_workspace_size", "rmsnorm_plan_info", "rmsnorm_check_device_status",
            "rmsnorm_strerror", "rmsnorm_last_error", "rmsnorm_version")
 
 
@@ -82,6 +83,12 @@ def lib() -> ctypes.CDLL:
             L.rmsnorm_fwd_strided.argtypes = [vp, i64, vp, vp, i64, vp, i64, i64, f32, f32, i32,
                                               ctypes.POINTER(Options), vp]
             L.rmsnorm_fwd_strided.restype = i32
+            L.rmsnorm_fwd_host.argtypes = [vp, vp, vp, vp, i64, i64, f32, f32, i32, i64, vp, i64,
+                                           ctypes.POINTER(Options), vp]
+            L.rmsnorm_fwd_host.restype = i32
+            L.rmsnorm_fwd_host_workspace_size.argtypes = [i64, i64, i32, i64,
+                                                          ctypes.POINTER(ctypes.c_int64)]
+            L.rmsnorm_fwd_host_workspace_size.restype = i32
             L.rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp, i64,
                                       ctypes.POINTER(Options), vp]
             L.rmsnorm_bwd.restype = i32
@@ -115,15 +122,16 @@ def _check(rc: int) -> int:
 FLAG_NO_PDL = 1
 FLAG_BLOCKED_ROWS = 2
 FLAG_EARLY_LOADS = 4
+FLAG_HOST_DIRECT = 8
 
 
 def make_options(variant: str | int = "auto", max_ctas: int = 0, lanes_per_row: int = 0,
                  stages: int = 0, rows_per_stage: int = 0, wait_limit_ns: int = 0,
                  pdl: bool = True, blocked: bool = False, early_loads: bool = False,
-                 cluster_size: int = 0) -> Options:
+                 cluster_size: int = 0, host_direct: bool = False) -> Options:
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     flags = ((0 if pdl else FLAG_NO_PDL) | (FLAG_BLOCKED_ROWS if blocked else 0)
-             | (FLAG_EARLY_LOADS if early_loads else 0))
+             | (FLAG_EARLY_LOADS if early_loads else 0) | (FLAG_HOST_DIRECT if host_direct else 0))
     return Options(ctypes.sizeof(Options), v, max_ctas, lanes_per_row, stages, rows_per_stage,
                    flags, cluster_size, wait_limit_ns)
 
@@ -146,6 +154,21 @@ def rmsnorm_fwd_strided(x: int, ldx: int, w: int, y: int, ldy: int, rstd: int, M
                         stream: int) -> int:
     return lib().rmsnorm_fwd_strided(x, ldx, w, y, ldy, rstd, M, N, eps, offset, dtype,
                                      ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def rmsnorm_fwd_host(x_host: int, w: int, y_host: int, rstd_host: int, M: int, N: int,
+                     eps: float, offset: float, dtype: int, chunk_rows: int, workspace: int,
+                     workspace_bytes: int, opts: Options | None, stream: int) -> int:
+    """The forward over host-resident x/y/rstd (w and the workspace on the device)."""
+    return lib().rmsnorm_fwd_host(x_host, w, y_host, rstd_host, M, N, eps, offset, dtype,
+                                  chunk_rows, workspace, workspace_bytes,
+                                  ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def rmsnorm_fwd_host_workspace_size(M: int, N: int, dtype: int, chunk_rows: int = 0) -> int:
+    out = ctypes.c_int64(0)
+    _check(lib().rmsnorm_fwd_host_workspace_size(M, N, dtype, chunk_rows, ctypes.byref(out)))
+    return out.value
 
 
 def rmsnorm_bwd(x: int, w: int, rstd: int, dy: int, dx: int, dw: int, M: int, N: int,
@@ -247,6 +270,48 @@ def fwd(x, w, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=None, stream=
     with torch.cuda.device(x.device):
         _check(rmsnorm_fwd_strided(x.data_ptr(), ldx, w.data_ptr(), y.data_ptr(), ldy, r_ptr, M,
                                    N, eps, offset, _dtype_code(x), opts, s.cuda_stream))
+    return y, (None if rstd is False else rstd)
+
+
+def fwd_host(x, w, eps: float = 1e-6, offset: float = 0.0, y=None, rstd=None,
+             chunk_rows: int = 0, workspace=None, stream=None, **options):
+    """y, rstd = fwd_host(x, w): the forward of a contiguous CPU tensor x[..., N]
+    (pinned for overlapped copies) with w on the GPU, through rmsnorm_fwd_host.
+
+    ``y`` and ``rstd`` are CPU tensors (allocated pinned when not given; y may be
+    x itself); ``rstd=False`` skips rstd. The device ``workspace`` (a CUDA tensor)
+    is allocated here with torch when not given (none with ``host_direct=True``:
+    the kernel then reads and writes the pinned host buffers itself). The call
+    is asynchronous on
+    ``stream`` (or the current stream of w's device): synchronise before reading.
+    """
+    import torch
+    if x.is_cuda or not w.is_cuda:
+        raise ValueError("x must be a CPU tensor and w a CUDA tensor")
+    if not (x.is_contiguous() and w.is_contiguous()):
+        raise ValueError("x and w must be contiguous")
+    N = x.shape[-1]
+    if w.dtype != x.dtype or w.numel() != N:
+        raise ValueError("w must have x's dtype and N elements")
+    M = x.numel() // N if N else 0
+    if y is None:
+        y = torch.empty(x.shape, dtype=x.dtype).pin_memory()
+    if y.shape != x.shape or y.dtype != x.dtype or y.is_cuda or not y.is_contiguous():
+        raise ValueError("y must be a contiguous CPU tensor like x")
+    if rstd is None:
+        rstd = torch.empty(x.shape[:-1], dtype=torch.float32).pin_memory()
+    r_ptr = 0 if rstd is False else rstd.data_ptr()
+    code = _dtype_code(x)
+    opts = make_options(**options) if options else None
+    with torch.cuda.device(w.device):
+        need = rmsnorm_fwd_host_workspace_size(M, N, code, chunk_rows)
+        if workspace is None and not options.get("host_direct"):
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=w.device)
+        s = stream if stream is not None else torch.cuda.current_stream(w.device)
+        ws_ptr = 0 if workspace is None else workspace.data_ptr()
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _check(rmsnorm_fwd_host(x.data_ptr(), w.data_ptr(), y.data_ptr(), r_ptr, M, N, eps,
+                                offset, code, chunk_rows, ws_ptr, ws_bytes, opts, s.cuda_stream))
     return y, (None if rstd is False else rstd)
 
 

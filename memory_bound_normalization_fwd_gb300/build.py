@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(CSRC, "_build")
 LIB = os.path.join(PKG, "librmsnorm_gb300.so")
 SOURCES = ["api.cu", "kernels_warp.cu", "kernels_cta.cu", "kernels_tma.cu", "kernels_cluster.cu",
-           "kernels_generic.cu", "kernels_bwd.cu"]
+           "kernels_generic.cu", "kernels_bwd.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -15,8 +15,8 @@
 
 namespace rmsn {
 namespace {
-
 thread_local char t_last_error[512] = "";
+}  // namespace
 
 int fail(int code, const char* fmt, ...) {
     va_list ap;
@@ -25,6 +25,8 @@ int fail(int code, const char* fmt, ...) {
     va_end(ap);
     return code;
 }
+
+namespace {
 
 constexpr int kMaxDevices = 64;
 std::once_flag g_dev_once[kMaxDevices];
@@ -49,6 +51,8 @@ cudaError_t device_info(DeviceInfo* out) {
     *out = g_dev[dev];
     return cudaSuccess;
 }
+
+}  // namespace
 
 bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
@@ -115,7 +119,8 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
                     o->variant);
     if (o->max_ctas < 0 || o->lanes_per_row < 0 || o->rows_per_stage < 0 || o->stages < 0 ||
         o->stages > 8 || o->wait_limit_ns < 0 || o->cluster_size < 0 || o->cluster_size > 16 ||
-        (o->flags & ~(RMSNORM_FLAG_NO_PDL | RMSNORM_FLAG_BLOCKED_ROWS | RMSNORM_FLAG_EARLY_LOADS)) != 0)
+        (o->flags & ~(RMSNORM_FLAG_NO_PDL | RMSNORM_FLAG_BLOCKED_ROWS | RMSNORM_FLAG_EARLY_LOADS |
+                      RMSNORM_FLAG_HOST_DIRECT)) != 0)
         return fail(RMSNORM_ERR_OPTIONS, "options fields out of range");
     *variant = o->variant;
     k->flags = o->flags;
@@ -127,6 +132,8 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
     k->cluster_size = o->cluster_size;
     return RMSNORM_OK;
 }
+
+namespace {
 
 // Chooses the variant. The automatic choice, when x, w and y are 16-byte
 // aligned and rows are whole 16-byte vectors (measured on GB300, bf16; the
@@ -143,6 +150,20 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
 int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch& l,
          int* chosen) {
     bool ok = false;
+    if (k.flags & kKnobNoBulkCopies) {
+        // Operands in host memory, read by the kernel over the host link: only
+        // the kernels that use plain loads and stores.
+        if (variant == RMSNORM_VARIANT_TMA || variant == RMSNORM_VARIANT_CLUSTER)
+            return fail(RMSNORM_ERR_UNSUPPORTED,
+                        "variant %d stages rows with bulk copies; host-direct needs plain loads",
+                        variant);
+        if (variant == RMSNORM_VARIANT_AUTO) {
+            const int64_t row_bytes = a.N * elem_bytes(a.dtype);
+            if (row_bytes <= 2048 && warp_choose(a, d, k, l)) variant = RMSNORM_VARIANT_WARP;
+            else if ((l = Launch{}, cta_choose(a, d, k, l))) variant = RMSNORM_VARIANT_CTA;
+            else variant = RMSNORM_VARIANT_GENERIC, l = Launch{};
+        }
+    }
     switch (variant) {
         case RMSNORM_VARIANT_WARP: ok = warp_choose(a, d, k, l); break;
         case RMSNORM_VARIANT_CTA: ok = cta_choose(a, d, k, l); break;
@@ -208,12 +229,6 @@ int occupancy(const void* kernel, int threads, int smem) {
     return n;
 }
 
-}  // namespace rmsn
-
-using namespace rmsn;
-
-namespace {
-
 int forward(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, float* rstd,
             int64_t M, int64_t N, float eps, float offset, int dtype,
             const rmsnorm_options_t* opts, void* stream) {
@@ -223,6 +238,14 @@ int forward(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, flo
     Knobs k;
     rc = read_knobs(opts, &variant, &k);
     if (rc != RMSNORM_OK) return rc;
+    k.flags &= ~RMSNORM_FLAG_HOST_DIRECT;  // meaningful for rmsnorm_fwd_host only
+    return forward_knobs(x, ldx, w, y, ldy, rstd, M, N, eps, offset, dtype, variant, k, stream);
+}
+
+int forward_knobs(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, float* rstd,
+                  int64_t M, int64_t N, float eps, float offset, int dtype, int variant,
+                  const Knobs& k, void* stream) {
+    int rc = RMSNORM_OK;
     if (M == 0) return RMSNORM_OK;
     DeviceInfo d;
     cudaError_t e = device_info(&d);
@@ -241,7 +264,9 @@ int forward(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, flo
     return RMSNORM_OK;
 }
 
-}  // namespace
+}  // namespace rmsn
+
+using namespace rmsn;
 
 extern "C" int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M,
                               int64_t N, float eps, float offset, int dtype,

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "rmsnorm.h"
+
 namespace rmsn {
 
 // Everything a kernel launch needs, already validated by the front end.
@@ -51,6 +53,10 @@ struct Launch {
     bool early = false;    // x and w may be read before the previous kernel completes
     int mode() const { return (blocked ? kModeBlocked : 0) | (early ? kModeEarlyLoads : 0); }
 };
+
+// Internal knob bit (above the public RMSNORM_FLAG_* bits): the operands are in
+// host memory read by the kernel itself, so only plain-load kernels may run.
+constexpr int kKnobNoBulkCopies = 1 << 20;
 
 // Caller knobs (rmsnorm_options_t), validated by the front end. 0 = planner's choice.
 struct Knobs {
@@ -110,6 +116,22 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
 cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial);
 // The backward's built-in scratch on the current device (set up on first use).
 cudaError_t bwd_builtin_scratch(float** ptr, int64_t* floats);
+
+// Front end (api.cu), shared with the host-buffer path: the thread's error
+// detail (returns `code`), the forward's argument checks, byte-span overlap,
+// option decoding, and the whole device forward (checks, plan, launch).
+int fail(int code, const char* fmt, ...);
+int validate(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, float* rstd,
+             int64_t M, int64_t N, float eps, float offset, int dtype);
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes);
+int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k);
+int forward(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, float* rstd,
+            int64_t M, int64_t N, float eps, float offset, int dtype,
+            const rmsnorm_options_t* opts, void* stream);
+// The forward after validation, with decoded knobs (may carry internal bits).
+int forward_knobs(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, float* rstd,
+                  int64_t M, int64_t N, float eps, float offset, int dtype, int variant,
+                  const Knobs& k, void* stream);
 
 // Device status words (bounded-wait timeouts) of the staged variants: read and
 // clear on the current device.

@@ -126,7 +126,7 @@ def test_m_zero_is_ok_without_buffers(lib):
 @pytest.mark.parametrize("field,value", [("variant", 6), ("variant", -1), ("max_ctas", -1),
                                          ("stages", 9), ("stages", -1), ("wait_limit_ns", -5),
                                          ("lanes_per_row", -2), ("struct_size", 8),
-                                         ("flags", 8), ("cluster_size", 17),
+                                         ("flags", 16), ("cluster_size", 17),
                                          ("cluster_size", -1)])
 def test_bad_options(lib, field, value):
     o = B.make_options()
@@ -148,3 +148,51 @@ def test_bwd_validation_errors(lib):
     assert call(dx=X + 2) == -5          # partial overlap with x
     assert call(dw=W_) == -5             # dw over w
     assert call(r=R + 1) == -10
+
+
+# ---------------------------------------------------------------- host-buffer forward
+
+@pytest.mark.parametrize("M,N,dt,chunk,want", [
+    (0, 512, 0, 0, 0),                                    # slots + rstd of all M rows:
+    (10, 512, 0, 0, 10240 + 256),                         # one chunk of all 10 rows: one slot
+    (100000, 512, 0, 0, 4 * (4 << 20) + 400128),          # 4096-row chunks (4 MiB), four slots
+    (20, 3, 2, 7, 3 * 256 + 256),                         # fp32, 3 chunks of 7 rows: 3 slots
+    (14, 3, 2, 7, 2 * 256 + 256),                         # two chunks: two slots
+    (5, 1000, 1, 1, 4 * 2048 + 256),                      # one row per chunk
+])
+def test_host_path_workspace_size(lib, M, N, dt, chunk, want):
+    assert B.rmsnorm_fwd_host_workspace_size(M, N, dt, chunk) == want
+
+
+@pytest.mark.parametrize("args,code", [((4, 8, 5, 0), -3), ((4, 8, 0, -1), -2), ((-1, 8, 0, 0), -2),
+                                       ((4, 0, 0, 0), -2)])
+def test_host_path_workspace_size_errors(lib, args, code):
+    with pytest.raises(B.RMSNormError) as e:
+        B.rmsnorm_fwd_host_workspace_size(*args)
+    assert e.value.status == code
+
+
+HX, HY, HR = 0x7F0000000000, 0x7F0010000000, 0x7F0020000000  # "host" addresses, never touched
+WS = 0x50000000
+
+
+def _host_call(lib, x=HX, w=W_, y=HY, r=HR, M=4, N=8, dt=0, chunk=0, ws=WS, nbytes=1 << 20,
+               opts=None):
+    return B.rmsnorm_fwd_host(x, w, y, r, M, N, 1e-6, 0.0, dt, chunk, ws, nbytes, opts, 0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), -1), (dict(ws=WS + 8), -10), (dict(nbytes=100), -11),
+    (dict(ws=W_), -5),                         # workspace over w
+    (dict(ws=HX, nbytes=1 << 20), -5),         # workspace over x
+    (dict(w=0), -1), (dict(x=0), -1), (dict(dt=7), -3), (dict(chunk=-3), -2),
+    (dict(y=HX + 2), -5),                      # y partly over x
+    (dict(r=HX + 4), -5),                      # rstd inside x
+])
+def test_host_path_validation_before_any_cuda_call(lib, kw, code):
+    assert _host_call(lib, **kw) == code
+    assert B.rmsnorm_last_error() != ""
+
+
+def test_host_path_m_zero_needs_nothing(lib):
+    assert _host_call(lib, x=0, y=0, r=0, M=0, ws=0, nbytes=0) == 0
