@@ -158,10 +158,25 @@ int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch
                         "variant %d stages rows with bulk copies; host-direct needs plain loads",
                         variant);
         if (variant == RMSNORM_VARIANT_AUTO) {
-            const int64_t row_bytes = a.N * elem_bytes(a.dtype);
-            if (row_bytes <= 2048 && warp_choose(a, d, k, l)) variant = RMSNORM_VARIANT_WARP;
-            else if ((l = Launch{}, cta_choose(a, d, k, l))) variant = RMSNORM_VARIANT_CTA;
-            else variant = RMSNORM_VARIANT_GENERIC, l = Launch{};
+            // The kernel the device-memory call would run, or, for the TMA kernel,
+            // the plain-load kernel with the same per-row reduction (team of T
+            // threads, V vectors each: the warp kernel for T <= 32, the CTA kernel
+            // above), so both calls give the same bits. The cluster kernel's
+            // slice sums have no plain-load counterpart: those rows take the
+            // general kernel (within the same 1-ulp parity, not bit-identical).
+            Knobs kd = k;
+            kd.flags &= ~kKnobNoBulkCopies;
+            Launch ld;
+            int dev = RMSNORM_VARIANT_GENERIC;
+            if (plan(a, d, RMSNORM_VARIANT_AUTO, kd, ld, &dev) != RMSNORM_OK) return RMSNORM_ERR_UNSUPPORTED;
+            Knobs km = k;
+            if (dev == RMSNORM_VARIANT_TMA) {
+                km.lanes_per_row = ld.lanes_per_row;
+                variant = ld.lanes_per_row <= 32 ? RMSNORM_VARIANT_WARP : RMSNORM_VARIANT_CTA;
+            } else {
+                variant = dev == RMSNORM_VARIANT_CLUSTER ? RMSNORM_VARIANT_GENERIC : dev;
+            }
+            return plan(a, d, variant, km, l, chosen);
         }
     }
     switch (variant) {

@@ -276,13 +276,18 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     const int64_t row_bytes = nvec * 16;
     // Stage shape, measured on GB300 (1 KB .. 16 KB rows): rows under 4 KB take
     // 16 KB stages, two deep (small footprint, so the next launch's CTAs fit in
-    // early); 4-8 KB rows take 32 KB stages and longer rows one row per stage,
-    // four deep. A stage of several rows holds a whole number of rows per team.
+    // early); 4-8 KB rows take 32 KB stages, four deep. Longer 16-bit rows take
+    // one row per stage, three deep, at two CTAs per SM (16384x8192 bf16: 6.62
+    // TB/s, against 6.60 four deep; 65536x8192: 6.60 against 6.39). Longer fp32
+    // rows keep 32 KB stages, four deep: their kernel needs fewer registers, so
+    // one-row stages would run three CTAs per SM and 192 KB in flight per SM,
+    // which measured 5.80 TB/s at 65536x4096 against 6.87 for two-row stages at
+    // one CTA per SM. A stage of several rows holds a whole number of rows per team.
     const bool short_rows = row_bytes < 4096;
+    const bool long_narrow = row_bytes > 8192 && elem_bytes(a.dtype) == 2;
     int64_t R = k.rows_per_stage;
     if (R == 0) {
-        R = short_rows ? (16 * 1024) / row_bytes
-                       : (row_bytes <= 8192 ? (32 * 1024) / row_bytes : 1);
+        R = short_rows ? (16 * 1024) / row_bytes : (long_narrow ? 1 : (32 * 1024) / row_bytes);
         if (R > teams) R = R / teams * teams;
         if (R < 1) R = 1;
     }
@@ -291,7 +296,8 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     // With early loads, 2-4 KB rows gain from four stages too (32768x1000 bf16:
     // 6.6-6.75 TB/s against 6.1-6.55 at two stages); 1 KB rows do not.
     const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) && !(k.flags & RMSNORM_FLAG_NO_PDL);
-    int S = k.stages > 0 ? k.stages : (short_rows && !(early && row_bytes >= 2048) ? 2 : 4);
+    int S = k.stages > 0 ? k.stages
+                         : (short_rows && !(early && row_bytes >= 2048) ? 2 : (long_narrow ? 3 : 4));
     if (S < 1 || S > kMaxStages) return false;
     if (k.stages == 0)
         while (S > 1 && kAlignSlack + kHeaderBytes + S * stage_stride > max_dyn) --S;

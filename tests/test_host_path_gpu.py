@@ -143,10 +143,11 @@ def test_host_direct_matches_oracle_and_device_path(M, N, dtype):
     torch.cuda.synchronize()
     _oracle_check(x, w, W.from_torch(y), r.numpy(), wl, where=f"direct {M}x{N} {dtype}")
     if N * W.ELEM_BYTES[dtype] <= 65536:
-        # Same row reduction order as the device call (rows up to 64 KB take
-        # register or staged kernels with the same per-thread/warp order there;
-        # longer rows take the cluster kernel on the device and the general
-        # kernel here, whose sums associate differently: oracle parity only).
+        # Same bits as the device call: host-direct runs the device plan's
+        # kernel, or for a TMA plan the plain-load kernel with the same team and
+        # vectors per thread (the same sum order). Rows over 64 KB take the
+        # cluster kernel on the device and the general kernel here, whose sums
+        # associate differently: oracle parity only.
         yd, rd = _device_reference(xt, wd, wl)
         iv = torch.int32 if dtype == "fp32" else torch.int16
         assert torch.equal(y.view(iv), yd.view(iv)) and torch.equal(r, rd)
