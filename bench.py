@@ -371,11 +371,12 @@ def bench_ours(args, wl, rank, world, local_rank):
     pool, set_bytes, l2, stream, sh = pb.pool, pb.set_bytes, pb.l2, pb.stream, pb.stream.cuda_stream
     timed = pb.timed
 
-    def make_opts(early: bool):
+    def make_opts(early: bool, early_weights: bool = False):
         return B.make_options(variant=args.variant, lanes_per_row=args.lanes_per_row,
                               stages=args.stages, rows_per_stage=args.rows_per_stage,
                               max_ctas=args.max_ctas, early_loads=early, blocked=args.blocked,
-                              pdl=not args.no_pdl, cluster_size=args.cluster_size)
+                              pdl=not args.no_pdl, cluster_size=args.cluster_size,
+                              early_weights=early_weights)
 
     # Main measurement. The steps are independent batches (x and w are written
     # by no step), which meets the precondition of RMSNORM_FLAG_EARLY_LOADS:
@@ -397,12 +398,17 @@ def bench_ours(args, wl, rank, world, local_rank):
         splan = B.rmsnorm_plan_info(wl.M, wl.N, dcode, xs[0].data_ptr(), w_dev.data_ptr(),
                                     ys[0].data_ptr(), sopts)
         Ks = min(K, 100000)
+        # Weights resident (as in inference), x the previous step's output: the
+        # strict chain with only w read early.
+        w_max, _, _, _ = timed(make_opts(False, True), Ks, Wm)
         s_max, s_launch, _, _ = timed(sopts, Ks, Wm)
         strict = {"value": round(whole_job_gbs(wl.algorithmic_bytes, Ks, world, s_max), 2),
                   "unit": "GB/s", "steps": Ks,
                   "frac": None, "plan": splan,
+                  "early_weights": round(whole_job_gbs(wl.algorithmic_bytes, Ks, world, w_max), 2),
                   "note": "no RMSNORM_FLAG_EARLY_LOADS: each launch reads x only after the "
-                          "previous step completes"}
+                          "previous step completes; early_weights: the same with "
+                          "RMSNORM_FLAG_EARLY_WEIGHTS (w read before the wait, x after)"}
     opts = make_opts(False)  # the end-to-end leg keeps strict order (copies precede each call)
 
     # End to end through the public host-buffer call: per step, rmsnorm_fwd_host
@@ -532,7 +538,8 @@ def ablation_configs(wl):
     occupancy; plus launch overlap and row order)."""
     eb = 4 if wl.dtype == "fp32" else 2
     nvec, row = wl.N * eb // 16, eb * wl.N
-    cfgs = [dict(), dict(early_loads=True), dict(pdl=False), dict(blocked=True)]
+    cfgs = [dict(), dict(early_loads=True), dict(early_weights=True), dict(pdl=False),
+            dict(blocked=True)]
     if nvec <= 128:
         for G in (8, 16, 32):
             for D in (1, 2, 4):

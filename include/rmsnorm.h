@@ -121,6 +121,13 @@ typedef enum rmsnorm_variant {
  * for that kernel to complete. Without the promise every access waits. Ignored
  * with RMSNORM_FLAG_NO_PDL and by the general kernel. */
 #define RMSNORM_FLAG_EARLY_LOADS 4
+/* The caller promises only that no kernel still running earlier on the stream
+ * writes w (a weight that is not being updated, as in inference); x may be
+ * the previous kernel's output. The kernel then reads w before the previous
+ * kernel finishes and waits only before reading x, taking the weight load off
+ * the critical path of a chain of dependent kernels. Ignored with
+ * RMSNORM_FLAG_NO_PDL and by the general kernel; implied by EARLY_LOADS. */
+#define RMSNORM_FLAG_EARLY_WEIGHTS 16
 /* rmsnorm_fwd_host only: no ring and no copies; the kernel reads x and writes
  * y and rstd in page-locked host memory through their device addresses (the
  * GPU's own loads and stores cross the host link). Needs every host buffer to

@@ -120,7 +120,7 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
     if (o->max_ctas < 0 || o->lanes_per_row < 0 || o->rows_per_stage < 0 || o->stages < 0 ||
         o->stages > 8 || o->wait_limit_ns < 0 || o->cluster_size < 0 || o->cluster_size > 16 ||
         (o->flags & ~(RMSNORM_FLAG_NO_PDL | RMSNORM_FLAG_BLOCKED_ROWS | RMSNORM_FLAG_EARLY_LOADS |
-                      RMSNORM_FLAG_HOST_DIRECT)) != 0)
+                      RMSNORM_FLAG_HOST_DIRECT | RMSNORM_FLAG_EARLY_WEIGHTS)) != 0)
         return fail(RMSNORM_ERR_OPTIONS, "options fields out of range");
     *variant = o->variant;
     k->flags = o->flags;
@@ -274,6 +274,7 @@ int forward_knobs(const void* x, int64_t ldx, const void* w, void* y, int64_t ld
     l.pdl = (k.flags & RMSNORM_FLAG_NO_PDL) == 0;
     l.blocked = (k.flags & RMSNORM_FLAG_BLOCKED_ROWS) != 0;
     l.early = l.pdl && (k.flags & RMSNORM_FLAG_EARLY_LOADS) != 0;
+    l.early_weights = l.pdl && (k.flags & RMSNORM_FLAG_EARLY_WEIGHTS) != 0;
     e = run(chosen, a, l);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
     return RMSNORM_OK;

@@ -99,6 +99,7 @@ cluster_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float
     const int my_vecs = nvec - v0 < slice_vecs ? nvec - v0 : slice_vecs;  // >= 1 by planning
     const int64_t nlocal = cluster < M ? (M - cluster + nclusters - 1) / nclusters : 0;
     const bool early = (mode & kModeEarlyLoads) != 0;
+    const bool early_w = (mode & kModeEarlyWeights) != 0;
 
     const uint32_t raw = smem_u32(smem);
     unsigned char* base = smem + (((raw + 127u) & ~127u) - raw);
@@ -114,7 +115,7 @@ cluster_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float
         fence_mbar_init();
     }
     __syncthreads();
-    if (!early) pdl_wait();
+    if (!early && !early_w) pdl_wait();
 
     auto issue = [&](int64_t k) {
         if (k >= nlocal) return;
@@ -127,6 +128,9 @@ cluster_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float
     if (tid == 0) {
         mbar_arrive_expect_tx(wbar, slice_bytes);
         bulk_g2s(smem_u32(base + kHeader), w + v0, slice_bytes, wbar);
+    }
+    if (early_w && !early) pdl_wait();  // x only after the previous kernel completes
+    if (tid == 0) {
         for (int k = 0; k < stages; ++k) issue(k);
     }
     pdl_launch_dependents();

@@ -31,7 +31,8 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
 
     const bool blocked = (mode & kModeBlocked) != 0;
     const bool early = (mode & kModeEarlyLoads) != 0;
-    if (!early) pdl_wait();
+    const bool early_w = (mode & kModeEarlyWeights) != 0;
+    if (!early && !early_w) pdl_wait();
     pdl_launch_dependents();
     float s[V][VecElems<DT>::value];
 #pragma unroll
@@ -41,6 +42,7 @@ cta_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         if (c < nvec) wv = __ldg(w + c);
         weights_vec<DT>(wv, offset, s[v]);
     }
+    if (early_w && !early) pdl_wait();  // x only after the previous kernel completes
 
     // Row order. Strided (default): rows blockIdx.x, + gridDim.x, ... Blocked: one
     // contiguous block per CTA, the blocks differing by at most one row.

@@ -68,6 +68,7 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     const int t = tid % TEAM;
     const bool blocked = (mode & kModeBlocked) != 0;
     const bool early = (mode & kModeEarlyLoads) != 0;
+    const bool early_w = (mode & kModeEarlyWeights) != 0;
     const int R = rows_per_stage;
     // Chunks of R consecutive rows. Strided (default): this CTA takes chunks
     // blockIdx.x, + gridDim.x, ... of x. Blocked: this CTA owns one contiguous
@@ -94,8 +95,9 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         fence_mbar_init();
     }
     // No global memory is touched before the previous kernel completes, unless the
-    // caller promised x and w are ready: then only the stores wait (below).
-    if (!early) pdl_wait();
+    // caller promised w (early weights) or x and w (early loads) are not being
+    // written: then those reads go first and only the rest waits.
+    if (!early && !early_w) pdl_wait();
     float s[V][VecElems<DT>::value];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -105,6 +107,7 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         weights_vec<DT>(wv, offset, s[v]);
     }
     __syncthreads();
+    if (early_w && !early) pdl_wait();  // x only after the previous kernel completes
 
     // Local chunk k goes to stage k % stages.
     auto issue = [&](int64_t k) {

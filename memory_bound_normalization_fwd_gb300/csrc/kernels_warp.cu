@@ -44,6 +44,7 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
     // back. Blocked: each CTA owns one contiguous block of rows (block sizes
     // differing by at most one row) and sweeps it alone.
     const bool early = (mode & kModeEarlyLoads) != 0;
+    const bool early_w = (mode & kModeEarlyWeights) != 0;
     int64_t first0, stride, r_end;  // team 0 of this warp in pass 0; rows per pass; bound
     if (mode & kModeBlocked) {
         first0 = static_cast<int64_t>(blockIdx.x) * M / gridDim.x + wid * kTeams;
@@ -55,11 +56,12 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
         stride = static_cast<int64_t>(gridDim.x) * kPass;
     }
 
-    if (!early) pdl_wait();
+    if (!early && !early_w) pdl_wait();
     for (int i = threadIdx.x; i < nvec; i += kWarps * 32)
         weights_vec_to_smem<DT>(__ldg(w + i), offset, sw, i);
     __syncthreads();
     pdl_launch_dependents();
+    if (early_w && !early) pdl_wait();  // x only after the previous kernel completes
 
     uint4 buf[D][V];
 #pragma unroll

@@ -32,6 +32,7 @@ inline int vec_elems(int dtype) { return 16 / elem_bytes(dtype); }
 // Kernel `mode` argument bits.
 constexpr int kModeBlocked = 1;     // one contiguous block of rows per CTA
 constexpr int kModeEarlyLoads = 2;  // first loads of x and w before the PDL wait (caller's promise)
+constexpr int kModeEarlyWeights = 4;  // w (not x) read before the PDL wait (caller's promise)
 
 // A launch shape chosen by a variant's planner.
 struct Launch {
@@ -51,7 +52,11 @@ struct Launch {
     bool pdl = true;
     bool blocked = false;  // contiguous row block per CTA instead of strided passes
     bool early = false;    // x and w may be read before the previous kernel completes
-    int mode() const { return (blocked ? kModeBlocked : 0) | (early ? kModeEarlyLoads : 0); }
+    bool early_weights = false;  // w may be read before the previous kernel completes
+    int mode() const {
+        return (blocked ? kModeBlocked : 0) | (early ? kModeEarlyLoads : 0) |
+               (early_weights ? kModeEarlyWeights : 0);
+    }
 };
 
 // Internal knob bit (above the public RMSNORM_FLAG_* bits): the operands are in

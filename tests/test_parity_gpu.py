@@ -271,10 +271,13 @@ def _raw_call(x, w, y, r, M, N, eps, offset, **opts):
 
 @pytest.mark.parametrize("variant,N", [("warp", 512), ("tma", 1000), ("tma", 4096),
                                        ("cta", 8192), ("generic", 1000), ("cluster", 65536)])
-def test_chained_calls_keep_stream_order(variant, N):
+@pytest.mark.parametrize("early_weights", [False, True], ids=["plain", "early_weights"])
+def test_chained_calls_keep_stream_order(variant, N, early_weights):
     # Each call reads the previous call's output (ping-pong between two buffers),
     # launched back to back with programmatic dependent launch: the result must be
-    # bit-identical to the same calls separated by a device synchronize.
+    # bit-identical to the same calls separated by a device synchronize. With
+    # early weights the kernels read w before the previous call ends, but x
+    # (the previous output) only after it.
     M = 3000
     wl = W.custom(M, N, "bf16", seed=N + 17)
     x, w = W.generate(wl)
@@ -285,10 +288,10 @@ def test_chained_calls_keep_stream_order(variant, N):
         b = torch.empty_like(a)
         r = torch.empty(M, dtype=torch.float32, device="cuda")
         for _ in range(12):
-            _raw_call(a, w_dev, b, r, M, N, 1e-6, 0.0, variant=variant)
+            _raw_call(a, w_dev, b, r, M, N, 1e-6, 0.0, variant=variant, early_weights=early_weights)
             if sync:
                 torch.cuda.synchronize()
-            _raw_call(b, w_dev, a, r, M, N, 1e-6, 0.0, variant=variant)
+            _raw_call(b, w_dev, a, r, M, N, 1e-6, 0.0, variant=variant, early_weights=early_weights)
             if sync:
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
