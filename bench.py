@@ -35,9 +35,9 @@ sys.path.insert(0, ROOT)
 METRIC = "RMSNorm fwd achieved HBM GB/s and % of GB300 peak (1 GPU), per M×N×dtype"
 DCODE = {"bf16": 0, "fp16": 1, "fp32": 2}  # rmsnorm_dtype_t
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["common.cuh", "async_copy.cuh", "launch.h", "kernels_warp.cu", "kernels_cta.cu",
-                  "kernels_tma.cu", "kernels_cluster.cu", "kernels_generic.cu", "kernels_bwd.cu",
-                  "api.cu"]
+KERNEL_SOURCES = ["common.cuh", "async_copy.cuh", "cluster.cuh", "launch.h", "kernels_warp.cu",
+                  "kernels_cta.cu", "kernels_tma.cu", "kernels_cluster.cu", "kernels_generic.cu",
+                  "kernels_bwd.cu", "api.cu", "host_pipeline.cu"]
 
 
 # ---------------------------------------------------------------- host-side helpers
@@ -112,7 +112,7 @@ def load_peaks():
 # it includes); a traffic figure stays valid while these and the launch plan do.
 VARIANT_SOURCES = {
     "warp": ["kernels_warp.cu"], "cta": ["kernels_cta.cu"], "tma": ["kernels_tma.cu"],
-    "cluster": ["kernels_cluster.cu"], "generic": ["kernels_generic.cu"],
+    "cluster": ["cluster.cuh", "kernels_cluster.cu"], "generic": ["kernels_generic.cu"],
 }
 COMMON_SOURCES = ["common.cuh", "async_copy.cuh", "launch.h"]
 
@@ -616,7 +616,9 @@ def bench_backward(args, wl):
     dxs = [torch.empty_like(x0) for _ in range(pool)]
     rs = [r0.clone() for _ in range(pool)]
     dw = torch.empty(wl.N, dtype=torch.float32, device=dev)
-    nbytes = B.rmsnorm_bwd_workspace_size(wl.M, wl.N, dcode)
+    opts = B.make_options(variant=args.variant, max_ctas=args.max_ctas,
+                          lanes_per_row=args.lanes_per_row)
+    nbytes = B.rmsnorm_bwd_workspace_size(wl.M, wl.N, dcode, opts)
     ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
@@ -625,7 +627,7 @@ def bench_backward(args, wl):
         i = k % pool
         rc = B.rmsnorm_bwd(xs[i].data_ptr(), w.data_ptr(), rs[i].data_ptr(), dys[i].data_ptr(),
                            dxs[i].data_ptr(), dw.data_ptr(), wl.M, wl.N, wl.offset, dcode,
-                           ws.data_ptr(), ws.numel() * 4, None, sh)
+                           ws.data_ptr(), ws.numel() * 4, opts, sh)
         if rc != 0:
             raise RuntimeError(B.rmsnorm_last_error())
 
@@ -655,7 +657,7 @@ def bench_backward(args, wl):
     gbs = step_bytes * K / sec / 1e9
     return {"backward": wl.name, "value": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak, 4),
             "steps": K, "ms_per_step": round(sec * 1e3 / K, 5), "bytes_per_step": step_bytes,
-            "workspace_bytes": nbytes,
+            "workspace_bytes": nbytes, "variant": args.variant, "max_ctas": args.max_ctas,
             "l2": f"rotating pool of {pool} sets ({pool * set_bytes / 1e6:.0f} MB) > 3x L2"}
 
 

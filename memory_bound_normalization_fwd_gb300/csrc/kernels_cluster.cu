@@ -23,6 +23,7 @@
 // hardware barriers that every CTA reaches by construction (same row count,
 // same decisions).
 #include "async_copy.cuh"
+#include "cluster.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -43,36 +44,6 @@ constexpr int kMaxStages = 4;
 constexpr int kHeader = 128;     // mbarriers: one per stage, one for the weight slice
 constexpr int kAlignSlack = 128;  // room to align the dynamic shared memory base
 constexpr long long kDrainLimitNs = 1000000000LL;
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-// Cluster-wide barrier: release this CTA's prior shared-memory writes, acquire the
-// peers'. The .aligned forms need the whole warp converged, hence the __syncwarp.
-__device__ __forceinline__ void cluster_sync() {
-    __syncwarp();
-    asm volatile(
-        "barrier.cluster.arrive.release.aligned;\n\t"
-        "barrier.cluster.wait.acquire.aligned;" ::
-            : "memory");
-}
-
-// Reads a 32-bit word at the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t ld_peer_u32(uint32_t local_addr, uint32_t rank) {
-    uint32_t remote, v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-    return v;
-}
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads)
