@@ -595,20 +595,22 @@ def run_ablation(args, names):
 
 def bench_backward(args, wl):
     """Throughput of rmsnorm_bwd on the workload: algorithmic bytes per step =
-    x, dy read and dx written (6 M N) + rstd read (4 M) + w read (2 N) + dw
-    written (4 N); the dw partials in the workspace are not counted."""
+    x, dy read and dx written (3 e M N, e bytes per element) + rstd read (4 M)
+    + w read (e N) + dw written (4 N); the dw partials in the workspace are not
+    counted."""
     import torch
     from memory_bound_normalization_fwd_gb300 import binding as B
     from memory_bound_normalization_fwd_gb300 import workloads as W
     dev = torch.device("cuda", 0)
-    dcode = B.BF16 if wl.dtype == "bf16" else B.FP16
+    dcode = DCODE[wl.dtype]
+    eb = W.ELEM_BYTES[wl.dtype]
     x_bits, w_bits = W.generate(wl)
     dy_bits, _ = W.generate(W.custom(wl.M, wl.N, wl.dtype, seed=99))
     x0, dy0 = W.to_torch(x_bits, wl.dtype).to(dev), W.to_torch(dy_bits, wl.dtype).to(dev)
     w = W.to_torch(w_bits, wl.dtype).to(dev)
     r0 = torch.empty(wl.M, dtype=torch.float32, device=dev)
     B.fwd(x0, w, eps=wl.eps, offset=wl.offset, y=torch.empty_like(x0), rstd=r0)
-    set_bytes = 6 * wl.M * wl.N + 4 * wl.M
+    set_bytes = 3 * eb * wl.M * wl.N + 4 * wl.M
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     pool = max(2, -(-3 * l2 // set_bytes))
     xs = [x0.clone() for _ in range(pool)]
@@ -652,7 +654,7 @@ def bench_backward(args, wl):
         b.record(stream)
     torch.cuda.synchronize()
     sec = a.elapsed_time(b) / 1e3
-    step_bytes = 6 * wl.M * wl.N + 4 * wl.M + 2 * wl.N + 4 * wl.N
+    step_bytes = 3 * eb * wl.M * wl.N + 4 * wl.M + eb * wl.N + 4 * wl.N
     peak, _ = load_peaks()
     gbs = step_bytes * K / sec / 1e9
     return {"backward": wl.name, "value": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak, 4),
@@ -703,7 +705,7 @@ def main(argv=None):
 
     if args.backward:
         for name in ([args.workload] if args.workload else list(W.WORKLOADS)):
-            print(json.dumps(bench_backward(args, W.WORKLOADS[name])), flush=True)
+            print(json.dumps(bench_backward(args, W.get(name))), flush=True)
         return 0
 
     if args.ablation:

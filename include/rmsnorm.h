@@ -66,7 +66,7 @@ extern "C" {
 typedef enum rmsnorm_dtype {
     RMSNORM_DTYPE_BF16 = 0,
     RMSNORM_DTYPE_FP16 = 1,
-    RMSNORM_DTYPE_FP32 = 2 /* forward only; the backward takes bf16 and fp16 */
+    RMSNORM_DTYPE_FP32 = 2
 } rmsnorm_dtype_t;
 
 typedef enum rmsnorm_status {
@@ -255,7 +255,8 @@ int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void
  *   dw[j] = sum_i dy[i,j] * x[i,j] * rstd[i]                              (fp32)
  * fp32 arithmetic; dx rounded once to nearest even; dw summed per CTA over its
  * rows, then over CTAs in index order (deterministic for a fixed device).
- *   x, dy, dx  [M, N] x's dtype, contiguous; dx may equal x or dy exactly
+ *   x, dy, dx  [M, N] x's dtype (bf16, fp16 or fp32), contiguous; dx may equal
+ *              x or dy exactly
  *   w          [N]    x's dtype
  *   rstd       [M]    fp32, as written by rmsnorm_fwd
  *   dw         [N]    fp32 output (overwritten; zero when M == 0)

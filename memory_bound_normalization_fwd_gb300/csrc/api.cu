@@ -308,12 +308,14 @@ namespace {
 
 int bwd_validate(const void* x, const void* w, const float* rstd, const void* dy, void* dx,
                  float* dw, int64_t M, int64_t N, float offset, int dtype, const void* ws) {
-    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16)
-        return fail(RMSNORM_ERR_DTYPE, "the backward takes bf16 (0) or fp16 (1), not dtype %d", dtype);
+    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16 && dtype != RMSNORM_DTYPE_FP32)
+        return fail(RMSNORM_ERR_DTYPE, "dtype %d is not RMSNORM_DTYPE_BF16 (0), _FP16 (1) or _FP32 (2)",
+                    dtype);
     if (M < 0 || N <= 0)
         return fail(RMSNORM_ERR_SHAPE, "need M >= 0 and N > 0 (got M=%lld N=%lld)",
                     static_cast<long long>(M), static_cast<long long>(N));
-    if (M > 0 && (N > (int64_t(1) << 47) / M || M > (int64_t(1) << 46)))
+    const int64_t eb = elem_bytes(dtype);
+    if (M > 0 && (N > ((int64_t(1) << 48) / eb) / M || M > (int64_t(1) << 46)))
         return fail(RMSNORM_ERR_SHAPE, "x would exceed 2^48 bytes");
     if (!std::isfinite(offset)) return fail(RMSNORM_ERR_SCALAR, "offset must be finite");
     if (w == nullptr || dw == nullptr) return fail(RMSNORM_ERR_NULL, "w and dw must be non-NULL");
@@ -322,24 +324,27 @@ int bwd_validate(const void* x, const void* w, const float* rstd, const void* dy
         return fail(RMSNORM_ERR_NULL, "x, rstd, dy, dx and the workspace must be non-NULL");
     const uintptr_t a2 = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
                          reinterpret_cast<uintptr_t>(dy) | reinterpret_cast<uintptr_t>(dx);
-    if (a2 & 1u) return fail(RMSNORM_ERR_ALIGN, "x, w, dy and dx must be 2-byte aligned");
+    if (a2 & static_cast<uintptr_t>(eb - 1))
+        return fail(RMSNORM_ERR_ALIGN, "x, w, dy and dx must be aligned to the element size (%d bytes)",
+                    static_cast<int>(eb));
     if ((reinterpret_cast<uintptr_t>(rstd) | reinterpret_cast<uintptr_t>(dw)) & 3u)
         return fail(RMSNORM_ERR_ALIGN, "rstd and dw must be 4-byte aligned");
     if (reinterpret_cast<uintptr_t>(ws) & 15u)
         return fail(RMSNORM_ERR_ALIGN, "the workspace must be 16-byte aligned");
+    const int64_t wb = N * eb;
     if (M == 0) {
-        if (overlaps(dw, N * 4, w, N * 2)) return fail(RMSNORM_ERR_OVERLAP, "dw overlaps w");
+        if (overlaps(dw, N * 4, w, wb)) return fail(RMSNORM_ERR_OVERLAP, "dw overlaps w");
         return RMSNORM_OK;
     }
-    const int64_t tb = M * N * 2;
+    const int64_t tb = M * N * eb;
     if (dx != x && overlaps(dx, tb, x, tb))
         return fail(RMSNORM_ERR_OVERLAP, "dx overlaps x without being equal to it");
     if (dx != dy && overlaps(dx, tb, dy, tb))
         return fail(RMSNORM_ERR_OVERLAP, "dx overlaps dy without being equal to it");
-    if (overlaps(dx, tb, w, N * 2) || overlaps(dx, tb, rstd, M * 4) || overlaps(dx, tb, dw, N * 4))
+    if (overlaps(dx, tb, w, wb) || overlaps(dx, tb, rstd, M * 4) || overlaps(dx, tb, dw, N * 4))
         return fail(RMSNORM_ERR_OVERLAP, "dx overlaps w, rstd or dw");
     if (overlaps(dw, N * 4, x, tb) || overlaps(dw, N * 4, dy, tb) ||
-        overlaps(dw, N * 4, w, N * 2) || overlaps(dw, N * 4, rstd, M * 4))
+        overlaps(dw, N * 4, w, wb) || overlaps(dw, N * 4, rstd, M * 4))
         return fail(RMSNORM_ERR_OVERLAP, "dw overlaps an input");
     return RMSNORM_OK;
 }
@@ -368,7 +373,7 @@ extern "C" int rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype,
                                           const rmsnorm_options_t* opts, int64_t* bytes) {
     if (bytes == nullptr) return fail(RMSNORM_ERR_NULL, "bytes is NULL");
     *bytes = 0;
-    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16)
+    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16 && dtype != RMSNORM_DTYPE_FP32)
         return fail(RMSNORM_ERR_DTYPE, "dtype %d is not a rmsnorm_dtype_t", dtype);
     if (M < 0 || N <= 0) return fail(RMSNORM_ERR_SHAPE, "need M >= 0 and N > 0");
     // The larger of the two kernels' needs (vector kernel with aligned
@@ -408,8 +413,9 @@ extern "C" int rmsnorm_bwd(const void* x, const void* w, const float* rstd, cons
     if (workspace_bytes < need)
         return fail(RMSNORM_ERR_WORKSPACE, "workspace of %lld bytes, %lld needed",
                     static_cast<long long>(workspace_bytes), static_cast<long long>(need));
-    if (M > 0 && (overlaps(workspace, need, x, M * N * 2) || overlaps(workspace, need, dy, M * N * 2) ||
-                  overlaps(workspace, need, dx, M * N * 2) || overlaps(workspace, need, w, N * 2) ||
+    const int64_t tb = M * N * elem_bytes(dtype), wb = N * elem_bytes(dtype);
+    if (M > 0 && (overlaps(workspace, need, x, tb) || overlaps(workspace, need, dy, tb) ||
+                  overlaps(workspace, need, dx, tb) || overlaps(workspace, need, w, wb) ||
                   overlaps(workspace, need, rstd, M * 4) || overlaps(workspace, need, dw, N * 4)))
         return fail(RMSNORM_ERR_OVERLAP, "the workspace overlaps an argument");
     cudaError_t e = bwd_run(a, l, static_cast<float*>(workspace));

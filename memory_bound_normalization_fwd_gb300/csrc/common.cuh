@@ -165,9 +165,8 @@ __device__ __forceinline__ void weights_vec(const uint4& v, float offset, float*
 // (offset + w) of vector c kept in shared memory as VecElems floats (float4
 // reads), and the scale step with those weights.
 template <int DT>
-__device__ __forceinline__ uint4 scale_vec_smem(const uint4& v, float r, const float4* sw, int c) {
+__device__ __forceinline__ void weights_from_smem(const float4* sw, int c, float* s) {
     constexpr int kE = VecElems<DT>::value;
-    float s[kE];
 #pragma unroll
     for (int q = 0; q < kE / 4; ++q) {
         const float4 t = sw[c * (kE / 4) + q];
@@ -176,7 +175,44 @@ __device__ __forceinline__ uint4 scale_vec_smem(const uint4& v, float r, const f
         s[4 * q + 2] = t.z;
         s[4 * q + 3] = t.w;
     }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 scale_vec_smem(const uint4& v, float r, const float4* sw, int c) {
+    float s[VecElems<DT>::value];
+    weights_from_smem<DT>(sw, c, s);
     return scale_vec<DT>(v, r, s);
+}
+
+// All elements of a 16-byte vector widened to fp32, and the single rounding of
+// a vector's worth of fp32 values back to the dtype.
+template <int DT>
+__device__ __forceinline__ void unpack_vec(const uint4& v, float* f) {
+    if constexpr (DT == kFP32) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 p = Codec<DT>::unpack2(w[k]);
+            f[2 * k] = p.x;
+            f[2 * k + 1] = p.y;
+        }
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack_vec(const float* f) {
+    if constexpr (DT == kFP32) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    } else {
+        return make_uint4(Codec<DT>::pack2(f[0], f[1]), Codec<DT>::pack2(f[2], f[3]),
+                          Codec<DT>::pack2(f[4], f[5]), Codec<DT>::pack2(f[6], f[7]));
+    }
 }
 
 template <int DT>

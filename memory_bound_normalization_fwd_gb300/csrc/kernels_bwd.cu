@@ -21,23 +21,6 @@
 namespace rmsn {
 namespace {
 
-template <int DT>
-__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float2 p = Codec<DT>::unpack2(w[k]);
-        f[2 * k] = p.x;
-        f[2 * k + 1] = p.y;
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ uint4 pack8(const float* f) {
-    return make_uint4(Codec<DT>::pack2(f[0], f[1]), Codec<DT>::pack2(f[2], f[3]),
-                      Codec<DT>::pack2(f[4], f[5]), Codec<DT>::pack2(f[6], f[7]));
-}
-
 // (Loading the next row ahead, as the warp kernel does, measured slower here:
 // the extra registers cost a CTA per SM at 512 threads, and long rows already
 // keep enough bytes in flight; 16384x8192 5.50 against 5.60 TB/s.)
@@ -47,7 +30,8 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
                 const uint4* dy, uint4* dx, float* __restrict__ partial, int64_t M, int nvec,
                 float n, float offset) {
     constexpr int kWarps = THREADS / 32;
-    extern __shared__ float4 sw[];  // (offset + w) in fp32, 2 float4 per 16-byte vector
+    constexpr int E = VecElems<DT>::value;  // elements per 16-byte vector
+    extern __shared__ float4 sw[];  // (offset + w) in fp32, E / 4 float4 per 16-byte vector
     __shared__ float part[2][kWarps];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -55,18 +39,13 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 
     pdl_wait();
     pdl_launch_dependents();
-    for (int i = tid; i < nvec; i += THREADS) {
-        float q[kVecElems];
-        weights8<DT>(__ldg(w + i), offset, q);
-        sw[2 * i] = make_float4(q[0], q[1], q[2], q[3]);
-        sw[2 * i + 1] = make_float4(q[4], q[5], q[6], q[7]);
-    }
+    for (int i = tid; i < nvec; i += THREADS) weights_vec_to_smem<DT>(__ldg(w + i), offset, sw, i);
     __syncthreads();
-    float acc[V][kVecElems];
+    float acc[V][E];
 #pragma unroll
     for (int v = 0; v < V; ++v)
 #pragma unroll
-        for (int e = 0; e < kVecElems; ++e) acc[v][e] = 0.f;
+        for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
 
     int parity = 0;
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
@@ -86,13 +65,12 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
         for (int v = 0; v < V; ++v) {
             const int c = v * THREADS + tid;
             if (c >= nvec) continue;
-            float xf[kVecElems], gf[kVecElems];
-            unpack8<DT>(xv[v], xf);
-            unpack8<DT>(gv[v], gf);
-            const float4 s0 = sw[2 * c], s1 = sw[2 * c + 1];
-            const float sv[kVecElems] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            float xf[E], gf[E], sv[E];
+            unpack_vec<DT>(xv[v], xf);
+            unpack_vec<DT>(gv[v], gf);
+            weights_from_smem<DT>(sw, c, sv);
 #pragma unroll
-            for (int e = 0; e < kVecElems; ++e) cs = fmaf(gf[e] * sv[e], xf[e], cs);
+            for (int e = 0; e < E; ++e) cs = fmaf(gf[e] * sv[e], xf[e], cs);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
@@ -106,29 +84,29 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
         for (int v = 0; v < V; ++v) {
             const int c = v * THREADS + tid;
             if (c >= nvec) continue;
-            float xf[kVecElems], gf[kVecElems], o[kVecElems];
-            unpack8<DT>(xv[v], xf);
-            unpack8<DT>(gv[v], gf);
-            const float4 s0 = sw[2 * c], s1 = sw[2 * c + 1];
-            const float sv[kVecElems] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            float xf[E], gf[E], sv[E], o[E];
+            unpack_vec<DT>(xv[v], xf);
+            unpack_vec<DT>(gv[v], gf);
+            weights_from_smem<DT>(sw, c, sv);
 #pragma unroll
-            for (int e = 0; e < kVecElems; ++e) {
+            for (int e = 0; e < E; ++e) {
                 o[e] = r * (gf[e] * sv[e] - xf[e] * k);
                 acc[v][e] = fmaf(gf[e] * xf[e], r, acc[v][e]);
             }
-            st_stream(dx + row * nvec + c, pack8<DT>(o));
+            st_stream(dx + row * nvec + c, pack_vec<DT>(o));
         }
         parity ^= 1;
     }
 
-    float4* out = reinterpret_cast<float4*>(partial + static_cast<int64_t>(blockIdx.x) * nvec * 8);
+    float4* out = reinterpret_cast<float4*>(partial + static_cast<int64_t>(blockIdx.x) * nvec * E);
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = v * THREADS + tid;
-        if (c < nvec) {
-            out[2 * c] = make_float4(acc[v][0], acc[v][1], acc[v][2], acc[v][3]);
-            out[2 * c + 1] = make_float4(acc[v][4], acc[v][5], acc[v][6], acc[v][7]);
-        }
+        if (c < nvec)
+#pragma unroll
+            for (int q = 0; q < E / 4; ++q)
+                out[c * (E / 4) + q] = make_float4(acc[v][4 * q], acc[v][4 * q + 1], acc[v][4 * q + 2],
+                                                   acc[v][4 * q + 3]);
     }
 }
 
@@ -142,24 +120,20 @@ __global__ void __launch_bounds__(256)
 bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __restrict__ rstd,
                 const uint4* dy, uint4* dx, float* __restrict__ partial, int64_t M, int nvec,
                 float n, float offset) {
-    extern __shared__ float4 sw[];  // (offset + w): 2 float4 per vector; then 8 x N floats of dw
+    constexpr int E = VecElems<DT>::value;  // elements per 16-byte vector
+    extern __shared__ float4 sw[];  // (offset + w): N floats; then 8 x N floats of dw
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int wid = tid >> 5;
     pdl_wait();
     pdl_launch_dependents();
-    for (int i = tid; i < nvec; i += 256) {
-        float q[kVecElems];
-        weights8<DT>(__ldg(w + i), offset, q);
-        sw[2 * i] = make_float4(q[0], q[1], q[2], q[3]);
-        sw[2 * i + 1] = make_float4(q[4], q[5], q[6], q[7]);
-    }
+    for (int i = tid; i < nvec; i += 256) weights_vec_to_smem<DT>(__ldg(w + i), offset, sw, i);
     __syncthreads();
-    float acc[V][kVecElems];
+    float acc[V][E];
 #pragma unroll
     for (int v = 0; v < V; ++v)
 #pragma unroll
-        for (int e = 0; e < kVecElems; ++e) acc[v][e] = 0.f;
+        for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
 
     // Each warp walks its rows with the next row's x, dy and rstd loaded before
     // the current row is reduced (one row in flight ahead: measured 3.84 TB/s
@@ -190,13 +164,12 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
         for (int v = 0; v < V; ++v) {
             const int c = v * 32 + lane;
             if (c >= nvec) continue;
-            float xf[kVecElems], gf[kVecElems];
-            unpack8<DT>(xv[v], xf);
-            unpack8<DT>(gv[v], gf);
-            const float4 s0 = sw[2 * c], s1 = sw[2 * c + 1];
-            const float sv[kVecElems] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            float xf[E], gf[E], sv[E];
+            unpack_vec<DT>(xv[v], xf);
+            unpack_vec<DT>(gv[v], gf);
+            weights_from_smem<DT>(sw, c, sv);
 #pragma unroll
-            for (int e = 0; e < kVecElems; ++e) cs = fmaf(gf[e] * sv[e], xf[e], cs);
+            for (int e = 0; e < E; ++e) cs = fmaf(gf[e] * sv[e], xf[e], cs);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
@@ -205,31 +178,30 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
         for (int v = 0; v < V; ++v) {
             const int c = v * 32 + lane;
             if (c >= nvec) continue;
-            float xf[kVecElems], gf[kVecElems], o[kVecElems];
-            unpack8<DT>(xv[v], xf);
-            unpack8<DT>(gv[v], gf);
-            const float4 s0 = sw[2 * c], s1 = sw[2 * c + 1];
-            const float sv[kVecElems] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            float xf[E], gf[E], sv[E], o[E];
+            unpack_vec<DT>(xv[v], xf);
+            unpack_vec<DT>(gv[v], gf);
+            weights_from_smem<DT>(sw, c, sv);
 #pragma unroll
-            for (int e = 0; e < kVecElems; ++e) {
+            for (int e = 0; e < E; ++e) {
                 o[e] = r * (gf[e] * sv[e] - xf[e] * k);
                 acc[v][e] = fmaf(gf[e] * xf[e], r, acc[v][e]);
             }
-            st_stream(dx + row * nvec + c, pack8<DT>(o));
+            st_stream(dx + row * nvec + c, pack_vec<DT>(o));
         }
 #pragma unroll
         for (int v = 0; v < V; ++v) xv[v] = xn[v], gv[v] = gn[v];
         r = rn;
     }
 
-    float* red = reinterpret_cast<float*>(sw + 2 * nvec);  // [8][nvec * 8]
-    const int N8 = nvec * kVecElems;
+    float* red = reinterpret_cast<float*>(sw + nvec * (E / 4));  // [8][N]
+    const int N8 = nvec * E;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int c = v * 32 + lane;
         if (c < nvec)
 #pragma unroll
-            for (int e = 0; e < kVecElems; ++e) red[wid * N8 + c * kVecElems + e] = acc[v][e];
+            for (int e = 0; e < E; ++e) red[wid * N8 + c * E + e] = acc[v][e];
     }
     __syncthreads();
     for (int j = tid; j < N8; j += 256) {
@@ -243,9 +215,15 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 // General backward: any N and 2-byte alignment. dw partial in shared memory (N floats).
 template <int DT, int THREADS>
 __global__ void __launch_bounds__(THREADS)
-bwd_generic_kernel(const uint16_t* x, const uint16_t* __restrict__ w,
-                   const float* __restrict__ rstd, const uint16_t* dy, uint16_t* dx,
+bwd_generic_kernel(const void* xv, const void* __restrict__ wv,
+                   const float* __restrict__ rstd, const void* dyv, void* dxv,
                    float* __restrict__ partial, int64_t M, int64_t N, float n, float offset) {
+    using E = Elem<DT>;
+    using T = typename E::T;
+    const T* x = static_cast<const T*>(xv);
+    const T* __restrict__ w = static_cast<const T*>(wv);
+    const T* dy = static_cast<const T*>(dyv);
+    T* dx = static_cast<T*>(dxv);
     constexpr int kWarps = THREADS / 32;
     extern __shared__ float sacc[];
     __shared__ float part[2][kWarps];
@@ -255,13 +233,13 @@ bwd_generic_kernel(const uint16_t* x, const uint16_t* __restrict__ w,
     for (int64_t j = tid; j < N; j += THREADS) sacc[j] = 0.f;
     int parity = 0;
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
-        const uint16_t* xr = x + row * N;
-        const uint16_t* gr = dy + row * N;
+        const T* xr = x + row * N;
+        const T* gr = dy + row * N;
         const float r = __ldg(rstd + row);
         float cs = 0.f;
         for (int64_t j = tid; j < N; j += THREADS) {
-            const float sj = offset + Codec<DT>::unpack1(__ldg(w + j));
-            cs = fmaf(Codec<DT>::unpack1(gr[j]) * sj, Codec<DT>::unpack1(xr[j]), cs);
+            const float sj = offset + E::load(__ldg(w + j));
+            cs = fmaf(E::load(gr[j]) * sj, E::load(xr[j]), cs);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
@@ -271,11 +249,11 @@ bwd_generic_kernel(const uint16_t* x, const uint16_t* __restrict__ w,
 #pragma unroll
         for (int q = 0; q < kWarps; ++q) c_row += part[parity][q];
         const float k = (r * r) * c_row / n;
-        uint16_t* dr = dx + row * N;
+        T* dr = dx + row * N;
         for (int64_t j = tid; j < N; j += THREADS) {
-            const float sj = offset + Codec<DT>::unpack1(__ldg(w + j));
-            const float xf = Codec<DT>::unpack1(xr[j]), gf = Codec<DT>::unpack1(gr[j]);
-            dr[j] = Codec<DT>::pack1(r * (gf * sj - xf * k));
+            const float sj = offset + E::load(__ldg(w + j));
+            const float xf = E::load(xr[j]), gf = E::load(gr[j]);
+            dr[j] = E::store(r * (gf * sj - xf * k));
             sacc[j] = fmaf(gf * xf, r, sacc[j]);
         }
         parity ^= 1;
@@ -320,8 +298,8 @@ dw_reduce_kernel(const float* __restrict__ partial, float* __restrict__ dw, int 
 
 using VecFn = void (*)(const uint4*, const uint4*, const float*, const uint4*, uint4*, float*,
                        int64_t, int, float, float);
-using GenFn = void (*)(const uint16_t*, const uint16_t*, const float*, const uint16_t*,
-                       uint16_t*, float*, int64_t, int64_t, float, float);
+using GenFn = void (*)(const void*, const void*, const float*, const void*, void*, float*,
+                       int64_t, int64_t, float, float);
 
 template <int DT>
 VecFn pick_vec(int T, int V) {
@@ -349,21 +327,24 @@ GenFn pick_gen(int T) {
 }  // namespace
 
 bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int variant, Launch& l) {
-    const int64_t nvec = a.N / kVecElems;
-    const bool vec = a.N % kVecElems == 0 && aligned16(a.x) && aligned16(a.w) &&
+    const int64_t e = vec_elems(a.dtype);
+    const int64_t nvec = a.N / e;
+    const bool vec = a.N % e == 0 && aligned16(a.x) && aligned16(a.w) &&
                      aligned16(a.dy) && aligned16(a.dx);
     if ((variant == 0 || variant == 1) && vec && nvec <= 128) {
         const int V = nvec <= 32 ? 1 : nvec <= 64 ? 2 : 4;
         VecFn fn = nullptr;
         if (a.dtype == kBF16)
             fn = V == 1 ? bwd_warp_kernel<kBF16, 1> : V == 2 ? bwd_warp_kernel<kBF16, 2> : bwd_warp_kernel<kBF16, 4>;
-        else
+        else if (a.dtype == kFP16)
             fn = V == 1 ? bwd_warp_kernel<kFP16, 1> : V == 2 ? bwd_warp_kernel<kFP16, 2> : bwd_warp_kernel<kFP16, 4>;
+        else
+            fn = V == 1 ? bwd_warp_kernel<kFP32, 1> : V == 2 ? bwd_warp_kernel<kFP32, 2> : bwd_warp_kernel<kFP32, 4>;
         l.kernel = reinterpret_cast<const void*>(fn);
         l.threads = 256;
         l.lanes_per_row = 32;
         l.vecs_per_lane = V;
-        l.smem = static_cast<int>(nvec * 32 + 8 * nvec * kVecElems * 4);
+        l.smem = static_cast<int>(a.N * 4 + 8 * a.N * 4);  // (offset + w), then 8 warps' dw
         l.ctas_per_sm = occupancy(l.kernel, 256, l.smem);
         l.grid = persistent_grid(a.M > 0 ? a.M : 1, 8, d.sm_count, l.ctas_per_sm, k.max_ctas);
         l.work_items = a.M;
@@ -378,8 +359,10 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
         }
         int V = 1;
         while (static_cast<int64_t>(V) * T < nvec) V <<= 1;
-        VecFn fn = a.dtype == kBF16 ? pick_vec<kBF16>(T, V) : pick_vec<kFP16>(T, V);
-        const int smem = static_cast<int>(nvec * 32);
+        VecFn fn = a.dtype == kBF16   ? pick_vec<kBF16>(T, V)
+                   : a.dtype == kFP16 ? pick_vec<kFP16>(T, V)
+                                      : pick_vec<kFP32>(T, V);
+        const int smem = static_cast<int>(a.N * 4);  // (offset + w) in fp32
         if (fn && smem > 48 * 1024 &&
             cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -401,7 +384,9 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
     // General kernel: dw partial for the whole row in shared memory.
     if (a.N * 4 > d.max_smem_optin - 1024) return false;
     int T = k.lanes_per_row > 0 ? k.lanes_per_row : (a.N >= 4096 ? 1024 : a.N >= 512 ? 256 : 64);
-    GenFn fn = a.dtype == kBF16 ? pick_gen<kBF16>(T) : pick_gen<kFP16>(T);
+    GenFn fn = a.dtype == kBF16   ? pick_gen<kBF16>(T)
+               : a.dtype == kFP16 ? pick_gen<kFP16>(T)
+                                  : pick_gen<kFP32>(T);
     if (!fn) return false;
     const int smem = static_cast<int>(a.N * 4);
     if (smem > 48 * 1024 &&
@@ -429,13 +414,11 @@ cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial) {
             e = cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                                    static_cast<const uint4*>(a.w), a.rstd,
                                    static_cast<const uint4*>(a.dy), static_cast<uint4*>(a.dx),
-                                   partial, a.M, static_cast<int>(a.N / kVecElems),
+                                   partial, a.M, static_cast<int>(a.N / vec_elems(a.dtype)),
                                    static_cast<float>(a.N), a.offset);
         } else {
             GenFn fn = reinterpret_cast<GenFn>(const_cast<void*>(l.kernel));
-            e = cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint16_t*>(a.x),
-                                   static_cast<const uint16_t*>(a.w), a.rstd,
-                                   static_cast<const uint16_t*>(a.dy), static_cast<uint16_t*>(a.dx),
+            e = cudaLaunchKernelEx(&c.cfg, fn, a.x, a.w, a.rstd, a.dy, a.dx,
                                    partial, a.M, a.N, static_cast<float>(a.N), a.offset);
         }
         if (e != cudaSuccess) return e;

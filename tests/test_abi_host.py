@@ -111,11 +111,15 @@ def test_fp32_validation_uses_four_byte_elements(lib, kw, code):
     assert B.rmsnorm_last_error() != ""
 
 
-def test_backward_rejects_fp32(lib):
-    assert B.rmsnorm_bwd(X, W_, R, 0x60000000, Y, 0x70000000, 4, 8, 0.0, 2, 0x50000000, 1 << 20,
+def test_backward_fp32_checks_four_byte_elements(lib):
+    call = lambda **k: B.rmsnorm_bwd(k.get("x", X), W_, R, k.get("dy", 0x60000000), k.get("dx", Y),
+                                     0x70000000, 4, 8, 0.0, 2, 0x50000000, 1 << 20, None, 0)
+    assert call(x=X + 2) == -10            # 2-byte aligned is not enough for fp32
+    assert call(dx=X + 4 * 8 * 4 - 4) == -5  # dx starts on x's last 4-byte element
+    assert call(dx=Y, dy=Y + 64) == -5       # dy inside dx (4 x 8 x 4 bytes)
+    assert call(x=X, dy=0x7) == -10
+    assert B.rmsnorm_bwd(X, W_, R, 0x60000000, Y, 0x70000000, 4, 8, 0.0, 3, 0x50000000, 1 << 20,
                          None, 0) == -3
-    with pytest.raises(B.RMSNormError):
-        B.rmsnorm_bwd_workspace_size(4, 8, 2)
 
 
 def test_m_zero_is_ok_without_buffers(lib):

@@ -2,7 +2,7 @@
 same seeded inputs and the same fp32 rstd (the oracle forward's, rounded to
 fp32: the value a forward keeps for the backward).
 
-Tolerance, derived from the arithmetic: dx = r (dy s - x r^2 c / N) is a
+bf16, fp16 and fp32 inputs. Tolerance, derived from the arithmetic: dx = r (dy s - x r^2 c / N) is a
 difference of two fp32 terms, each with relative error of a few 1e-7 (c is a
 fp32 sum over the row), so |dx_gpu - dx| <= 1 ulp(dx) + 1e-5 * r (|dy s| +
 |x| r^2 sum|dy s x| / N); dw is an fp32 sum over rows (per CTA, then over
@@ -20,11 +20,11 @@ from memory_bound_normalization_fwd_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 TAU = 1e-5
-DT = {"bf16": B.BF16, "fp16": B.FP16}
+DT = {"bf16": B.BF16, "fp16": B.FP16, "fp32": B.FP32}
 
 
 def _ulp(dtype, v):
-    mbits, emin = (7, -126) if dtype == "bf16" else (10, -14)
+    mbits, emin = {"bf16": (7, -126), "fp16": (10, -14), "fp32": (23, -126)}[dtype]
     e = np.floor(np.log2(np.maximum(np.abs(v), 1e-300)))
     return np.exp2(np.maximum(e, emin) - mbits)
 
@@ -76,7 +76,7 @@ SHAPES = [(1, 8), (37, 512), (300, 1000), (64, 4096), (33, 8192), (17, 16384), (
           (5, 20000), (130, 520)]
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("M,N", SHAPES)
 @pytest.mark.parametrize("variant", ["auto", "warp", "cta", "generic"])
 def test_bwd_parity(dtype, M, N, variant):
@@ -91,7 +91,10 @@ def test_bwd_parity(dtype, M, N, variant):
         try:
             dx, dw = _run(x, w, dy, rstd, offset, dtype, variant=variant, max_ctas=max_ctas)
         except AssertionError:
-            if (variant == "cta" and (N % 8 or N > 16384)) or (variant == "warp" and (N % 8 or N > 1024)):
+            e = 4 if dtype == "fp32" else 8   # elements per 16-byte vector
+            nvec = N // e                      # vector kernels: up to 2048 (CTA), 128 (warp)
+            if (variant == "cta" and (N % e or nvec > 2048)) or \
+                    (variant == "warp" and (N % e or nvec > 128)):
                 pytest.skip("vector kernel does not take this shape")
             raise
         _check(x, w, dy, rstd, dx, dw, offset, dtype, where=f"{variant} {M}x{N} {max_ctas}")
@@ -141,6 +144,14 @@ def test_bwd_rejects_a_small_workspace():
                        dwd.data_ptr(), M, N, 0.0, B.BF16, ws.data_ptr(), 16, None,
                        torch.cuda.current_stream().cuda_stream)
     assert rc == -11
+
+
+def test_fp32_full_size_and_in_place():
+    x, w, dy, rstd = _inputs(32768, 1000, "fp32", seed=21, offset=1.0)
+    dx, dw = _run(x, w, dy, rstd, 1.0, "fp32")
+    _check(x, w, dy, rstd, dx, dw, 1.0, "fp32", where="fp32 32768x1000")
+    dx2, dw2 = _run(x, w, dy, rstd, 1.0, "fp32", inplace="dy")
+    assert np.array_equal(dx, dx2) and np.array_equal(dw, dw2)
 
 
 def test_torch_convenience_forward_then_backward():

@@ -19,7 +19,7 @@ from memory_bound_normalization_fwd_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 TAU = 1e-5  # the backward tests' relative bound on an fp32 dw sum (see test_bwd_gpu.py)
-DT = {"bf16": B.BF16, "fp16": B.FP16}
+DT = {"bf16": B.BF16, "fp16": B.FP16, "fp32": B.FP32}
 
 
 def _inputs(M, N, dtype, seed):
@@ -57,11 +57,12 @@ def _no_alloc(xd, wd, rd, gd, offset, dtype):
 
 def _ordinal(t):
     b = W.from_torch(t).astype(np.int64)
-    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+    sign = 0x80000000 if t.dtype == torch.float32 else 0x8000
+    return np.where(b & sign, -(b & (sign - 1)), b)
 
 
 @pytest.mark.parametrize("M,N,dtype", [(20000, 8192, "bf16"), (777, 512, "fp16"),
-                                       (50, 777, "bf16"), (3, 16384, "fp16")])
+                                       (50, 777, "bf16"), (3, 16384, "fp16"), (4000, 1000, "fp32")])
 def test_no_alloc_backward_matches_the_workspace_backward(M, N, dtype):
     for call, seed in enumerate((11, 12)):  # two calls in a row, different inputs
         xd, wd, gd, rd = _inputs(M, N, dtype, seed + N)
