@@ -1,6 +1,7 @@
-// General variant: any N, any element alignment (2 bytes; 4 for fp32). One CTA per row, persistent.
-// Pass 1 reads the row element by element (consecutive threads on consecutive
-// elements, so each warp access is one contiguous 64-byte span) and sums the
+// General variant: any N, any element alignment (2 bytes; 4 for fp32). One CTA
+// per row, persistent. Pass 1 reads the row element by element (consecutive
+// threads on consecutive elements, so each warp access is one contiguous span
+// of 64 bytes, or 128 for fp32) and sums the
 // squares in fp32; a warp butterfly plus a shared-memory step gives the row
 // sum. Pass 2 re-reads the row (now in L1/L2) and writes y.
 //

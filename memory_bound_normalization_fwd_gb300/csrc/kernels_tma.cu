@@ -1,7 +1,8 @@
 // TMA-staged variant: rows reach shared memory through bulk asynchronous copies
 // (cp.async.bulk, completion counted on an mbarrier), in a ring of S stages of
-// R consecutive rows each; a stage of R rows is one contiguous span of x, so it
-// is a single copy. One thread issues the copies; all threads consume.
+// R consecutive rows each; for packed rows a stage is one contiguous span of x,
+// so it is a single copy (strided rows take one copy each, counted on the same
+// mbarrier). One thread issues the copies; all threads consume.
 //
 // This is the CTA-per-row design for large hidden sizes that stages rows
 // through shared memory instead of holding them in registers, so the bytes in
