@@ -554,6 +554,8 @@ def ablation_configs(wl):
             if S * R * row <= 200 * 1024:
                 for early in (False, True):
                     cfgs.append(dict(variant="tma", rows_per_stage=R, stages=S, early_loads=early))
+    for early in (False, True):  # TMA stores: y leaves by cp.async.bulk from the stage
+        cfgs.append(dict(variant="tma", bulk_store=True, early_loads=early))
     if nvec >= 512:
         for C in (2, 4):
             cfgs.append(dict(variant="cluster", cluster_size=C, early_loads=True))

@@ -128,6 +128,10 @@ typedef enum rmsnorm_variant {
  * the critical path of a chain of dependent kernels. Ignored with
  * RMSNORM_FLAG_NO_PDL and by the general kernel; implied by EARLY_LOADS. */
 #define RMSNORM_FLAG_EARLY_WEIGHTS 16
+/* TMA variant with packed rows: y is written into the shared-memory stage and
+ * leaves with one bulk copy (cp.async.bulk shared -> global) per stage instead
+ * of per-thread stores. Ignored by the other variants and for strided rows. */
+#define RMSNORM_FLAG_BULK_STORE 32
 /* rmsnorm_fwd_host only: no ring and no copies; the kernel reads x and writes
  * y and rstd in page-locked host memory through their device addresses (the
  * GPU's own loads and stores cross the host link). Needs every host buffer to

@@ -124,17 +124,18 @@ FLAG_BLOCKED_ROWS = 2
 FLAG_EARLY_LOADS = 4
 FLAG_HOST_DIRECT = 8
 FLAG_EARLY_WEIGHTS = 16
+FLAG_BULK_STORE = 32
 
 
 def make_options(variant: str | int = "auto", max_ctas: int = 0, lanes_per_row: int = 0,
                  stages: int = 0, rows_per_stage: int = 0, wait_limit_ns: int = 0,
                  pdl: bool = True, blocked: bool = False, early_loads: bool = False,
                  cluster_size: int = 0, host_direct: bool = False,
-                 early_weights: bool = False) -> Options:
+                 early_weights: bool = False, bulk_store: bool = False) -> Options:
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     flags = ((0 if pdl else FLAG_NO_PDL) | (FLAG_BLOCKED_ROWS if blocked else 0)
              | (FLAG_EARLY_LOADS if early_loads else 0) | (FLAG_HOST_DIRECT if host_direct else 0)
-             | (FLAG_EARLY_WEIGHTS if early_weights else 0))
+             | (FLAG_EARLY_WEIGHTS if early_weights else 0) | (FLAG_BULK_STORE if bulk_store else 0))
     return Options(ctypes.sizeof(Options), v, max_ctas, lanes_per_row, stages, rows_per_stage,
                    flags, cluster_size, wait_limit_ns)
 

@@ -120,7 +120,8 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
     if (o->max_ctas < 0 || o->lanes_per_row < 0 || o->rows_per_stage < 0 || o->stages < 0 ||
         o->stages > 8 || o->wait_limit_ns < 0 || o->cluster_size < 0 || o->cluster_size > 16 ||
         (o->flags & ~(RMSNORM_FLAG_NO_PDL | RMSNORM_FLAG_BLOCKED_ROWS | RMSNORM_FLAG_EARLY_LOADS |
-                      RMSNORM_FLAG_HOST_DIRECT | RMSNORM_FLAG_EARLY_WEIGHTS)) != 0)
+                      RMSNORM_FLAG_HOST_DIRECT | RMSNORM_FLAG_EARLY_WEIGHTS |
+                      RMSNORM_FLAG_BULK_STORE)) != 0)
         return fail(RMSNORM_ERR_OPTIONS, "options fields out of range");
     *variant = o->variant;
     k->flags = o->flags;

@@ -35,6 +35,43 @@ static __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, u
         : "memory");
 }
 
+// Orders this thread's earlier generic-proxy writes to shared memory before later
+// async-proxy (bulk copy) reads of them; each writing thread runs it before the
+// barrier that precedes the copy.
+static __device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared -> global bulk copy, tracked in the issuing thread's bulk async-groups.
+// Both addresses 16-byte aligned, `bytes` a multiple of 16.
+static __device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+
+static __device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Returns once every bulk group this thread committed has finished reading its
+// shared-memory source (the buffer may then be overwritten).
+static __device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Returns once at most the newest of this thread's committed bulk groups may
+// still be reading its shared-memory source.
+static __device__ __forceinline__ void bulk_wait_read_all_but_newest() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// Returns once every bulk group this thread committed has completed (its global
+// writes are done).
+static __device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 static __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(

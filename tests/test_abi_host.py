@@ -130,7 +130,7 @@ def test_m_zero_is_ok_without_buffers(lib):
 @pytest.mark.parametrize("field,value", [("variant", 6), ("variant", -1), ("max_ctas", -1),
                                          ("stages", 9), ("stages", -1), ("wait_limit_ns", -5),
                                          ("lanes_per_row", -2), ("struct_size", 8),
-                                         ("flags", 32), ("cluster_size", 17),
+                                         ("flags", 64), ("cluster_size", 17),
                                          ("cluster_size", -1)])
 def test_bad_options(lib, field, value):
     o = B.make_options()

@@ -158,6 +158,16 @@ def test_rstd_null_and_torch_convenience(variant, N):
     assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
 
 
+@pytest.mark.parametrize("N", [256, 1000, 4096])
+def test_tma_bulk_store(N):
+    wl = W.custom(700, N, "fp32", seed=N + 900)
+    x, w = W.generate(wl)
+    for early in (False, True):
+        _check(x, w, wl.eps, wl.offset, variant="tma", bulk_store=True, early_loads=early,
+               runs=2 if early else 1)
+    _check(x, w, wl.eps, wl.offset, inplace=True, variant="tma", bulk_store=True)
+
+
 def test_zero_rows_and_eps_zero_give_nan():
     wl = W.custom(64, 512, "fp32", seed=800)
     x, w = W.generate(wl)

@@ -247,6 +247,68 @@ def test_tma_bounded_wait_reports_timeout_and_recovers():
     compare(y, r, yo, ro, "bf16")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("N", [512, 1000, 4096, 8192])
+@pytest.mark.parametrize("early", [False, True], ids=["strict", "early_loads"])
+def test_tma_bulk_store(dtype, N, early):
+    # y written into the shared-memory stage and copied out by cp.async.bulk:
+    # same bits as per-thread stores, any grid, in place too.
+    wl = W.custom(611, N, dtype, seed=N + 7, offset=float(early))
+    x, w = W.generate(wl)
+    for max_ctas in (0, 5):
+        _run_and_check(x, w, dtype, wl.eps, wl.offset, variant="tma", bulk_store=True,
+                       early_loads=early, max_ctas=max_ctas, expect_variant="tma")
+    _run_and_check(x, w, dtype, wl.eps, wl.offset, inplace=True, variant="tma", bulk_store=True)
+    a = DeviceCase(x, w, dtype)
+    b = DeviceCase(x, w, dtype)
+    assert a.run(wl.eps, wl.offset, variant="tma") == 0
+    assert b.run(wl.eps, wl.offset, variant="tma", bulk_store=True) == 0
+    ya, ra = a.results()
+    yb, rb = b.results()
+    assert np.array_equal(ya, yb) and np.array_equal(ra, rb)
+
+
+@pytest.mark.parametrize("N", [1000, 8192])
+def test_tma_bulk_store_chained_calls_and_timeout(N):
+    # Each call reads the previous call's output: the bulk stores must have
+    # completed before the next kernel reads y as its x.
+    M = 3000
+    wl = W.custom(M, N, "bf16", seed=N + 29)
+    x, w = W.generate(wl)
+    w_dev = W.to_torch(w, "bf16").cuda()
+
+    def chain(sync: bool):
+        a = W.to_torch(x, "bf16").cuda()
+        b = torch.empty_like(a)
+        r = torch.empty(M, dtype=torch.float32, device="cuda")
+        for _ in range(8):
+            _raw_call(a, w_dev, b, r, M, N, 1e-6, 0.0, variant="tma", bulk_store=True)
+            if sync:
+                torch.cuda.synchronize()
+            _raw_call(b, w_dev, a, r, M, N, 1e-6, 0.0, variant="tma", bulk_store=True)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return W.from_torch(a), r.cpu().numpy()
+
+    ya, ra = chain(False)
+    yb, rb = chain(True)
+    assert np.array_equal(ya, yb) and np.array_equal(ra, rb)
+    # A wait that gives up: the CTA stops, waits for its bulk stores and loads,
+    # and the next normal call is exact.
+    case = DeviceCase(x, w, "bf16")
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.rmsnorm_check_device_status(s) == 0
+    assert case.run(wl.eps, wl.offset, variant="tma", bulk_store=True, wait_limit_ns=1) == 0
+    assert B.rmsnorm_check_device_status(s) in (0, -7)
+    case.check_guards()
+    assert case.run(wl.eps, wl.offset, variant="tma", bulk_store=True) == 0
+    assert B.rmsnorm_check_device_status(s) == 0
+    y, r = case.results()
+    yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "bf16")
+    compare(y, r, yo, ro, "bf16")
+
+
 def test_results_are_deterministic():
     wl = W.WORKLOADS["rmsnorm_16384x512_bf16"]
     x, w = W.generate(wl)
