@@ -75,6 +75,7 @@ typedef enum rmsnorm_status {
     RMSNORM_ERR_SHAPE = -2,          /* M < 0, N <= 0, or x larger than 2^48 bytes */
     RMSNORM_ERR_DTYPE = -3,          /* dtype is not an rmsnorm_dtype_t value */
     RMSNORM_ERR_SCALAR = -4,         /* eps negative or not finite, or offset not finite */
+    RMSNORM_ERR_EPS = -4,            /* the same code under the name of the eps check */
     RMSNORM_ERR_OVERLAP = -5,        /* buffers overlap other than y == x exactly */
     RMSNORM_ERR_CUDA = -6,           /* a CUDA runtime call or launch failed */
     RMSNORM_ERR_DEVICE_TIMEOUT = -7, /* a kernel's bounded wait ran out (see rmsnorm_check_device_status) */

@@ -309,6 +309,49 @@ def test_tma_bulk_store_chained_calls_and_timeout(N):
     compare(y, r, yo, ro, "bf16")
 
 
+@pytest.mark.parametrize("variant,N", [("warp", 512), ("tma", 1000), ("cta", 16384),
+                                       ("cluster", 65536), ("generic", 777)])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_power_of_two_scale_invariance_on_gpu(variant, N, dtype):
+    # eps = 0: y(2^k x) is y(x) within 1 ulp (the oracle's is exact), and
+    # rstd(2^k x) is rstd(x) / 2^k within the rstd tolerance.
+    M = 64 if N < 65536 else 8
+    rng = np.random.default_rng(N)
+    mag = rng.uniform(0.5, 2.0, (M, N)) * rng.choice([-1.0, 1.0], (M, N))
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    x = W.from_torch(torch.from_numpy(mag).to(tdt))
+    w = W.from_torch(torch.from_numpy(rng.uniform(0.5, 1.5, N)).to(tdt))
+    outs = []
+    for k in (0, 3, -2):
+        xs = W.from_torch(W.to_torch(x, dtype).to(torch.float64).mul(2.0 ** k).to(tdt))
+        case = DeviceCase(xs, w, dtype)
+        assert case.run(0.0, 0.0, variant=variant) == 0, B.rmsnorm_last_error()
+        y, r = case.results()
+        outs.append((k, y, r))
+    _, y0, r0 = outs[0]
+    for k, y, r in outs[1:]:
+        compare(y, r * 2.0 ** k, y0, r0.astype(np.float64), dtype, where=f"2^{k} x")
+
+
+@pytest.mark.parametrize("variant,N", [("warp", 512), ("tma", 4096), ("cta", 16384),
+                                       ("generic", 100)])
+def test_gemma_identity_on_gpu(variant, N):
+    # offset 1 with w = 0 equals offset 0 with w = 1: (offset + w) is 1 either way.
+    wl = W.custom(128, N, "bf16", seed=N + 41)
+    x, _ = W.generate(wl)
+    zeros = W.from_torch(torch.zeros(N, dtype=torch.bfloat16))
+    ones = W.from_torch(torch.ones(N, dtype=torch.bfloat16))
+    a = DeviceCase(x, zeros, "bf16")
+    b = DeviceCase(x, ones, "bf16")
+    assert a.run(1e-6, 1.0, variant=variant) == 0
+    assert b.run(1e-6, 0.0, variant=variant) == 0
+    ya, ra = a.results()
+    yb, rb = b.results()
+    assert np.array_equal(ya, yb) and np.array_equal(ra, rb)
+    yo, ro = oracle.rmsnorm_fwd(x, ones, 1e-6, 0.0, "bf16")
+    compare(ya, ra, yo, ro, "bf16")
+
+
 def test_results_are_deterministic():
     wl = W.WORKLOADS["rmsnorm_16384x512_bf16"]
     x, w = W.generate(wl)
