@@ -282,6 +282,51 @@ class PoolBench:
             f" + {rem} direct calls" if rem else "")
         return max_over_ranks(ms / 1e3), ms / 1e3 / K, (sampler.summary() if sampler else None), launch
 
+    def trials(self, opts, n_trials: int = 20, min_ms: float = 2.0):
+        """GB/s of `n_trials` separately timed windows (each at least `min_ms` of
+        graph replays, CUDA events around each window), after the main timed
+        region: (median, min, max, steps per window)."""
+        import statistics as st
+        import torch
+        from memory_bound_normalization_fwd_gb300 import binding as B
+        wl, stream, sh = self.wl, self.stream, self.stream.cuda_stream
+
+        def step(k: int):
+            i = k % self.pool
+            rc = B.rmsnorm_fwd_ex(self.xs[i].data_ptr(), self.w_dev.data_ptr(), self.ys[i].data_ptr(),
+                                  self.rs[i].data_ptr(), wl.M, wl.N, wl.eps, wl.offset, self.dcode,
+                                  opts, sh)
+            if rc != 0:
+                raise RuntimeError(B.rmsnorm_last_error())
+        per_graph = self.pool * max(1, 384 // self.pool)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for k in range(per_graph):
+                step(k)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        # replays per window: enough for min_ms, from a timed probe replay
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        reps = max(1, int(min_ms / max(a.elapsed_time(b), 1e-3)) + 1)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_trials + 1)]
+        with torch.cuda.stream(stream):
+            evs[0].record(stream)
+            for t in range(n_trials):
+                for _ in range(reps):
+                    graph.replay()
+                evs[t + 1].record(stream)
+        torch.cuda.synchronize()
+        steps = reps * per_graph
+        gbs = [wl.algorithmic_bytes * steps / (evs[t].elapsed_time(evs[t + 1]) / 1e3) / 1e9
+               for t in range(n_trials)]
+        return st.median(gbs), min(gbs), max(gbs), steps
+
     def timed(self, opts, K: int, Wm: int, clock_gpu=None):
         """(max-over-ranks seconds, seconds per step, clocks, launch text) for K steps."""
         from memory_bound_normalization_fwd_gb300 import binding as B
@@ -409,6 +454,9 @@ def bench_ours(args, wl, rank, world, local_rank):
                   "note": "no RMSNORM_FLAG_EARLY_LOADS: each launch reads x only after the "
                           "previous step completes; early_weights: the same with "
                           "RMSNORM_FLAG_EARLY_WEIGHTS (w read before the wait, x after)"}
+    # Twenty separately timed windows of the headline configuration (after the
+    # timed region above, which alone gives `value`): median, min, max.
+    t_med, t_min, t_max, t_steps = pb.trials(make_opts(early))
     opts = make_opts(False)  # the end-to-end leg keeps strict order (copies precede each call)
 
     # End to end through the public host-buffer call: per step, rmsnorm_fwd_host
@@ -519,6 +567,9 @@ def bench_ours(args, wl, rank, world, local_rank):
                 "serial_one_stream": round(whole_job_gbs(wl.algorithmic_bytes, Ke, world,
                                                          serial_s), 2),
                 "host_direct": round(whole_job_gbs(wl.algorithmic_bytes, Ke, world, direct_s), 2)},
+        "trials": {"n": 20, "steps_each": t_steps, "median": round(t_med, 2), "min": round(t_min, 2),
+                   "max": round(t_max, 2), "unit": "GB/s",
+                   "note": "separately timed windows after the timed region; value is the timed region"},
         "gpu_launches": K,
         "clocks": clocks,
     }
