@@ -392,10 +392,19 @@ def cpu_baseline(x, w, wl, repeats: int = 3):
     cores = os.cpu_count() or 1
     secs = [run_oracle_threaded(x, w, wl, wl.M, cores) for _ in range(repeats)]
     t = statistics.median(secs)
+    # One thread, on a row sample of about a tenth of a second of work.
+    probe = min(wl.M, max(1, 256 * 512 // wl.N))
+    t1 = run_oracle_threaded(x, w, wl, probe, 1)
+    rows1 = int(min(wl.M, max(probe, probe * 0.1 / max(t1, 1e-6))))
+    t1 = statistics.median(run_oracle_threaded(x, w, wl, rows1, 1) for _ in range(repeats))
+    eb = 4 if wl.dtype == "fp32" else 2
+    bytes1 = 2 * eb * rows1 * wl.N + eb * wl.N + 4 * rows1
     return {"value": round(wl.algorithmic_bytes / t / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
+            "single_thread": round(bytes1 / t1 / 1e9, 4),
             "sample": f"whole {wl.M}x{wl.N} {wl.dtype} batch, {repeats} runs, median "
-                      f"({t:.3f} s each, fp64 C oracle, {cores} threads over row blocks)"}
+                      f"({t:.3f} s each, fp64 C oracle, {cores} threads over row blocks); "
+                      f"single_thread: {rows1} rows on one thread, median of {repeats}"}
 
 
 # ---------------------------------------------------------------- our arm
