@@ -539,6 +539,13 @@ def bench_ours(args, wl, rank, world, local_rank):
     direct_s = time_steps(direct_step, Ke)
     if not agree(W.from_torch(y_pin), W.from_torch(ys[j]), wl.dtype):
         raise RuntimeError("host-direct output differs from the device-resident output")
+
+    # Context: a plain device copy of x into y (torch) of the same size, same pool
+    # and graph shape: the ceiling a kernel moving these bytes meets at this size.
+    # (Last, since it overwrites the pool's y buffers.)
+    Kc = min(K, 20000)
+    c_s, _, _, _ = pb.copy_timed(Kc, 3)
+    copy_gbs = 2 * pb.x_host.element_size() * wl.M * wl.N * Kc / c_s / 1e9
     ring_rows = min(wl.M, args.chunk_rows or max(1, (4 << 20) // (eb * wl.N)))
 
     peak, peak_src = load_peaks()
@@ -576,6 +583,8 @@ def bench_ours(args, wl, rank, world, local_rank):
                 "serial_one_stream": round(whole_job_gbs(wl.algorithmic_bytes, Ke, world,
                                                          serial_s), 2),
                 "host_direct": round(whole_job_gbs(wl.algorithmic_bytes, Ke, world, direct_s), 2)},
+        "context": {"device_copy_same_size_gbs": round(copy_gbs, 1),
+                    "note": "torch copy of x into y, same pool and graph shape (x and y bytes only)"},
         "trials": {"n": 20, "steps_each": t_steps, "median": round(t_med, 2), "min": round(t_min, 2),
                    "max": round(t_max, 2), "unit": "GB/s",
                    "note": "separately timed windows after the timed region; value is the timed region"},
