@@ -139,9 +139,10 @@ namespace {
 // Chooses the variant. The automatic choice, when x, w and y are 16-byte
 // aligned and rows are whole 16-byte vectors (measured on GB300, bf16; the
 // limits are row bytes, so fp32 rows switch at half the column count):
-//   rows of up to 1536 bytes (768 bf16 columns) under strict stream order: the
-//     warp-team kernel (ahead of the TMA kernel at N = 512; with early loads
-//     the TMA kernel is ahead at every N measured);
+//   rows of up to 1536 bytes (768 bf16 columns) under strict stream order, and
+//     rows of up to 256 bytes in either mode: the warp-team kernel (ahead of
+//     the TMA kernel at N = 512 strict; with early loads the TMA kernel is
+//     ahead from N = 512 up, the warp kernel up to N = 128);
 //   rows of up to 16 KB (8192 columns): the TMA-staged kernel (ahead from
 //     N = 1000 to 8192);
 //   rows of up to 64 KB (32768 columns): the register CTA kernel (6.4 TB/s at
@@ -190,7 +191,11 @@ int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch
             const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) &&
                                !(k.flags & RMSNORM_FLAG_NO_PDL);
             const int64_t row_bytes = a.N * elem_bytes(a.dtype);
-            if (!early && row_bytes <= 1536 && warp_choose(a, d, k, l)) {
+            // Rows of up to 16 vectors would leave much of a TMA team (16 threads
+            // at least) idle: the warp kernel takes them in both launch modes
+            // (early loads, GB300: N = 64 bf16 4.97 against 2.47 TB/s, N = 128
+            // 5.72 against 5.37; at N = 256 the two trade places by M).
+            if ((!early || row_bytes <= 256) && row_bytes <= 1536 && warp_choose(a, d, k, l)) {
                 variant = RMSNORM_VARIANT_WARP;
             } else if (row_bytes <= 16384 && (l = Launch{}, tma_choose(a, d, k, l)) &&
                        (l.stages >= 2 || k.stages > 0)) {
