@@ -7,14 +7,13 @@ depend on how rows are grouped into launches).
 """
 from __future__ import annotations
 
-import numpy as np
 import pytest
 import torch
 
 import oracle
 from memory_bound_normalization_fwd_gb300 import binding as B
 from memory_bound_normalization_fwd_gb300 import workloads as W
-from parity_util import DT, compare, compare_fp32
+from parity_util import compare, compare_fp32
 
 pytestmark = pytest.mark.gpu
 
