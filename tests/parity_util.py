@@ -59,8 +59,10 @@ def compare(y_gpu, rstd_gpu, y_ref, rstd_ref, dtype, where=""):
                              f"oracle {y_ref[i]:#06x}")
     rg = np.asarray(rstd_gpu, dtype=np.float64)
     rr = np.asarray(rstd_ref, dtype=np.float64)
-    both_inf = np.isinf(rg) & np.isinf(rr)
-    rel = np.where(both_inf, 0.0, np.abs(rg - rr) / np.where(rr == 0, 1, np.abs(rr)))
+    same = (np.isinf(rg) & np.isinf(rr)) | (np.isnan(rg) & np.isnan(rr))
+    with np.errstate(invalid="ignore"):
+        rel = np.where(same, 0.0, np.abs(rg - rr) / np.where(rr == 0, 1, np.abs(rr)))
+    rel = np.where(np.isnan(rel), np.inf, rel)  # NaN on one side only is a mismatch
     max_rel = float(rel.max()) if rel.size else 0.0
     if not max_rel <= RSTD_REL:
         i = int(np.nanargmax(rel))

@@ -332,6 +332,22 @@ def test_brute_force_tiny_shapes_against_exact_arithmetic(dtype):
                     assert int(y[i, j]) == round_exact(dtype, v), (N, i, j)
 
 
+def test_nan_and_inf_propagate_per_ieee():
+    # A NaN in a row makes its sum, rstd and every y NaN; an Inf makes the sum
+    # Inf and rstd 0, so y = x * 0 * s: +-0 everywhere except NaN at the Inf.
+    x = _bits_of("bf16", [1, -2, 3, 4] * 3).reshape(3, 4)
+    nan_b = np.uint16(0x7FC0)
+    inf_b = np.uint16(0x7F80)
+    x[1, 2] = nan_b
+    x[2, 0] = inf_b
+    w = _bits_of("bf16", [1, 1, 1, 1])
+    y, r = oracle.rmsnorm_fwd(x, w, 1e-6, 0.0, "bf16")
+    yv = oracle.decode("bf16", y)
+    assert np.isfinite(r[0]) and np.all(np.isfinite(yv[0]))
+    assert np.isnan(r[1]) and np.all(np.isnan(yv[1]))
+    assert r[2] == 0.0 and np.isnan(yv[2, 0]) and np.all(yv[2, 1:] == 0)
+
+
 def test_eps_is_taken_as_float32():
     # eps crosses the C boundary as fp32; the oracle must use exactly that value.
     x = _bits_of("bf16", [0, 0])

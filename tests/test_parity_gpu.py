@@ -352,6 +352,26 @@ def test_gemma_identity_on_gpu(variant, N):
     compare(ya, ra, yo, ro, "bf16")
 
 
+@pytest.mark.parametrize("variant,N", [("warp", 512), ("tma", 1000), ("cta", 16384),
+                                       ("cluster", 65536), ("generic", 777)])
+def test_nan_and_inf_propagate(variant, N):
+    # Rows with a NaN give NaN rstd and y; rows with an Inf give rstd 0 and
+    # y = +-0 except NaN at the Inf itself, as in the oracle (IEEE).
+    M = 16
+    wl = W.custom(M, N, "bf16", seed=N + 77)
+    x, w = W.generate(wl)
+    x[3, N // 2] = 0x7FC0   # NaN
+    x[7, 1] = 0x7F80        # +Inf
+    x[9, N - 1] = 0xFF80    # -Inf
+    case = DeviceCase(x, w, "bf16")
+    assert case.run(wl.eps, wl.offset, variant=variant) == 0, B.rmsnorm_last_error()
+    y, r = case.results()
+    case.check_guards()
+    yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "bf16")
+    assert np.isnan(r[3]) and r[7] == 0.0 and r[9] == 0.0
+    compare(y, r, yo, ro, "bf16", where=f"nan/inf {variant}")
+
+
 def test_results_are_deterministic():
     wl = W.WORKLOADS["rmsnorm_16384x512_bf16"]
     x, w = W.generate(wl)
