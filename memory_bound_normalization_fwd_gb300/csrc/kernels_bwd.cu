@@ -18,6 +18,8 @@
 #include "common.cuh"
 #include "launch.h"
 
+#include <algorithm>
+
 namespace rmsn {
 namespace {
 
@@ -213,7 +215,11 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 }
 
 // General backward: any N and 2-byte alignment. dw partial in shared memory (N floats).
-template <int DT, int THREADS>
+// GACC: rows too long for a dw partial row in shared memory accumulate it in
+// this CTA's own row of the workspace instead (each thread owns fixed
+// columns, so no two threads touch one value; a read-modify-write per element
+// per row, for rows past ~56K columns).
+template <int DT, int THREADS, bool GACC>
 __global__ void __launch_bounds__(THREADS)
 bwd_generic_kernel(const void* xv, const void* __restrict__ wv,
                    const float* __restrict__ rstd, const void* dyv, void* dxv,
@@ -225,9 +231,10 @@ bwd_generic_kernel(const void* xv, const void* __restrict__ wv,
     const T* dy = static_cast<const T*>(dyv);
     T* dx = static_cast<T*>(dxv);
     constexpr int kWarps = THREADS / 32;
-    extern __shared__ float sacc[];
+    extern __shared__ float sacc_smem[];
     __shared__ float part[2][kWarps];
     const int tid = threadIdx.x;
+    float* sacc = GACC ? partial + static_cast<int64_t>(blockIdx.x) * N : sacc_smem;
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t j = tid; j < N; j += THREADS) sacc[j] = 0.f;
@@ -258,8 +265,11 @@ bwd_generic_kernel(const void* xv, const void* __restrict__ wv,
         }
         parity ^= 1;
     }
-    __syncthreads();
-    for (int64_t j = tid; j < N; j += THREADS) partial[static_cast<int64_t>(blockIdx.x) * N + j] = sacc[j];
+    if constexpr (!GACC) {
+        __syncthreads();
+        for (int64_t j = tid; j < N; j += THREADS)
+            partial[static_cast<int64_t>(blockIdx.x) * N + j] = sacc[j];
+    }
 }
 
 // dw_j = sum over g < G of partial[g][j]: 32 columns per CTA (lane = column);
@@ -315,11 +325,11 @@ VecFn pick_vec(int T, int V) {
 }
 
 template <int DT>
-GenFn pick_gen(int T) {
+GenFn pick_gen(int T, bool gacc) {
     switch (T) {
-        case 64: return bwd_generic_kernel<DT, 64>;
-        case 256: return bwd_generic_kernel<DT, 256>;
-        case 1024: return bwd_generic_kernel<DT, 1024>;
+        case 64: return gacc ? bwd_generic_kernel<DT, 64, true> : bwd_generic_kernel<DT, 64, false>;
+        case 256: return gacc ? bwd_generic_kernel<DT, 256, true> : bwd_generic_kernel<DT, 256, false>;
+        case 1024: return gacc ? bwd_generic_kernel<DT, 1024, true> : bwd_generic_kernel<DT, 1024, false>;
         default: return nullptr;
     }
 }
@@ -381,14 +391,15 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
         if (variant == 2) return false;
     }
     if (variant == 2) return false;
-    // General kernel: dw partial for the whole row in shared memory.
-    if (a.N * 4 > d.max_smem_optin - 1024) return false;
+    // General kernel: dw partial for the whole row in shared memory, or, past
+    // the shared-memory limit, in the CTA's workspace row.
+    const bool gacc = a.N * 4 > d.max_smem_optin - 1024;
     int T = k.lanes_per_row > 0 ? k.lanes_per_row : (a.N >= 4096 ? 1024 : a.N >= 512 ? 256 : 64);
-    GenFn fn = a.dtype == kBF16   ? pick_gen<kBF16>(T)
-               : a.dtype == kFP16 ? pick_gen<kFP16>(T)
-                                  : pick_gen<kFP32>(T);
+    GenFn fn = a.dtype == kBF16   ? pick_gen<kBF16>(T, gacc)
+               : a.dtype == kFP16 ? pick_gen<kFP16>(T, gacc)
+                                  : pick_gen<kFP32>(T, gacc);
     if (!fn) return false;
-    const int smem = static_cast<int>(a.N * 4);
+    const int smem = gacc ? 0 : static_cast<int>(a.N * 4);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -401,6 +412,10 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
     l.ctas_per_sm = occupancy(l.kernel, T, smem);
     if (l.ctas_per_sm < 1) return false;
     l.grid = persistent_grid(a.M > 0 ? a.M : 1, 1, d.sm_count, l.ctas_per_sm, k.max_ctas);
+    if (gacc) {  // keep the partial rows, read and written every row, within ~64 MB of L2
+        const int64_t cap = std::max<int64_t>(1, (int64_t(64) << 20) / (a.N * 4));
+        if (l.grid > cap) l.grid = static_cast<int>(cap);
+    }
     l.work_items = a.M;
     return true;
 }

@@ -100,6 +100,19 @@ def test_bwd_parity(dtype, M, N, variant):
         _check(x, w, dy, rstd, dx, dw, offset, dtype, where=f"{variant} {M}x{N} {max_ctas}")
 
 
+@pytest.mark.parametrize("M,N,dtype", [(64, 100000, "bf16"), (7, 70001, "fp32"), (300, 60000, "fp16")])
+@pytest.mark.parametrize("max_ctas", [0, 5])
+def test_bwd_rows_past_the_shared_memory_limit(M, N, dtype, max_ctas):
+    # Rows whose fp32 dw partial does not fit in shared memory (N * 4 bytes
+    # past ~227 KB): the general kernel keeps the partial in its workspace row.
+    offset = float(N % 2)
+    x, w, dy, rstd = _inputs(M, N, dtype, seed=N + M, offset=offset)
+    plan_bytes = B.rmsnorm_bwd_workspace_size(M, N, DT[dtype], B.make_options(max_ctas=max_ctas))
+    assert plan_bytes % (N * 4) == 0 and plan_bytes <= 64 << 20
+    dx, dw = _run(x, w, dy, rstd, offset, dtype, max_ctas=max_ctas)
+    _check(x, w, dy, rstd, dx, dw, offset, dtype, where=f"{M}x{N} {dtype} {max_ctas}")
+
+
 @pytest.mark.parametrize("inplace", ["x", "dy"])
 @pytest.mark.parametrize("N", [512, 777])
 def test_bwd_in_place(inplace, N):

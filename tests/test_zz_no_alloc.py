@@ -62,7 +62,8 @@ def _ordinal(t):
 
 
 @pytest.mark.parametrize("M,N,dtype", [(20000, 8192, "bf16"), (777, 512, "fp16"),
-                                       (50, 777, "bf16"), (3, 16384, "fp16"), (4000, 1000, "fp32")])
+                                       (50, 777, "bf16"), (3, 16384, "fp16"), (4000, 1000, "fp32"),
+                                       (40, 100000, "bf16")])
 def test_no_alloc_backward_matches_the_workspace_backward(M, N, dtype):
     for call, seed in enumerate((11, 12)):  # two calls in a row, different inputs
         xd, wd, gd, rd = _inputs(M, N, dtype, seed + N)
