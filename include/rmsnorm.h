@@ -273,8 +273,9 @@ int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void
  * a warp-per-row kernel and rows of up to 16384 columns a CTA-per-row kernel;
  * others the general kernel, which keeps a CTA's dw partial row in shared memory
  * up to about 56K columns and, past that, in its own row of the workspace (any
- * N; the grid is then capped so that the partial rows stay within 64 MB). Options: variant AUTO, WARP, CTA or GENERIC,
- * lanes_per_row (CTA: threads per CTA), max_ctas, RMSNORM_FLAG_NO_PDL.
+ * N; the grid is then capped so that the partial rows stay within 64 MB).
+ * Options: variant AUTO, WARP, CTA or GENERIC, lanes_per_row (CTA: threads per
+ * CTA), max_ctas, RMSNORM_FLAG_NO_PDL.
  */
 int rmsnorm_bwd(const void* x, const void* w, const float* rstd, const void* dy, void* dx,
                 float* dw, int64_t M, int64_t N, float offset, int dtype, void* workspace,
