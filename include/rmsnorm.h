@@ -259,7 +259,7 @@ int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void
  *   dx    = rstd[i] * (dy[i,j] * s_j - x[i,j] * rstd[i]^2 * c_i / N)   (x's dtype)
  *   dw[j] = sum_i dy[i,j] * x[i,j] * rstd[i]                              (fp32)
  * fp32 arithmetic; dx rounded once to nearest even; dw summed per CTA over its
- * rows, then over CTAs in index order (deterministic for a fixed device).
+ * rows, then over CTAs in a fixed order (deterministic for a fixed device).
  *   x, dy, dx  [M, N] x's dtype (bf16, fp16 or fp32), contiguous; dx may equal
  *              x or dy exactly
  *   w          [N]    x's dtype

@@ -12,9 +12,9 @@
 // fp32 registers across all the rows it sees; the row sum c goes through a
 // warp butterfly and a shared-memory step. At the end each CTA writes its dw
 // partial (fp32, N values) to row blockIdx.x of the caller's workspace.
-// Kernel 2 sums the partials over CTAs in index order (deterministic) into dw.
-// The general kernel takes any N and alignment with element accesses and a
-// shared-memory dw partial.
+// Kernel 2 sums the partials over CTAs in a fixed order (deterministic) into dw.
+// The general kernel takes any N and alignment with element accesses; its dw
+// partial sits in shared memory, or in its workspace row for very long rows.
 #include "common.cuh"
 #include "launch.h"
 
