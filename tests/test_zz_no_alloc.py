@@ -86,3 +86,20 @@ def test_no_alloc_rejects_bad_arguments_on_the_host():
     s = torch.cuda.current_stream().cuda_stream
     assert B.rmsnorm_bwd_noalloc(0, wd.data_ptr(), 0, 0, 0, 0, 0, 64, 0.0, B.BF16, None, s) == -1
     assert B.rmsnorm_bwd_noalloc(0, wd.data_ptr(), 0, 0, 0, 0, 0, 64, 0.0, 7, None, s) == -3
+
+
+def test_no_alloc_refuses_rows_longer_than_its_scratch():
+    # One partial row of N fp32 values must fit the built-in 8 MiB scratch
+    # (2^21 values): a longer row is refused before any launch, dw untouched.
+    N = (1 << 21) + 8
+    xd = torch.zeros((1, N), dtype=torch.bfloat16, device="cuda")
+    gd, dxd = torch.zeros_like(xd), torch.zeros_like(xd)
+    wd = torch.ones(N, dtype=torch.bfloat16, device="cuda")
+    rd = torch.ones(1, dtype=torch.float32, device="cuda")
+    dwd = torch.full((N,), 5.0, dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    rc = B.rmsnorm_bwd_noalloc(xd.data_ptr(), wd.data_ptr(), rd.data_ptr(), gd.data_ptr(),
+                               dxd.data_ptr(), dwd.data_ptr(), 1, N, 0.0, B.BF16, None, s)
+    assert rc == -11 and "scratch" in B.rmsnorm_last_error()
+    torch.cuda.synchronize()
+    assert torch.all(dwd == 5.0)
