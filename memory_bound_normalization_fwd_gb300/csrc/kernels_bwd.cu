@@ -442,7 +442,7 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
             l.ctas_per_sm = occupancy(l.kernel, T, smem);
             l.grid = persistent_grid(a.M > 0 ? a.M : 1, 1, d.sm_count, l.ctas_per_sm, k.max_ctas);
             l.work_items = a.M;
-                return true;
+            return true;
         }
         if (variant == 2) return false;
     }
