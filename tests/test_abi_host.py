@@ -200,3 +200,48 @@ def test_host_path_validation_before_any_cuda_call(lib, kw, code):
 
 def test_host_path_m_zero_needs_nothing(lib):
     assert _host_call(lib, x=0, y=0, r=0, M=0, ws=0, nbytes=0) == 0
+
+
+CONSUMER = r"""
+#include "rmsnorm.h"
+#include <stdio.h>
+#include <string.h>
+
+int main(void) {
+    rmsnorm_options_t o;
+    int64_t bytes = -1;
+    memset(&o, 0, sizeof(o));
+    o.struct_size = (int)sizeof(o);
+    /* host-side validation only: a null x is refused before any CUDA call */
+    int rc = rmsnorm_fwd(NULL, NULL, NULL, NULL, 4, 8, 1e-6f, 0.0f, RMSNORM_DTYPE_BF16, NULL);
+    int rc_ex = rmsnorm_fwd_ex(NULL, NULL, NULL, NULL, 4, 8, 1e-6f, 0.0f, RMSNORM_DTYPE_FP16, &o, NULL);
+    int rc_ws = rmsnorm_fwd_host_workspace_size(1000, 512, RMSNORM_DTYPE_BF16, 0, &bytes);
+    printf("%d %d %d %d %lld|%s|%s\n", rmsnorm_version(), rc, rc_ex, rc_ws, (long long)bytes,
+           rmsnorm_strerror(rc), rmsnorm_last_error());
+    return 0;
+}
+"""
+
+
+@pytest.mark.parametrize("compiler,std", [("gcc", "-std=c99"), ("g++", "-std=c++17")])
+def test_plain_c_and_cpp_consumers_compile_link_and_call(lib, tmp_path, compiler, std):
+    # The header is the boundary: a C99 (and a C++) program that includes it
+    # with warnings as errors, links the shared library and calls host-only
+    # entry points gets the same answers as the Python binding.
+    import shutil
+    import subprocess
+    if shutil.which(compiler) is None:
+        pytest.skip(f"{compiler} not installed")
+    src = tmp_path / ("consumer.c" if compiler == "gcc" else "consumer.cpp")
+    src.write_text(CONSUMER)
+    exe = tmp_path / "consumer"
+    libdir = os.path.dirname(B.library_path())
+    subprocess.run([compiler, std, "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                    os.path.join(ROOT, "include"), str(src), B.library_path(),
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.strip()
+    head, strerr, detail = out.split("|")
+    version, rc, rc_ex, rc_ws, nbytes = (int(v) for v in head.split())
+    assert version == B.rmsnorm_version()
+    assert rc == rc_ex == -1 and strerr == B.rmsnorm_strerror(-1) and detail
+    assert rc_ws == 0 and nbytes == B.rmsnorm_fwd_host_workspace_size(1000, 512, B.BF16, 0)
