@@ -61,6 +61,8 @@ def _build(tmp, source: str) -> ctypes.CDLL:
     L.oracle_rmsnorm_fwd.argtypes = [vp, vp, vp, f64p, f64p, ctypes.c_int64, ctypes.c_int64,
                                      ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int64,
                                      ctypes.c_int64]
+    L.oracle_rmsnorm_bwd.argtypes = [vp, vp, vp, f64p, vp, f64p, f64p, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_float, ctypes.c_float, ctypes.c_int]
     L.oracle_encode.argtypes = [ctypes.c_int, ctypes.c_int64, f64p, vp]
     L.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_int64, vp, f64p]
     return L
@@ -184,6 +186,85 @@ def _just_below_tie_rounds_down(L, dtype) -> bool:
     return y[0].tolist() == [round_exact(dtype, Fraction(1) + Fraction(ulp))] * 4
 
 
+# Slips in the backward (dx = r (dy s - x r^2 c / N), c = sum dy s x, dw = sum dy x r).
+BWD_MUTATIONS = {
+    "bwd: projection term dropped": ("double v = r * (gv * sv - xv * r * r * c / (double)N);",
+                                     "double v = r * gv * sv;"),
+    "bwd: projection term added": ("double v = r * (gv * sv - xv * r * r * c / (double)N);",
+                                   "double v = r * (gv * sv + xv * r * r * c / (double)N);"),
+    "bwd: r instead of r^2": ("double v = r * (gv * sv - xv * r * r * c / (double)N);",
+                              "double v = r * (gv * sv - xv * r * c / (double)N);"),
+    "bwd: divides by N+1": ("double v = r * (gv * sv - xv * r * r * c / (double)N);",
+                            "double v = r * (gv * sv - xv * r * r * c / (double)(N + 1));"),
+    "bwd: weight left out of c": (
+        "c += load_elem(dtype, dy, base + j) * (off + load_elem(dtype, w, j)) *",
+        "c += load_elem(dtype, dy, base + j) * (off + 1.0) *"),
+    "bwd: offset left out of the scale": ("double sv = off + load_elem(dtype, w, j);",
+                                          "double sv = load_elem(dtype, w, j);"),
+    "bwd: dw without r": ("if (dw) dw[j] += gv * xv * r;", "if (dw) dw[j] += gv * xv;"),
+    "bwd: dw times the scale": ("if (dw) dw[j] += gv * xv * r;",
+                                "if (dw) dw[j] += gv * xv * r * sv;"),
+    "bwd: recomputed rstd without eps": ("r = 1.0 / sqrt(s / (double)N + (double)eps);",
+                                         "r = 1.0 / sqrt(s / (double)N);"),
+    "bwd: x and dy swapped": (
+        "double xv = load_elem(dtype, x, base + j), gv = load_elem(dtype, dy, base + j);",
+        "double gv = load_elem(dtype, x, base + j), xv = load_elem(dtype, dy, base + j);"),
+}
+
+
+def _bwd(L, x, w, dy, rstd, eps, offset, dtype):
+    M, N = x.shape
+    x, w, dy = (np.ascontiguousarray(a, dtype=BITS[dtype]) for a in (x, w, dy))
+    dx = np.zeros((M, N), dtype=BITS[dtype])
+    dx64 = np.zeros((M, N), dtype=np.float64)
+    dw = np.zeros(N, dtype=np.float64)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    rp = None if rstd is None else np.ascontiguousarray(rstd, dtype=np.float64)
+    rc = L.oracle_rmsnorm_bwd(x.ctypes.data, w.ctypes.data, dy.ctypes.data,
+                              None if rp is None else rp.ctypes.data_as(f64p), dx.ctypes.data,
+                              dx64.ctypes.data_as(f64p), dw.ctypes.data_as(f64p), M, N, eps,
+                              offset, CODE[dtype])
+    assert rc == 0
+    return dx, dx64, dw
+
+
+def _bwd_pins_hold(L) -> bool:
+    """The backward against torch float64 autograd of the textbook forward
+    expression (an outside routine), with the saved rstd passed in and with
+    rstd recomputed; dx's stored bits are the encoder's rounding of its fp64
+    value."""
+    import torch
+    rng = np.random.default_rng(5)
+    eps = 1e-3
+    e = float(np.float32(eps))
+    for dtype in ("bf16", "fp16", "fp32"):
+        for N in (1, 5, 33):
+            M = 3
+            x = _bits(dtype, rng.normal(0, 1.5, M * N).astype(np.float32)).reshape(M, N)
+            dy = _bits(dtype, rng.normal(0, 1.0, M * N).astype(np.float32)).reshape(M, N)
+            w = _bits(dtype, rng.normal(0, 0.7, N).astype(np.float32))
+            xv = torch.tensor(_decode(L, dtype, x).reshape(M, N), requires_grad=True)
+            gv = torch.tensor(_decode(L, dtype, dy).reshape(M, N))
+            for offset in (0.0, 1.0):
+                wv = torch.tensor(_decode(L, dtype, w), requires_grad=True)
+                xv.grad = None
+                r = torch.rsqrt(xv.pow(2).mean(-1, keepdim=True) + e)
+                ((xv * r * (offset + wv)) * gv).sum().backward()
+                terms = (r * gv.abs() * (offset + wv).abs()).detach().numpy()
+                r64 = r.detach().numpy().ravel()
+                for rstd in (r64, None):
+                    dx, dx64, dw = _bwd(L, x, w, dy, rstd, eps, offset, dtype)
+                    if not np.all(np.abs(dx64 - xv.grad.numpy())
+                                  <= 1e-11 * np.abs(dx64) + 1e-13 * terms):
+                        return False
+                    ref_dw = wv.grad.numpy()
+                    if not np.allclose(dw, ref_dw, rtol=1e-11, atol=1e-13 * np.abs(ref_dw).max()):
+                        return False
+                    if not np.array_equal(dx.ravel(), _encode(L, dtype, dx64.ravel())):
+                        return False
+    return True
+
+
 def test_the_oracle_itself_passes_the_battery(tmp_path):
     assert _pins_hold(_build(str(tmp_path), open(SRC).read()))
 
@@ -195,3 +276,15 @@ def test_each_planted_slip_fails_the_pins(tmp_path, name):
     assert old in src, f"mutation anchor not found: {old}"
     # The first occurrence is the forward's (the backward follows it in the file).
     assert not _pins_hold(_build(str(tmp_path), src.replace(old, new, 1)))
+
+
+def test_the_oracle_backward_passes_its_battery(tmp_path):
+    assert _bwd_pins_hold(_build(str(tmp_path), open(SRC).read()))
+
+
+@pytest.mark.parametrize("name", list(BWD_MUTATIONS))
+def test_each_planted_backward_slip_fails_the_pins(tmp_path, name):
+    old, new = BWD_MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old}"
+    assert not _bwd_pins_hold(_build(str(tmp_path), src.replace(old, new)))
