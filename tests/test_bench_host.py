@@ -1,5 +1,6 @@
 """Host logic of bench.py that needs no GPU: which committed traffic figure
-the benchmark line may quote."""
+the benchmark line may quote, the bit-agreement rule, and the reference arm
+(the oracle timed on the host cores) with its JSON line."""
 from __future__ import annotations
 
 import json
@@ -42,3 +43,37 @@ def test_agree_allows_one_ulp_and_nothing_more():
     assert not bench.agree(a, np.array([0x3F82, 0x8001, 0x0000, 0x7F7F], dtype=np.uint16), "bf16")
     f = np.array([1.0, -2.5], dtype=np.float32).view(np.uint32)
     assert bench.agree(f, f + 64, "fp32") and not bench.agree(f, f + 65, "fp32")
+
+
+def _reference_arm(env_extra):
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, **env_extra)
+    root = os.path.dirname(os.path.abspath(bench.__file__))
+    return subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                           "--workload", "rmsnorm_2048x512_bf16", "--steps", "3", "--warmup", "3"],
+                          capture_output=True, text=True, env=env, cwd=root, timeout=300)
+
+
+def test_reference_arm_prints_one_contract_line_on_the_host():
+    # The reference arm is the oracle on the host cores: no GPU, one JSON line
+    # with the metric, unit and direction of the main arm, and the extra keys.
+    p = _reference_arm({"RANK": "0", "WORLD_SIZE": "1", "LOCAL_RANK": "0"})
+    assert p.returncode == 0, p.stderr
+    lines = [ln for ln in p.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["higher_is_better"] is True and d["steps"] == 3 and d["warmup"] >= 3
+    assert d["value"] > 0 and d["config"]["workload"] == "rmsnorm_2048x512_bf16"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    p = _reference_arm({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert p.returncode == 0, p.stderr
+    assert p.stdout.strip() == ""
