@@ -130,3 +130,24 @@ def test_saved_rstd_equals_recomputed():
     assert all(np.array_equal(p, q) for p, q in zip(a, b))
     # and dx is the single rounding of its fp64 value
     assert np.array_equal(a[0], oracle.encode("fp16", a[1]))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("offset", [0.0, 1.0])
+def test_constant_row_centres_the_scaled_gradient(dtype, offset):
+    # Closed form: x_ij = c for all j, eps = 0 gives r = 1/|c| and
+    # x_j r^2 c_i / N = mean_k(dy_k s_k), so dx_j = (dy_j s_j - mean_k dy_k s_k) / |c|
+    # and dw_j = sum_i dy_ij sign(c_i). Dyadic inputs and N = 16 make it exact.
+    rng = np.random.default_rng(17)
+    N = 16
+    cs = [2.0, -0.5, 4.0]
+    dyv = rng.integers(-8, 9, (3, N)) / 4.0
+    wv = rng.integers(-4, 5, N) / 8.0
+    x = np.array([oracle.encode(dtype, np.full(N, c)) for c in cs])
+    dy = oracle.encode(dtype, dyv.ravel()).reshape(3, N)
+    w = oracle.encode(dtype, wv)
+    _, dx64, dw = oracle.rmsnorm_bwd(x, w, dy, offset, dtype, eps=0.0)
+    g = dyv * (offset + wv)
+    want = (g - g.mean(axis=1, keepdims=True)) / np.abs(np.array(cs))[:, None]
+    assert np.array_equal(dx64, want)
+    assert np.array_equal(dw, (dyv * np.sign(np.array(cs))[:, None]).sum(axis=0))
