@@ -28,6 +28,7 @@ import sys
 import tempfile
 import threading
 import time
+from typing import NamedTuple
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -45,14 +46,16 @@ KERNEL_SOURCES = ["common.cuh", "async_copy.cuh", "cluster.cuh", "launch.h", "ke
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=300000)
-    p.add_argument("--warmup", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=None, help="named workload (default: the 16384x512 bf16 one)")
     p.add_argument("--e2e-steps", type=int, default=400)
     p.add_argument("--chunk-rows", type=int, default=0,
                    help="rows per chunk of the host-buffer path (0: the library's default)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-workload", action="store_true",
+                   help="skip the per-workload entries (every named workload, both launch modes)")
     p.add_argument("--variant", default="auto", help="force a kernel variant (ablation)")
     p.add_argument("--lanes-per-row", type=int, default=0)
     p.add_argument("--stages", type=int, default=0)
@@ -134,23 +137,25 @@ PLAN_KEYS = ("variant", "threads", "grid", "lanes_per_row", "vecs_per_lane", "ro
 def load_traffic(workload: str, plan: dict, profiles_dir: str | None = None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current sources of the timed kernel (its `kernel_hash` line matches the
-    variant's source hash) with the same launch plan (its `plan` line), else None."""
+    variant's source hash) with the same launch plan (its `plan` line), else None.
+    A summary may hold several entries (one per launch plan, e.g. both launch
+    modes); each starts at its own `kernel_hash` line."""
     path = os.path.join(profiles_dir or os.path.join(ROOT, "profiles"), f"traffic_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
-    m_hash = re.search(r"kernel_hash:\s*`?([0-9a-f]+)", text)
-    m_bytes = re.search(r"traffic_bytes_per_launch:\s*`?([0-9]+)", text)
-    m_plan = re.search(r"plan:\s*`(\{.*?\})`", text)
-    if not (m_hash and m_bytes and m_plan):
-        return None
-    if m_hash.group(1) != kernel_hash(plan["variant"]):
-        return None
-    recorded = json.loads(m_plan.group(1))
-    if any(recorded.get(k) != plan.get(k) for k in PLAN_KEYS):
-        return None
-    return int(m_bytes.group(1))
+    want = kernel_hash(plan["variant"])
+    for seg in re.split(r"(?=kernel_hash:)", text)[1:]:
+        m_hash = re.search(r"kernel_hash:\s*`?([0-9a-f]+)", seg)
+        m_bytes = re.search(r"traffic_bytes_per_launch:\s*`?([0-9]+)", seg)
+        m_plan = re.search(r"plan:\s*`(\{.*?\})`", seg)
+        if not (m_hash and m_bytes and m_plan) or m_hash.group(1) != want:
+            continue
+        recorded = json.loads(m_plan.group(1))
+        if all(recorded.get(k) == plan.get(k) for k in PLAN_KEYS):
+            return int(m_bytes.group(1))
+    return None
 
 
 class ClockSampler:
@@ -217,6 +222,17 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- timing harness
 
+class Timed(NamedTuple):
+    """One timed region: max-over-ranks seconds, steps it ran, seconds per step
+    (this rank), clock samples, how it was launched, graph replays it held."""
+    max_s: float
+    steps: int
+    per_step_s: float
+    clocks: dict | None
+    launch: str
+    replays: int
+
+
 class PoolBench:
     """Inputs resident in HBM in a rotating pool of buffer sets (>= 3x L2, so no
     step reads another step's lines from L2), steps issued as a CUDA graph of
@@ -238,24 +254,40 @@ class PoolBench:
         self.rs = [torch.empty(wl.M, dtype=torch.float32, device=dev) for _ in range(self.pool)]
         self.stream = torch.cuda.Stream(dev)
 
-    def _graph_time(self, step, K: int, Wm: int, clock_gpu=None):
+    def _graph_time(self, step, K: int, Wm: int, clock_gpu=None, min_ms: float = 2.0):
+        """Time K steps as the GPU runs them, at any K.
+
+        Exactly K calls (rotating through the pool) are captured into one CUDA
+        graph. After Wm untimed direct calls and untimed replays of the graph,
+        the timed region is R back-to-back replays of that graph between two
+        CUDA events on the launching stream, R chosen (the same on every rank)
+        so that the region lasts at least ``min_ms``; the per-step time is the
+        region's time over R*K. A timed region of direct host calls would time
+        the host's launch rate instead of the kernels."""
         import torch
         stream = self.stream
         with torch.cuda.stream(stream):
             for k in range(max(3, min(Wm, 64))):
                 step(k)
         stream.synchronize()
-        per_graph = self.pool * max(1, 384 // self.pool)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
-            for k in range(per_graph):
+            for k in range(K):
                 step(k)
         torch.cuda.synchronize()
-        replays, rem = divmod(K, per_graph)
         with torch.cuda.stream(stream):
-            for _ in range(-(-Wm // per_graph)):
+            for _ in range(max(1, -(-Wm // K))):
                 graph.replay()
         torch.cuda.synchronize()
+        # Replays per timed region, from one timed probe replay (max over ranks,
+        # so every rank runs the same count).
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        reps = int(max_over_ranks(float(max(1, -(-min_ms // max(a.elapsed_time(b), 1e-3))))))
         barrier()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
@@ -267,10 +299,8 @@ class PoolBench:
             barrier()
             with torch.cuda.stream(stream):
                 start.record(stream)
-                for _ in range(replays):
+                for _ in range(reps):
                     graph.replay()
-                for k in range(rem):
-                    step(k)
                 end.record(stream)
             torch.cuda.synchronize()
             barrier()
@@ -278,9 +308,11 @@ class PoolBench:
             if sampler:
                 sampler.__exit__(None, None, None)
         ms = start.elapsed_time(end)
-        launch = f"CUDA graph of {per_graph} ABI calls, {replays} replays" + (
-            f" + {rem} direct calls" if rem else "")
-        return max_over_ranks(ms / 1e3), ms / 1e3 / K, (sampler.summary() if sampler else None), launch
+        steps = reps * K
+        launch = (f"CUDA graph of {K} ABI calls (rotating the pool), {reps} replays back to back "
+                  f"in the timed region ({steps} steps)")
+        return Timed(max_over_ranks(ms / 1e3), steps, ms / 1e3 / steps,
+                     sampler.summary() if sampler else None, launch, reps)
 
     def trials(self, opts, n_trials: int = 20, min_ms: float = 2.0):
         """GB/s of `n_trials` separately timed windows (each at least `min_ms` of
@@ -327,8 +359,8 @@ class PoolBench:
                for t in range(n_trials)]
         return st.median(gbs), min(gbs), max(gbs), steps
 
-    def timed(self, opts, K: int, Wm: int, clock_gpu=None):
-        """(max-over-ranks seconds, seconds per step, clocks, launch text) for K steps."""
+    def timed(self, opts, K: int, Wm: int, clock_gpu=None, min_ms: float = 2.0) -> Timed:
+        """K steps of rmsnorm_fwd_ex with `opts`, timed as `_graph_time` times them."""
         from memory_bound_normalization_fwd_gb300 import binding as B
         wl, sh = self.wl, self.stream.cuda_stream
 
@@ -339,14 +371,14 @@ class PoolBench:
                                   opts, sh)
             if rc != 0:
                 raise RuntimeError(B.rmsnorm_last_error())
-        return self._graph_time(step, K, Wm, clock_gpu)
+        return self._graph_time(step, K, Wm, clock_gpu, min_ms)
 
-    def copy_timed(self, K: int, Wm: int):
+    def copy_timed(self, K: int, Wm: int, min_ms: float = 2.0) -> Timed:
         """A plain device copy of x into y at the same size, same pool, same graph shape."""
         def step(k: int):
             i = k % self.pool
             self.ys[i].copy_(self.xs[i])
-        return self._graph_time(step, K, Wm)
+        return self._graph_time(step, K, Wm, None, min_ms)
 
 
 def agree(a_bits, b_bits, dtype: str) -> bool:
@@ -441,28 +473,34 @@ def bench_ours(args, wl, rank, world, local_rank):
     plan = B.rmsnorm_plan_info(wl.M, wl.N, dcode, xs[0].data_ptr(), w_dev.data_ptr(),
                                ys[0].data_ptr(), opts)
     K, Wm = args.steps, max(3, args.warmup)
-    max_s, per_launch_s, clocks, launch = timed(
-        opts, K, Wm, torch.cuda.current_device() if world == 1 else local_rank)
-    value = whole_job_gbs(wl.algorithmic_bytes, K, world, max_s)
+    # The timed region lasts at least half a second, so that the clock sampler
+    # sees it under load.
+    main = timed(opts, K, Wm, torch.cuda.current_device() if world == 1 else local_rank,
+                 min_ms=500.0)
+    value = whole_job_gbs(wl.algorithmic_bytes, main.steps, world, main.max_s)
+    per_launch_s = main.per_step_s
 
-    # The same workload under strict stream order (every access waits for the previous step).
+    # The same workload under strict stream order (every access waits for the
+    # previous step): the figure that applies to a dependent chain of layers,
+    # where each launch reads the previous kernel's output.
     strict = None
     if early:
         sopts = make_opts(False)
         splan = B.rmsnorm_plan_info(wl.M, wl.N, dcode, xs[0].data_ptr(), w_dev.data_ptr(),
                                     ys[0].data_ptr(), sopts)
-        Ks = min(K, 100000)
         # Weights resident (as in inference), x the previous step's output: the
         # strict chain with only w read early.
-        w_max, _, _, _ = timed(make_opts(False, True), Ks, Wm)
-        s_max, s_launch, _, _ = timed(sopts, Ks, Wm)
-        strict = {"value": round(whole_job_gbs(wl.algorithmic_bytes, Ks, world, s_max), 2),
-                  "unit": "GB/s", "steps": Ks,
+        tw = timed(make_opts(False, True), K, Wm, min_ms=100.0)
+        ts = timed(sopts, K, Wm, min_ms=100.0)
+        strict = {"value": round(whole_job_gbs(wl.algorithmic_bytes, ts.steps, world, ts.max_s), 2),
+                  "unit": "GB/s", "steps": ts.steps, "launch": ts.launch,
                   "frac": None, "plan": splan,
-                  "early_weights": round(whole_job_gbs(wl.algorithmic_bytes, Ks, world, w_max), 2),
+                  "early_weights": round(whole_job_gbs(wl.algorithmic_bytes, tw.steps, world,
+                                                       tw.max_s), 2),
                   "note": "no RMSNORM_FLAG_EARLY_LOADS: each launch reads x only after the "
-                          "previous step completes; early_weights: the same with "
-                          "RMSNORM_FLAG_EARLY_WEIGHTS (w read before the wait, x after)"}
+                          "previous step completes (the case of a dependent chain of layers); "
+                          "early_weights: the same with RMSNORM_FLAG_EARLY_WEIGHTS (w read "
+                          "before the wait, x after)"}
     # Twenty separately timed windows of the headline configuration (after the
     # timed region above, which alone gives `value`): median, min, max.
     t_med, t_min, t_max, t_steps = pb.trials(make_opts(early))
@@ -543,9 +581,8 @@ def bench_ours(args, wl, rank, world, local_rank):
     # Context: a plain device copy of x into y (torch) of the same size, same pool
     # and graph shape: the ceiling a kernel moving these bytes meets at this size.
     # (Last, since it overwrites the pool's y buffers.)
-    Kc = min(K, 20000)
-    c_s, _, _, _ = pb.copy_timed(Kc, 3)
-    copy_gbs = 2 * pb.x_host.element_size() * wl.M * wl.N * Kc / c_s / 1e9
+    tc = pb.copy_timed(K, 3, min_ms=100.0)
+    copy_gbs = 2 * pb.x_host.element_size() * wl.M * wl.N * tc.steps / tc.max_s / 1e9
     ring_rows = min(wl.M, args.chunk_rows or max(1, (4 << 20) // (eb * wl.N)))
 
     peak, peak_src = load_peaks()
@@ -553,7 +590,7 @@ def bench_ours(args, wl, rank, world, local_rank):
     traffic = load_traffic(wl.name, plan)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": K, "warmup": Wm, "ms_per_step": round(max_s * 1e3 / K, 6),
+        "steps": K, "warmup": Wm, "ms_per_step": round(main.max_s * 1e3 / main.steps, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded torch CPU generator; see workloads.py)",
         "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "eps": wl.eps, "offset": wl.offset,
@@ -562,7 +599,7 @@ def bench_ours(args, wl, rank, world, local_rank):
                    "bytes_per_step": wl.algorithmic_bytes,
                    "l2": f"rotating pool of {pool} buffer sets ({pool * set_bytes / 1e6:.0f} MB) "
                          f"> 3x L2 ({l2 / 1e6:.0f} MB); no flush needed",
-                   "launch": launch,
+                   "launch": main.launch,
                    "launch_order": ("early loads (RMSNORM_FLAG_EARLY_LOADS): steps are independent "
                                     "batches, so step k+1 may start loading x while step k "
                                     "finishes; all stores stay in stream order") if early
@@ -588,15 +625,57 @@ def bench_ours(args, wl, rank, world, local_rank):
         "trials": {"n": 20, "steps_each": t_steps, "median": round(t_med, 2), "min": round(t_min, 2),
                    "max": round(t_max, 2), "unit": "GB/s",
                    "note": "separately timed windows after the timed region; value is the timed region"},
-        "gpu_launches": K,
-        "clocks": clocks,
+        "timed_region": {"steps": main.steps, "graph_replays": main.replays,
+                         "seconds": round(main.max_s, 6),
+                         "note": f"the --steps {K} ABI calls captured once as a CUDA graph and "
+                                 f"replayed {main.replays} times back to back between CUDA events; "
+                                 "ms_per_step = region time / steps run"},
+        "gpu_launches": main.steps,  # one kernel per rmsnorm_fwd_ex call
+        "clocks": main.clocks,
     }
     if strict is not None:
         strict["frac"] = round(strict["value"] / peak, 4)
         line["strict_order"] = strict
+    if world == 1 and not args.no_per_workload:
+        del pb, xs, ys, rs
+        torch.cuda.empty_cache()
+        line["per_workload"] = per_workload(args, dev, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x_bits, w_bits, wl)
     return line
+
+
+def per_workload(args, dev, peak: float) -> dict:
+    """Every named workload (the metric is per M x N x dtype), in both launch
+    modes, timed as the headline is: a CUDA graph of `steps` ABI calls over a
+    rotating pool (>= 3x L2) replayed back to back for at least 100 ms. Each
+    entry: GB/s, fraction of the peak, the plan, and the DRAM traffic per
+    launch from the committed ncu summary when it matches the current kernel
+    sources and plan (else null)."""
+    import torch
+    from memory_bound_normalization_fwd_gb300 import binding as B
+    from memory_bound_normalization_fwd_gb300 import workloads as W
+    out = {}
+    for name, wl in W.WORKLOADS.items():
+        x_bits, w_bits = W.generate(wl)
+        pb = PoolBench(wl, x_bits, w_bits, dev)
+        K = max(1, min(args.steps, 200))
+        entry = {"M": wl.M, "N": wl.N, "dtype": wl.dtype, "bytes_per_step": wl.algorithmic_bytes,
+                 "pool_sets": pb.pool}
+        for mode, early in (("early_loads", True), ("strict", False)):
+            opts = B.make_options(early_loads=early)
+            plan = B.rmsnorm_plan_info(wl.M, wl.N, pb.dcode, pb.xs[0].data_ptr(),
+                                       pb.w_dev.data_ptr(), pb.ys[0].data_ptr(), opts)
+            t = pb.timed(opts, K, 3, min_ms=100.0)
+            gbs = wl.algorithmic_bytes / t.per_step_s / 1e9
+            entry[mode] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                           "us_per_step": round(t.per_step_s * 1e6, 3), "steps": t.steps,
+                           "graph_calls": K, "plan": plan,
+                           "traffic": load_traffic(name, plan)}
+        out[name] = entry
+        del pb
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------- ablation matrix
@@ -643,10 +722,10 @@ def run_ablation(args, names):
         x_bits, w_bits = W.generate(wl)
         pb = PoolBench(wl, x_bits, w_bits, dev)
         K = args.steps if wl.M * wl.N < (1 << 26) else max(200, args.steps // 20)
-        s, _, _, _ = pb.copy_timed(K, 3)
+        t = pb.copy_timed(K, 3, min_ms=100.0)
         print(json.dumps({"ablation": name, "config": "device copy x -> y (torch)",
-                          "gbs": round(2 * pb.x_host.element_size() * wl.M * wl.N * K / s / 1e9,
-                                       1)}), flush=True)
+                          "gbs": round(2 * pb.x_host.element_size() * wl.M * wl.N * t.steps
+                                       / t.max_s / 1e9, 1)}), flush=True)
         for cfg in ablation_configs(wl):
             opts = B.make_options(**cfg)
             try:
@@ -654,8 +733,8 @@ def run_ablation(args, names):
                                            pb.w_dev.data_ptr(), pb.ys[0].data_ptr(), opts)
             except B.RMSNormError:
                 continue
-            s, _, _, _ = pb.timed(opts, K, 3)
-            gbs = wl.algorithmic_bytes * K / s / 1e9
+            t = pb.timed(opts, K, 3, min_ms=100.0)
+            gbs = wl.algorithmic_bytes * t.steps / t.max_s / 1e9
             print(json.dumps({"ablation": name, "config": cfg, "gbs": round(gbs, 1),
                               "frac": round(gbs / peak, 4), "plan": plan}), flush=True)
         del pb

@@ -29,6 +29,20 @@ def test_traffic_needs_matching_kernel_sources_and_plan(tmp_path):
     assert bench.load_traffic("missing", PLAN, d) is None
 
 
+def test_traffic_file_with_one_entry_per_launch_plan(tmp_path):
+    # Both launch modes of one workload in one summary: each plan finds its own figure.
+    strict = dict(PLAN, variant="warp", grid=760, lanes_per_row=32, vecs_per_lane=2,
+                  rows_per_stage=0, stages=1, smem_bytes=2048)
+    (tmp_path / "traffic_w.md").write_text(
+        f"## early\nkernel_hash: `{bench.kernel_hash('tma')}`\nplan: `{json.dumps(PLAN)}`\n"
+        f"traffic_bytes_per_launch: `111`\n\n## strict\nkernel_hash: `{bench.kernel_hash('warp')}`\n"
+        f"plan: `{json.dumps(strict)}`\ntraffic_bytes_per_launch: `222`\n")
+    d = str(tmp_path)
+    assert bench.load_traffic("w", PLAN, d) == 111
+    assert bench.load_traffic("w", strict, d) == 222
+    assert bench.load_traffic("w", dict(strict, grid=608), d) is None
+
+
 def test_variant_hashes_cover_their_own_sources():
     assert len({bench.kernel_hash(v) for v in bench.VARIANT_SOURCES}) == len(bench.VARIANT_SOURCES)
     assert bench.kernel_hash("tma") != bench.kernel_hash()
