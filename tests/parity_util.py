@@ -190,6 +190,50 @@ def oracle_rows(x_bits, w_bits, eps, offset, dtype, rows=None, want_y64=False):
     return oracle.rmsnorm_fwd(xs, w_bits, eps, offset, dtype, want_y64=want_y64)
 
 
+def oracle_threaded(x_bits, w_bits, eps, offset, dtype, threads: int | None = None):
+    """The oracle on every row, the rows split into contiguous blocks over host
+    threads (ctypes releases the GIL during each C call). Same result as
+    ``oracle.rmsnorm_fwd`` on the whole array: each row is computed alone."""
+    import os
+    import threading
+    x_bits = np.ascontiguousarray(x_bits, dtype=oracle.bits_dtype(dtype))
+    w_bits = np.ascontiguousarray(w_bits, dtype=oracle.bits_dtype(dtype))
+    M, N = x_bits.shape
+    y = np.empty((M, N), dtype=oracle.bits_dtype(dtype))
+    r = np.empty(M, dtype=np.float64)
+    n = max(1, min(threads or os.cpu_count() or 1, M))
+    bounds = [M * i // n for i in range(n + 1)]
+    oracle.lib()
+    ts = [threading.Thread(target=oracle.rmsnorm_fwd_into,
+                           args=(x_bits, w_bits, y, r, eps, offset, dtype, bounds[i], bounds[i + 1]))
+          for i in range(n) if bounds[i + 1] > bounds[i]]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    return y, r
+
+
+def compare_blocked(y_gpu, rstd_gpu, y_ref, rstd_ref, dtype, where="", block_elems=1 << 24):
+    """``compare`` over blocks of rows (bounded temporaries for GiB-sized
+    outputs). Returns (max ulp, max rstd rel err, {ulp distance: count})."""
+    M, N = y_ref.shape
+    rows = max(1, block_elems // N)
+    max_ulp, max_rel, hist = 0, 0.0, {}
+    for r0 in range(0, M, rows):
+        r1 = min(M, r0 + rows)
+        u, e = compare(y_gpu[r0:r1], rstd_gpu[r0:r1], y_ref[r0:r1], rstd_ref[r0:r1], dtype,
+                       where=f"{where} rows {r0}..{r1 - 1}")
+        d = np.abs(ordinal(np.asarray(y_gpu[r0:r1], dtype=np.uint16))
+                   - ordinal(np.asarray(y_ref[r0:r1], dtype=np.uint16)))
+        d[is_nan(np.asarray(y_gpu[r0:r1], dtype=np.uint16), dtype)] = 0
+        for k, c in enumerate(np.bincount(d.ravel())):
+            if c:
+                hist[k] = hist.get(k, 0) + int(c)
+        max_ulp, max_rel = max(max_ulp, u), max(max_rel, e)
+    return max_ulp, max_rel, hist
+
+
 def sample_rows(M: int, k: int, seed: int = 0) -> np.ndarray:
     """First, last and k random rows (sorted, unique)."""
     rng = np.random.default_rng(seed)

@@ -17,7 +17,8 @@ import torch
 import oracle
 from memory_bound_normalization_fwd_gb300 import binding as B
 from memory_bound_normalization_fwd_gb300 import workloads as W
-from parity_util import DeviceCase, compare, oracle_rows, sample_rows, DT
+from parity_util import (DT, DeviceCase, compare, compare_blocked, oracle_rows,
+                         oracle_threaded, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,14 +47,27 @@ def _run_and_check(x, w, dtype, eps, offset, rows=None, x_shift=0, y_shift=0, in
 
 # ---------------------------------------------------------------- full-size workloads
 
-@pytest.mark.parametrize("early", [False, True], ids=["strict", "early_loads"])
+_ORACLE_CACHE: dict = {}
+
+
+def _full_oracle(name):
+    """Inputs and the oracle's y and rstd on every row of a named workload
+    (computed once per test session, threaded over the host cores)."""
+    if name not in _ORACLE_CACHE:
+        wl = W.WORKLOADS[name]
+        x, w = W.generate(wl)
+        _ORACLE_CACHE[name] = (x, w) + oracle_threaded(x, w, wl.eps, wl.offset, wl.dtype)
+    return _ORACLE_CACHE[name]
+
+
 @pytest.mark.parametrize("name", list(W.WORKLOADS))
-def test_workload_full_size_automatic_launch(name, early):
-    # The automatic plan, in both launch modes bench.py times (early loads is the
-    # headline mode: two back-to-back calls, the second overlapping the first).
+@pytest.mark.parametrize("early", [False, True], ids=["strict", "early_loads"])
+def test_workload_full_size_automatic_launch(name, early, parity_report):
+    # The automatic plan, in both launch modes bench.py times (early loads: two
+    # back-to-back calls, the second overlapping the first), compared with the
+    # oracle on every element of every row.
     wl = W.WORKLOADS[name]
-    x, w = W.generate(wl)
-    rows = None if wl.M * wl.N <= (1 << 23) else sample_rows(wl.M, 192, seed=1)
+    x, w, yo, ro = _full_oracle(name)
     case = DeviceCase(x, w, wl.dtype)
     for _ in range(2 if early else 1):
         assert case.run(wl.eps, wl.offset, early_loads=early) == 0, B.rmsnorm_last_error()
@@ -63,10 +77,12 @@ def test_workload_full_size_automatic_launch(name, early):
     assert np.all(np.isfinite(r)) and np.all(r > 0)
     exp_mask = 0x7F80 if wl.dtype == "bf16" else 0x7C00
     assert not np.any((y & exp_mask) == exp_mask), "non-finite y"
-    yo, ro = oracle_rows(x, w, wl.eps, wl.offset, wl.dtype, rows)
-    if rows is not None:
-        y, r = y[rows], r[rows]
-    compare(y, r, yo, ro, wl.dtype, where=name)
+    max_ulp, max_rel, hist = compare_blocked(y, r, yo, ro, wl.dtype, where=name)
+    plan = _plan(wl.M, wl.N, wl.dtype, case, early_loads=early)
+    parity_report.append(
+        f"{name} [{'early loads' if early else 'strict'}, {plan['variant']}]: {wl.M} rows x "
+        f"{wl.N} compared, max ulp {max_ulp} (" +
+        ", ".join(f"{k}: {v}" for k, v in sorted(hist.items())) + f"), max rstd rel err {max_rel:.3g}")
     if wl.dtype == "fp16":
         assert abs(float(np.mean(r)) * wl.x_std - 1.0) < 0.01  # rstd ~ 1/64
 

@@ -103,3 +103,19 @@ def test_no_alloc_refuses_rows_longer_than_its_scratch():
     assert rc == -11 and "scratch" in B.rmsnorm_last_error()
     torch.cuda.synchronize()
     assert torch.all(dwd == 5.0)
+
+
+@pytest.mark.parametrize("dtype,N", [("bf16", 512), ("fp16", 1000), ("fp32", 8192)])
+def test_no_alloc_with_no_rows_writes_zero_dw(dtype, N):
+    # M = 0: no row kernel runs and nothing touches the scratch; the reduction
+    # over zero partial rows must still write dw = 0 (NaN before the call),
+    # on two calls in a row. x, dy, dx and rstd may be NULL when there are no rows.
+    wd = W.to_torch(W.generate(W.custom(1, N, dtype, seed=N))[1], dtype).cuda()
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):
+        dw = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+        rc = B.rmsnorm_bwd_noalloc(0, wd.data_ptr(), 0, 0, 0, dw.data_ptr(), 0, N, 1.0, DT[dtype],
+                                   None, s)
+        assert rc == 0, B.rmsnorm_last_error()
+        torch.cuda.synchronize()
+        assert torch.all(dw == 0.0)
