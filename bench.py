@@ -66,6 +66,8 @@ def parse_args(argv=None):
     p.add_argument("--blocked", action="store_true", help="contiguous row block per CTA")
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--cluster-size", type=int, default=0)
+    p.add_argument("--l2-prefetch", type=int, default=0,
+                   help="L2 prefetch distance (rmsnorm_options_t.l2_prefetch; 0 = planner's choice)")
     p.add_argument("--ablation", action="store_true",
                    help="time a matrix of kernel variants and knobs per workload, one JSON line each")
     p.add_argument("--backward", action="store_true",
@@ -131,7 +133,7 @@ def kernel_hash(variant: str | None = None) -> str:
 
 
 PLAN_KEYS = ("variant", "threads", "grid", "lanes_per_row", "vecs_per_lane", "rows_per_stage",
-             "stages", "smem_bytes", "cluster_size")
+             "stages", "smem_bytes", "cluster_size", "l2_prefetch")
 
 
 def load_traffic(workload: str, plan: dict, profiles_dir: str | None = None):
@@ -258,10 +260,11 @@ class PoolBench:
         """Time K steps as the GPU runs them, at any K.
 
         Exactly K calls (rotating through the pool) are captured into one CUDA
-        graph. After Wm untimed direct calls and untimed replays of the graph,
-        the timed region is R back-to-back replays of that graph between two
-        CUDA events on the launching stream, R chosen (the same on every rank)
-        so that the region lasts at least ``min_ms``; the per-step time is the
+        graph (several such graphs over successive slices of the pool when it
+        holds more than K buffer sets). After Wm untimed direct calls and untimed
+        replays, the timed region is R back-to-back replays between two CUDA
+        events on the launching stream, R chosen (the same on every rank) so
+        that the region lasts at least ``min_ms``; the per-step time is the
         region's time over R*K. A timed region of direct host calls would time
         the host's launch rate instead of the kernels."""
         import torch
@@ -270,24 +273,33 @@ class PoolBench:
             for k in range(max(3, min(Wm, 64))):
                 step(k)
         stream.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
-            for k in range(K):
-                step(k)
+        # When the pool holds more buffer sets than K, one graph of K calls would
+        # cycle through only K of them (and a small workload would then stay in
+        # L2): graphs g = 0, 1, ... each take the next K sets, and replays go
+        # round-robin over them, so consecutive replays still walk the whole pool.
+        n_graphs = max(1, -(-self.pool // K))
+        graphs = []
+        for g in range(n_graphs):
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+                for k in range(K):
+                    step(g * K + k)
+            graphs.append(graph)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
-            for _ in range(max(1, -(-Wm // K))):
-                graph.replay()
+            for r in range(max(n_graphs, -(-Wm // K))):
+                graphs[r % n_graphs].replay()
         torch.cuda.synchronize()
         # Replays per timed region, from one timed probe replay (max over ranks,
-        # so every rank runs the same count).
+        # so every rank runs the same count), rounded up to whole pool cycles.
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             a.record(stream)
-            graph.replay()
+            graphs[0].replay()
             b.record(stream)
         torch.cuda.synchronize()
         reps = int(max_over_ranks(float(max(1, -(-min_ms // max(a.elapsed_time(b), 1e-3))))))
+        reps = -(-reps // n_graphs) * n_graphs
         barrier()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
@@ -299,8 +311,8 @@ class PoolBench:
             barrier()
             with torch.cuda.stream(stream):
                 start.record(stream)
-                for _ in range(reps):
-                    graph.replay()
+                for r in range(reps):
+                    graphs[r % n_graphs].replay()
                 end.record(stream)
             torch.cuda.synchronize()
             barrier()
@@ -309,8 +321,10 @@ class PoolBench:
                 sampler.__exit__(None, None, None)
         ms = start.elapsed_time(end)
         steps = reps * K
-        launch = (f"CUDA graph of {K} ABI calls (rotating the pool), {reps} replays back to back "
-                  f"in the timed region ({steps} steps)")
+        launch = (f"CUDA graph of {K} ABI calls (rotating the pool"
+                  + (f"; {n_graphs} such graphs over successive pool slices, replayed in turn"
+                     if n_graphs > 1 else "")
+                  + f"), {reps} replays back to back in the timed region ({steps} steps)")
         return Timed(max_over_ranks(ms / 1e3), steps, ms / 1e3 / steps,
                      sampler.summary() if sampler else None, launch, reps)
 
@@ -462,7 +476,7 @@ def bench_ours(args, wl, rank, world, local_rank):
                               stages=args.stages, rows_per_stage=args.rows_per_stage,
                               max_ctas=args.max_ctas, early_loads=early, blocked=args.blocked,
                               pdl=not args.no_pdl, cluster_size=args.cluster_size,
-                              early_weights=early_weights)
+                              early_weights=early_weights, l2_prefetch=args.l2_prefetch)
 
     # Main measurement. The steps are independent batches (x and w are written
     # by no step), which meets the precondition of RMSNORM_FLAG_EARLY_LOADS:
@@ -627,9 +641,9 @@ def bench_ours(args, wl, rank, world, local_rank):
                    "note": "separately timed windows after the timed region; value is the timed region"},
         "timed_region": {"steps": main.steps, "graph_replays": main.replays,
                          "seconds": round(main.max_s, 6),
-                         "note": f"the --steps {K} ABI calls captured once as a CUDA graph and "
-                                 f"replayed {main.replays} times back to back between CUDA events; "
-                                 "ms_per_step = region time / steps run"},
+                         "note": f"the --steps {K} ABI calls captured as a CUDA graph and "
+                                 f"replayed {main.replays} times back to back between CUDA events "
+                                 "(see config.launch); ms_per_step = region time / steps run"},
         "gpu_launches": main.steps,  # one kernel per rmsnorm_fwd_ex call
         "clocks": main.clocks,
     }
@@ -769,7 +783,7 @@ def bench_backward(args, wl):
     rs = [r0.clone() for _ in range(pool)]
     dw = torch.empty(wl.N, dtype=torch.float32, device=dev)
     opts = B.make_options(variant=args.variant, max_ctas=args.max_ctas,
-                          lanes_per_row=args.lanes_per_row)
+                          lanes_per_row=args.lanes_per_row, l2_prefetch=args.l2_prefetch)
     nbytes = B.rmsnorm_bwd_workspace_size(wl.M, wl.N, dcode, opts)
     ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
@@ -810,6 +824,7 @@ def bench_backward(args, wl):
     return {"backward": wl.name, "value": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak, 4),
             "steps": K, "ms_per_step": round(sec * 1e3 / K, 5), "bytes_per_step": step_bytes,
             "workspace_bytes": nbytes, "variant": args.variant, "max_ctas": args.max_ctas,
+            "l2_prefetch": args.l2_prefetch,
             "l2": f"rotating pool of {pool} sets ({pool * set_bytes / 1e6:.0f} MB) > 3x L2"}
 
 

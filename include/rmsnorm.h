@@ -154,6 +154,15 @@ typedef struct rmsnorm_options {
     int32_t flags;           /* RMSNORM_FLAG_* bits */
     int32_t cluster_size;    /* CLUSTER: CTAs per row (2..16); 0 = planner's choice */
     int64_t wait_limit_ns;   /* TMA: bound on each mbarrier wait in ns; 0 = 1 second */
+    int32_t l2_prefetch;     /* WARP and TMA: L2 prefetch distance (a hint: cp.async.bulk.
+                                prefetch.L2, no effect on results). WARP: each team asks
+                                for its rows this many passes past the ones held in
+                                registers to be brought into L2; TMA: each CTA, for this
+                                many chunks past its ring's stages (packed rows only).
+                                rmsnorm_bwd's warp kernel: the rows this many passes
+                                ahead go to L2 instead of the next row to registers.
+                                1..15; 0 = planner's choice; -1 = none */
+    int32_t reserved;        /* must be 0 */
 } rmsnorm_options_t;
 
 /* What the planner picked (rmsnorm_plan_info). */
@@ -169,6 +178,7 @@ typedef struct rmsnorm_plan {
     int32_t ctas_per_sm;     /* resident CTAs per SM (occupancy calculator) */
     int32_t sm_count;        /* SMs on the device */
     int32_t cluster_size;    /* CTAs per cluster (cluster variant; else 0) */
+    int32_t l2_prefetch;     /* L2 prefetch distance in use (WARP, TMA; 0 = none) */
 } rmsnorm_plan_t;
 
 /*

@@ -119,6 +119,7 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
                     o->variant);
     if (o->max_ctas < 0 || o->lanes_per_row < 0 || o->rows_per_stage < 0 || o->stages < 0 ||
         o->stages > 8 || o->wait_limit_ns < 0 || o->cluster_size < 0 || o->cluster_size > 16 ||
+        o->l2_prefetch < -1 || o->l2_prefetch > kMaxPrefetch || o->reserved != 0 ||
         (o->flags & ~(RMSNORM_FLAG_NO_PDL | RMSNORM_FLAG_BLOCKED_ROWS | RMSNORM_FLAG_EARLY_LOADS |
                       RMSNORM_FLAG_HOST_DIRECT | RMSNORM_FLAG_EARLY_WEIGHTS |
                       RMSNORM_FLAG_BULK_STORE)) != 0)
@@ -131,6 +132,7 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
     k->rows_per_stage = o->rows_per_stage;
     k->wait_limit_ns = o->wait_limit_ns;
     k->cluster_size = o->cluster_size;
+    k->l2_prefetch = o->l2_prefetch;
     return RMSNORM_OK;
 }
 
@@ -488,6 +490,7 @@ extern "C" int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x,
     out->ctas_per_sm = l.ctas_per_sm;
     out->sm_count = d.sm_count;
     out->cluster_size = l.cluster;
+    out->l2_prefetch = l.prefetch;
     return RMSNORM_OK;
 }
 

@@ -72,6 +72,14 @@ static __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Asks for `bytes` of global memory at `src` to be brought into L2 (a hint:
+// nothing lands in shared memory or registers and there is no completion to
+// wait for). `src` 16-byte aligned, `bytes` a multiple of 16. A later load of
+// those lines then meets L2 latency instead of DRAM latency.
+static __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 static __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(

@@ -15,6 +15,7 @@
 // Kernel 2 sums the partials over CTAs in a fixed order (deterministic) into dw.
 // The general kernel takes any N and alignment with element accesses; its dw
 // partial sits in shared memory, or in its workspace row for very long rows.
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -117,17 +118,51 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 // vectors v * 32 + l. At the end the 8 warps' dw contributions meet in shared
 // memory (summed in warp order) and the CTA writes one partial row, so the
 // number of partial rows is the grid, not the row count.
-template <int DT, int V>
+//
+// Rows ahead: with P == 0 each warp loads its next row's x, dy and rstd into
+// registers before reducing the current one (one row in flight ahead: 3.84 ->
+// 3.98 TB/s at 16384x512). With P > 0 (the L2 prefetch distance, mode bits)
+// the registers hold only the current row, and lane 0 instead asks for the x
+// and dy rows P passes ahead to be brought into L2 (cp.async.bulk.prefetch),
+// which frees the registers of the second row.
+template <int DT, int V, bool REGS_AHEAD>
 __global__ void __launch_bounds__(256)
 bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __restrict__ rstd,
                 const uint4* dy, uint4* dx, float* __restrict__ partial, int64_t M, int nvec,
-                float n, float offset) {
+                float n, float offset, int mode) {
     constexpr int E = VecElems<DT>::value;  // elements per 16-byte vector
     extern __shared__ float4 sw[];  // (offset + w): N floats; then 8 x N floats of dw
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int wid = tid >> 5;
+    const int P = REGS_AHEAD ? 0 : mode_prefetch(mode);
+    const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * 8;
+    int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + wid;
+    auto load = [&](int64_t rw, uint4* xv, uint4* gv, float& r) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * 32 + lane;
+            xv[v] = gv[v] = make_uint4(0u, 0u, 0u, 0u);
+            if (rw < M && c < nvec) {
+                xv[v] = ld_stream(x + rw * nvec + c);
+                gv[v] = ld_stream(dy + rw * nvec + c);
+            }
+        }
+        r = rw < M ? __ldg(rstd + rw) : 0.f;
+    };
+    auto prefetch = [&](int64_t rw) {
+        if (lane == 0 && rw < M) {
+            bulk_prefetch_l2(x + rw * nvec, row_bytes);
+            bulk_prefetch_l2(dy + rw * nvec, row_bytes);
+        }
+    };
     pdl_wait();
+    // The first row's loads (and prefetches) go out before the weights are read.
+    uint4 xv[V], gv[V];
+    float r;
+    load(row, xv, gv, r);
+    for (int p = 1; p <= P; ++p) prefetch(row + p * stride);
     pdl_launch_dependents();
     for (int i = tid; i < nvec; i += 256) weights_vec_to_smem<DT>(__ldg(w + i), offset, sw, i);
     __syncthreads();
@@ -137,30 +172,14 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
 
-    // Each warp walks its rows with the next row's x, dy and rstd loaded before
-    // the current row is reduced (one row in flight ahead: measured 3.84 TB/s
-    // at 16384x512 without it).
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * 8;
-    auto load = [&](int64_t row, uint4* xv, uint4* gv, float& r) {
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-            const int c = v * 32 + lane;
-            xv[v] = gv[v] = make_uint4(0u, 0u, 0u, 0u);
-            if (row < M && c < nvec) {
-                xv[v] = ld_stream(x + row * nvec + c);
-                gv[v] = ld_stream(dy + row * nvec + c);
-            }
-        }
-        r = row < M ? __ldg(rstd + row) : 0.f;
-    };
-    uint4 xv[V], gv[V];
-    float r;
-    int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + wid;
-    load(row, xv, gv, r);
     for (; row < M; row += stride) {
         uint4 xn[V], gn[V];
-        float rn;
-        load(row + stride, xn, gn, rn);
+        float rn = 0.f;
+        if constexpr (REGS_AHEAD) {
+            load(row + stride, xn, gn, rn);
+        } else {
+            prefetch(row + (P + 1) * stride);
+        }
         float cs = 0.f;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
@@ -191,9 +210,13 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
             }
             st_stream(dx + row * nvec + c, pack_vec<DT>(o));
         }
+        if constexpr (REGS_AHEAD) {
 #pragma unroll
-        for (int v = 0; v < V; ++v) xv[v] = xn[v], gv[v] = gn[v];
-        r = rn;
+            for (int v = 0; v < V; ++v) xv[v] = xn[v], gv[v] = gn[v];
+            r = rn;
+        } else {
+            load(row + stride, xv, gv, r);
+        }
     }
 
     float* red = reinterpret_cast<float*>(sw + nvec * (E / 4));  // [8][N]
@@ -364,6 +387,14 @@ bool reduce_narrow(int64_t N, int G, int dtype) {
 
 using VecFn = void (*)(const uint4*, const uint4*, const float*, const uint4*, uint4*, float*,
                        int64_t, int, float, float);
+using WarpFn = void (*)(const uint4*, const uint4*, const float*, const uint4*, uint4*, float*,
+                        int64_t, int, float, float, int);
+
+template <int DT, bool REGS_AHEAD>
+WarpFn pick_warp(int V) {
+    return V == 1 ? bwd_warp_kernel<DT, 1, REGS_AHEAD>
+                  : V == 2 ? bwd_warp_kernel<DT, 2, REGS_AHEAD> : bwd_warp_kernel<DT, 4, REGS_AHEAD>;
+}
 using GenFn = void (*)(const void*, const void*, const float*, const void*, void*, float*,
                        int64_t, int64_t, float, float);
 
@@ -399,14 +430,17 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
                      aligned16(a.dy) && aligned16(a.dx);
     if ((variant == 0 || variant == 1) && vec && nvec <= 128) {
         const int V = nvec <= 32 ? 1 : nvec <= 64 ? 2 : 4;
-        VecFn fn = nullptr;
+        const int P = k.l2_prefetch > 0 ? k.l2_prefetch : 0;
+        WarpFn fn = nullptr;
         if (a.dtype == kBF16)
-            fn = V == 1 ? bwd_warp_kernel<kBF16, 1> : V == 2 ? bwd_warp_kernel<kBF16, 2> : bwd_warp_kernel<kBF16, 4>;
+            fn = P > 0 ? pick_warp<kBF16, false>(V) : pick_warp<kBF16, true>(V);
         else if (a.dtype == kFP16)
-            fn = V == 1 ? bwd_warp_kernel<kFP16, 1> : V == 2 ? bwd_warp_kernel<kFP16, 2> : bwd_warp_kernel<kFP16, 4>;
+            fn = P > 0 ? pick_warp<kFP16, false>(V) : pick_warp<kFP16, true>(V);
         else
-            fn = V == 1 ? bwd_warp_kernel<kFP32, 1> : V == 2 ? bwd_warp_kernel<kFP32, 2> : bwd_warp_kernel<kFP32, 4>;
+            fn = P > 0 ? pick_warp<kFP32, false>(V) : pick_warp<kFP32, true>(V);
         l.kernel = reinterpret_cast<const void*>(fn);
+        l.prefetch = P;
+        l.bwd_warp = true;
         l.threads = 256;
         l.lanes_per_row = 32;
         l.vecs_per_lane = V;
@@ -480,7 +514,14 @@ cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial) {
     if (a.M > 0) {
         LaunchCfg c(l, a.stream, l.pdl);
         cudaError_t e;
-        if (l.vecs_per_lane > 0) {  // the vector kernel (the general one has none)
+        if (l.bwd_warp) {
+            WarpFn fn = reinterpret_cast<WarpFn>(const_cast<void*>(l.kernel));
+            e = cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
+                                   static_cast<const uint4*>(a.w), a.rstd,
+                                   static_cast<const uint4*>(a.dy), static_cast<uint4*>(a.dx),
+                                   partial, a.M, static_cast<int>(a.N / vec_elems(a.dtype)),
+                                   static_cast<float>(a.N), a.offset, l.mode());
+        } else if (l.vecs_per_lane > 0) {  // the CTA-per-row vector kernel
             VecFn fn = reinterpret_cast<VecFn>(const_cast<void*>(l.kernel));
             e = cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                                    static_cast<const uint4*>(a.w), a.rstd,

@@ -99,22 +99,8 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         for (int st = 0; st < stages; ++st) mbar_init(bars + 8 * st, 1);
         fence_mbar_init();
     }
-    // No global memory is touched before the previous kernel completes, unless the
-    // caller promised w (early weights) or x and w (early loads) are not being
-    // written: then those reads go first and only the rest waits.
-    if (!early && !early_w) pdl_wait();
-    float s[V][VecElems<DT>::value];
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-        const int c = v * TEAM + t;
-        uint4 wv = make_uint4(0u, 0u, 0u, 0u);
-        if (c < nvec) wv = __ldg(w + c);
-        weights_vec<DT>(wv, offset, s[v]);
-    }
-    __syncthreads();
-    if (early_w && !early) pdl_wait();  // x only after the previous kernel completes
-
-    // Local chunk k goes to stage k % stages.
+    // Local chunk k goes to stage k % stages (issued by thread 0 alone, in
+    // increasing order).
     auto issue = [&](int64_t k) {
         if (k >= nchunks) return;
         const int st = static_cast<int>(k % stages);
@@ -125,15 +111,41 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         mbar_arrive_expect_tx(bars + 8 * st, static_cast<uint32_t>(rows) * row_bytes);
         if (CONTIG) {  // contiguous rows: the whole stage is one span of x
             bulk_g2s(dst, x + r0 * nvec, static_cast<uint32_t>(rows) * row_bytes, bars + 8 * st);
+            // L2 prefetch of the chunk P issues ahead (chunks below `stages` are
+            // the ring's first loads, so each later chunk is asked for once).
+            const int64_t kp = k + mode_prefetch(mode);
+            if (kp > k && kp >= stages && kp < nchunks) {
+                const int64_t rp = chunk_row(kp);
+                const int64_t nrp = (r_end - rp) < R ? (r_end - rp) : R;
+                bulk_prefetch_l2(x + rp * nvec, static_cast<uint32_t>(nrp) * row_bytes);
+            }
         } else {       // strided rows: one copy per row, all counted on the same barrier
             for (int64_t q = 0; q < rows; ++q)
                 bulk_g2s(dst + static_cast<uint32_t>(q) * row_bytes, x + (r0 + q) * ldx, row_bytes,
                          bars + 8 * st);
         }
     };
+    // No global memory is touched before the previous kernel completes, unless the
+    // caller promised w (early weights) or x and w (early loads) are not being
+    // written: then those reads go first and only the rest waits. The weight
+    // loads are issued, then the first stages' copies, and only then are the
+    // weights converted, so the weights' L2 round trip hides under the copies.
+    if (!early && !early_w) pdl_wait();
+    uint4 wv[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * TEAM + t;
+        wv[v] = make_uint4(0u, 0u, 0u, 0u);
+        if (c < nvec) wv[v] = __ldg(w + c);
+    }
+    if (early_w && !early) pdl_wait();  // early weights only: w before the wait, x after it
     if (tid == 0) {
         for (int k = 0; k < stages; ++k) issue(k);
     }
+    float s[V][VecElems<DT>::value];
+#pragma unroll
+    for (int v = 0; v < V; ++v) weights_vec<DT>(wv[v], offset, s[v]);
+    __syncthreads();  // the barriers' initialisation is visible to every thread
     pdl_launch_dependents();
     if (early) pdl_wait();
 
@@ -222,9 +234,15 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
 
     if (aborted && tid == 0) {
         atomicOr(&g_status, 1u);
-        // Copies for local tiles k .. k + stages - 1 may still be in flight into
-        // this CTA's shared memory: wait for them before the CTA retires.
-        for (int64_t j = k; j < k + stages && j < nchunks; ++j) {
+        // Copies for the local chunks from k up to the last one issued may still
+        // be in flight into this CTA's shared memory: wait for them before the
+        // CTA retires. Chunks below k + stages are issued by the time chunk k is
+        // awaited, except with bulk stores and more than two stages, where the
+        // refill lags one stage (iteration j >= 1 issues chunk j - 1 + stages),
+        // so only chunks below k - 1 + stages are, once k >= 1. (A counter of
+        // issued chunks would cost registers in the consumer loop.)
+        const int64_t issued_end = k + stages - ((BULK_ST && stages > 2 && k >= 1) ? 1 : 0);
+        for (int64_t j = k; j < issued_end && j < nchunks; ++j) {
             mbar_wait_bounded(bars + 8 * static_cast<int>(j % stages),
                               static_cast<uint32_t>((j / stages) & 1), drain_cycles);
         }
@@ -355,6 +373,7 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     l.work_items = (a.M + R - 1) / R;
     l.grid = persistent_grid(l.work_items, 1, d.sm_count, l.ctas_per_sm, k.max_ctas);
     l.wait_limit_ns = k.wait_limit_ns > 0 ? k.wait_limit_ns : 1000000000LL;
+    l.prefetch = (contig && k.l2_prefetch > 0) ? k.l2_prefetch : 0;
     return true;
 }
 

@@ -18,6 +18,7 @@
 // one row (D = 1): on GB300 the registers a deeper ring costs are worth more
 // as resident warps (measured: 16384x512 bf16, 4650 GB/s at D = 1 against
 // 4380 at D = 2 and 3860 at D = 4).
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -26,8 +27,16 @@ namespace {
 
 constexpr int kWarps = 8;  // 256 threads per CTA
 
+// Resident CTAs per SM the register budget must allow. Teams holding at most
+// two vectors per lane with one row in flight fit six 256-thread CTAs per SM
+// (at most 40 registers, no spills: 48 warps in flight instead of 40 at the
+// uncapped 43-47); four-vector teams would spill at that cap and keep the
+// compiler's own count.
+template <int V, int D>
+constexpr int kMinCtas = (V <= 2 && D == 1) ? 6 : 1;
+
 template <int DT, int G, int V, int D>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, kMinCtas<V, D>)
 warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
                  int64_t M, int nvec, int64_t ldx, int64_t ldy, float n, float eps, float offset,
                  int mode) {
@@ -56,23 +65,51 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
         stride = static_cast<int64_t>(gridDim.x) * kPass;
     }
 
+    // The first D rows' loads go out before the weights are read whenever x may
+    // be read at that point (strict order after the wait, or early loads), so
+    // the weights' L2 round trip hides under them. With early weights only, w
+    // is read before the wait and x after it.
+    uint4 buf[D][V];
+    auto load_first = [&]() {
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+            const int64_t row = first0 + d * stride + team;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const int c = v * G + sub;
+                buf[d][v] = make_uint4(0u, 0u, 0u, 0u);
+                if (row < r_end && c < nvec) buf[d][v] = ld_stream(x + row * ldx + c);
+            }
+        }
+    };
+    // L2 prefetch (distance P passes): right after its first loads, the team's
+    // first lane asks for its rows D .. D + P - 1 passes ahead to be brought
+    // into L2, and later, each time a slot is refilled, for the row P passes
+    // past the refill, so rows come from L2 when their turn in registers comes.
+    const int P = mode_prefetch(mode);
+    const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
+    auto prefetch_first = [&]() {
+        if (P > 0 && sub == 0) {
+            for (int p = D; p < D + P; ++p) {
+                const int64_t prow = first0 + p * stride + team;
+                if (prow < r_end) bulk_prefetch_l2(x + prow * ldx, row_bytes);
+            }
+        }
+    };
+    const bool x_first = early || !early_w;
     if (!early && !early_w) pdl_wait();
+    if (x_first) {
+        load_first();
+        prefetch_first();
+    }
     for (int i = threadIdx.x; i < nvec; i += kWarps * 32)
         weights_vec_to_smem<DT>(__ldg(w + i), offset, sw, i);
     __syncthreads();
     pdl_launch_dependents();
-    if (early_w && !early) pdl_wait();  // x only after the previous kernel completes
-
-    uint4 buf[D][V];
-#pragma unroll
-    for (int d = 0; d < D; ++d) {
-        const int64_t row = first0 + d * stride + team;
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-            const int c = v * G + sub;
-            buf[d][v] = make_uint4(0u, 0u, 0u, 0u);
-            if (row < r_end && c < nvec) buf[d][v] = ld_stream(x + row * ldx + c);
-        }
+    if (!x_first) {
+        pdl_wait();  // x only after the previous kernel completes
+        load_first();
+        prefetch_first();
     }
     if (early) pdl_wait();  // every store comes after the previous kernel completes
 
@@ -101,6 +138,10 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
                     }
                 }
                 const int64_t nrow = row + D * stride;
+                if (P > 0 && sub == 0) {
+                    const int64_t prow = nrow + P * stride;
+                    if (prow < r_end) bulk_prefetch_l2(x + prow * ldx, row_bytes);
+                }
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const int c = v * G + sub;
@@ -184,6 +225,21 @@ bool warp_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) 
     l.work_items = a.M;
     l.grid = persistent_grid(a.M, static_cast<int64_t>(kWarps) * (32 / G), d.sm_count,
                              l.ctas_per_sm, k.max_ctas);
+    // L2 prefetch: the caller's distance, or by default one pass ahead for
+    // whole-warp teams under strict stream order when each team walks at least
+    // two passes of rows (GB300, strict: 16384x512 bf16 4605 -> 4781 GB/s,
+    // 16384x768 bf16 4688 -> 5057, 16384x256 fp32 4908 -> 5153; teams of 4-8
+    // lanes, single-pass grids (2048x512) and early loads gain nothing or
+    // lose). Never for operands in host memory (host-direct calls).
+    const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) && !(k.flags & RMSNORM_FLAG_NO_PDL);
+    const int64_t pass_rows = static_cast<int64_t>(l.grid) * kWarps * (32 / G);
+    if (k.l2_prefetch > 0)
+        l.prefetch = k.l2_prefetch;
+    else if (k.l2_prefetch == 0 && G == 32 && !early && a.M >= 2 * pass_rows)
+        l.prefetch = 1;
+    else
+        l.prefetch = 0;
+    if (k.flags & kKnobNoBulkCopies) l.prefetch = 0;
     return true;
 }
 

@@ -33,6 +33,14 @@ inline int vec_elems(int dtype) { return 16 / elem_bytes(dtype); }
 constexpr int kModeBlocked = 1;     // one contiguous block of rows per CTA
 constexpr int kModeEarlyLoads = 2;  // first loads of x and w before the PDL wait (caller's promise)
 constexpr int kModeEarlyWeights = 4;  // w (not x) read before the PDL wait (caller's promise)
+// Bits 8..11: L2 prefetch distance (0 = none): WARP, how many row passes past
+// the ones in registers each team prefetches; TMA, how many chunks past the
+// ring's stages each CTA prefetches.
+constexpr int kModePrefetchShift = 8;
+constexpr int kMaxPrefetch = 15;
+__host__ __device__ inline int mode_prefetch(int mode) {
+    return (mode >> kModePrefetchShift) & kMaxPrefetch;
+}
 
 // A launch shape chosen by a variant's planner.
 struct Launch {
@@ -53,9 +61,11 @@ struct Launch {
     bool blocked = false;  // contiguous row block per CTA instead of strided passes
     bool early = false;    // x and w may be read before the previous kernel completes
     bool early_weights = false;  // w may be read before the previous kernel completes
+    int prefetch = 0;            // L2 prefetch distance (kModePrefetchShift); 0 = none
+    bool bwd_warp = false;       // backward: the warp-per-row kernel (takes a mode argument)
     int mode() const {
         return (blocked ? kModeBlocked : 0) | (early ? kModeEarlyLoads : 0) |
-               (early_weights ? kModeEarlyWeights : 0);
+               (early_weights ? kModeEarlyWeights : 0) | (prefetch << kModePrefetchShift);
     }
 };
 
@@ -72,6 +82,7 @@ struct Knobs {
     int rows_per_stage = 0;
     int cluster_size = 0;
     int64_t wait_limit_ns = 0;
+    int l2_prefetch = 0;  // -1 none, 0 planner's choice, 1..kMaxPrefetch distance
 };
 
 // Device facts, cached per device by the front end.

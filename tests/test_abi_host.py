@@ -51,7 +51,7 @@ def test_options_struct_layout_matches_header():
     body = re.search(r"typedef struct rmsnorm_options \{(.*?)\} rmsnorm_options_t;", text, re.S)
     fields = re.findall(r"int(32|64)_t\s+(\w+);", body.group(1))
     assert [n for _, n in fields] == [n for n, _ in B.Options._fields_]
-    assert ctypes.sizeof(B.Options) == 40
+    assert ctypes.sizeof(B.Options) == 48
     body = re.search(r"typedef struct rmsnorm_plan \{(.*?)\} rmsnorm_plan_t;", text, re.S)
     assert [n for n in re.findall(r"int32_t\s+(\w+);", body.group(1))] == \
         [n for n, _ in B.Plan._fields_]
@@ -131,7 +131,8 @@ def test_m_zero_is_ok_without_buffers(lib):
                                          ("stages", 9), ("stages", -1), ("wait_limit_ns", -5),
                                          ("lanes_per_row", -2), ("struct_size", 8),
                                          ("flags", 64), ("cluster_size", 17),
-                                         ("cluster_size", -1)])
+                                         ("cluster_size", -1), ("l2_prefetch", -2),
+                                         ("l2_prefetch", 16), ("reserved", 1)])
 def test_bad_options(lib, field, value):
     o = B.make_options()
     setattr(o, field, value)

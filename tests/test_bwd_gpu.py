@@ -181,3 +181,23 @@ def test_torch_convenience_forward_then_backward():
     got = oracle.decode("bf16", W.from_torch(dx))
     assert np.all(np.abs(got - dx64) <= _ulp("bf16", dx64) + 3e-5 * np.abs(dx64).max())
     assert np.allclose(dw.cpu().numpy(), dw64, rtol=1e-4, atol=1e-4 * np.abs(dw64).max())
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("M,N", [(37, 512), (300, 1000), (1000, 256), (130, 520), (3, 8)])
+@pytest.mark.parametrize("P", [1, 2, 7, 15])
+def test_bwd_warp_l2_prefetch(dtype, M, N, P):
+    # The warp kernel's L2-prefetch form (only the current row in registers,
+    # the rows P passes ahead asked for in L2): same tolerance, small grids so
+    # each warp walks many rows, and in place.
+    e = 4 if dtype == "fp32" else 8  # elements per 16-byte vector
+    if N % e or N // e > 128:
+        pytest.skip("the warp kernel takes rows of up to 128 vectors")
+    offset = float(N % 3 == 0)
+    x, w, dy, rstd = _inputs(M, N, dtype, seed=M + N + P, offset=offset)
+    for max_ctas in (0, 1, 3):
+        dx, dw = _run(x, w, dy, rstd, offset, dtype, variant="warp", max_ctas=max_ctas, l2_prefetch=P)
+        _check(x, w, dy, rstd, dx, dw, offset, dtype, where=f"P={P} {M}x{N} {max_ctas}")
+    dx, dw = _run(x, w, dy, rstd, offset, dtype, inplace="x", variant="warp", max_ctas=2,
+                  l2_prefetch=P)
+    _check(x, w, dy, rstd, dx, dw, offset, dtype, where=f"P={P} {M}x{N} in place")

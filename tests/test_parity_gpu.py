@@ -122,6 +122,29 @@ def test_warp_lanes_per_row_and_ring_depth(G, N, D):
                        stages=D, max_ctas=max_ctas, blocked=blocked, expect_variant="warp")
 
 
+@pytest.mark.parametrize("variant,G", [("warp", 32), ("warp", 16), ("warp", 8), ("tma", 0),
+                                       ("tma", 64)])
+@pytest.mark.parametrize("M,N", [(37, 512), (257, 1000), (1000, 256), (130, 520), (64, 4096)])
+@pytest.mark.parametrize("P", [1, 3, 15])
+def test_l2_prefetch_parity(variant, G, M, N, P):
+    # L2 prefetch of rows (warp) or chunks (TMA) ahead: a hint only, so the bits
+    # must not change. Strict order and early loads, strided and blocked rows,
+    # grids small enough that every team walks many rows, and in place.
+    if G and (N // 8 + G - 1) // G > 4:
+        pytest.skip("more than 4 vectors per lane")
+    wl = W.custom(M, N, "bf16", seed=M + N + P + G, offset=float(P % 2))
+    x, w = W.generate(wl)
+    for max_ctas, blocked, early in ((0, False, False), (1, False, True), (3, True, False),
+                                     (5, False, False)):
+        _run_and_check(x, w, "bf16", wl.eps, wl.offset, variant=variant, lanes_per_row=G,
+                       l2_prefetch=P, max_ctas=max_ctas, blocked=blocked, early_loads=early,
+                       expect_variant=variant)
+    _run_and_check(x, w, "bf16", wl.eps, wl.offset, inplace=True, variant=variant,
+                   lanes_per_row=G, l2_prefetch=P, max_ctas=2, expect_variant=variant)
+    plan = _plan(M, N, "bf16", variant=variant, lanes_per_row=G, l2_prefetch=P)
+    assert plan["l2_prefetch"] == P
+
+
 @pytest.mark.parametrize("T", [64, 128, 256, 512, 1024])
 @pytest.mark.parametrize("N", [512, 4096, 8192])
 def test_cta_threads(T, N):
