@@ -72,6 +72,10 @@ def parse_args(argv=None):
                    help="time a matrix of kernel variants and knobs per workload, one JSON line each")
     p.add_argument("--backward", action="store_true",
                    help="time the backward (dx, dw) on the workload instead of the forward")
+    p.add_argument("--launch-only", type=int, default=0, metavar="N",
+                   help="no timing: N direct calls of the planned forward over the rotating pool "
+                        "(early loads unless --strict-order), for profiler captures of steady-state "
+                        "launches; prints the plan")
     return p.parse_args(argv)
 
 
@@ -692,6 +696,36 @@ def per_workload(args, dev, peak: float) -> dict:
     return out
 
 
+def launch_only(args, wl) -> dict:
+    """N direct rmsnorm_fwd_ex calls over the rotating pool, the plan bench_ours
+    times for this workload and launch mode; nothing is timed."""
+    import torch
+    from memory_bound_normalization_fwd_gb300 import binding as B
+    from memory_bound_normalization_fwd_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    x_bits, w_bits = W.generate(wl)
+    pb = PoolBench(wl, x_bits, w_bits, dev)
+    opts = B.make_options(variant=args.variant, lanes_per_row=args.lanes_per_row,
+                          stages=args.stages, rows_per_stage=args.rows_per_stage,
+                          max_ctas=args.max_ctas, early_loads=not args.strict_order,
+                          blocked=args.blocked, pdl=not args.no_pdl,
+                          cluster_size=args.cluster_size, l2_prefetch=args.l2_prefetch)
+    plan = B.rmsnorm_plan_info(wl.M, wl.N, pb.dcode, pb.xs[0].data_ptr(), pb.w_dev.data_ptr(),
+                               pb.ys[0].data_ptr(), opts)
+    with torch.cuda.stream(pb.stream):
+        for k in range(args.launch_only):
+            i = k % pb.pool
+            rc = B.rmsnorm_fwd_ex(pb.xs[i].data_ptr(), pb.w_dev.data_ptr(), pb.ys[i].data_ptr(),
+                                  pb.rs[i].data_ptr(), wl.M, wl.N, wl.eps, wl.offset, pb.dcode,
+                                  opts, pb.stream.cuda_stream)
+            if rc != 0:
+                raise RuntimeError(B.rmsnorm_last_error())
+    torch.cuda.synchronize()
+    return {"launch_only": wl.name, "launches": args.launch_only, "pool_sets": pb.pool,
+            "launch_order": "strict" if args.strict_order else "early loads", "plan": plan,
+            "kernel_hash": kernel_hash(plan["variant"])}
+
+
 # ---------------------------------------------------------------- ablation matrix
 
 def ablation_configs(wl):
@@ -782,47 +816,58 @@ def bench_backward(args, wl):
     dxs = [torch.empty_like(x0) for _ in range(pool)]
     rs = [r0.clone() for _ in range(pool)]
     dw = torch.empty(wl.N, dtype=torch.float32, device=dev)
-    opts = B.make_options(variant=args.variant, max_ctas=args.max_ctas,
-                          lanes_per_row=args.lanes_per_row, l2_prefetch=args.l2_prefetch)
-    nbytes = B.rmsnorm_bwd_workspace_size(wl.M, wl.N, dcode, opts)
+
+    def make(early):
+        return B.make_options(variant=args.variant, max_ctas=args.max_ctas,
+                              lanes_per_row=args.lanes_per_row, l2_prefetch=args.l2_prefetch,
+                              early_loads=early)
+    nbytes = B.rmsnorm_bwd_workspace_size(wl.M, wl.N, dcode, make(False))
     ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
-
-    def step(k):
-        i = k % pool
-        rc = B.rmsnorm_bwd(xs[i].data_ptr(), w.data_ptr(), rs[i].data_ptr(), dys[i].data_ptr(),
-                           dxs[i].data_ptr(), dw.data_ptr(), wl.M, wl.N, wl.offset, dcode,
-                           ws.data_ptr(), ws.numel() * 4, opts, sh)
-        if rc != 0:
-            raise RuntimeError(B.rmsnorm_last_error())
-
-    with torch.cuda.stream(stream):
-        for k in range(8):
-            step(k)
-    torch.cuda.synchronize()
-    per = pool * max(1, 128 // pool)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
-        for k in range(per):
-            step(k)
-    K = max(per, args.steps // per * per)
-    with torch.cuda.stream(stream):
-        g.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a.record(stream)
-        for _ in range(K // per):
-            g.replay()
-        b.record(stream)
-    torch.cuda.synchronize()
-    sec = a.elapsed_time(b) / 1e3
     step_bytes = 3 * eb * wl.M * wl.N + 4 * wl.M + eb * wl.N + 4 * wl.N
     peak, _ = load_peaks()
-    gbs = step_bytes * K / sec / 1e9
+
+    def run(opts):
+        def step(k):
+            i = k % pool
+            rc = B.rmsnorm_bwd(xs[i].data_ptr(), w.data_ptr(), rs[i].data_ptr(), dys[i].data_ptr(),
+                               dxs[i].data_ptr(), dw.data_ptr(), wl.M, wl.N, wl.offset, dcode,
+                               ws.data_ptr(), ws.numel() * 4, opts, sh)
+            if rc != 0:
+                raise RuntimeError(B.rmsnorm_last_error())
+
+        with torch.cuda.stream(stream):
+            for k in range(8):
+                step(k)
+        torch.cuda.synchronize()
+        per = pool * max(1, 128 // pool)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for k in range(per):
+                step(k)
+        K = max(per, args.steps // per * per)
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(K // per):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        sec = a.elapsed_time(b) / 1e3
+        return step_bytes * K / sec / 1e9, K, sec
+
+    gbs, K, sec = run(make(False))
+    gbs_e, _, sec_e = run(make(True))
     return {"backward": wl.name, "value": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak, 4),
             "steps": K, "ms_per_step": round(sec * 1e3 / K, 5), "bytes_per_step": step_bytes,
+            "early_loads": {"value": round(gbs_e, 1), "frac": round(gbs_e / peak, 4),
+                            "ms_per_step": round(sec_e * 1e3 / K, 5),
+                            "note": "RMSNORM_FLAG_EARLY_LOADS: x, w and rstd of the first rows read "
+                                    "before the previous step completes (steps are independent)"},
             "workspace_bytes": nbytes, "variant": args.variant, "max_ctas": args.max_ctas,
             "l2_prefetch": args.l2_prefetch,
             "l2": f"rotating pool of {pool} sets ({pool * set_bytes / 1e6:.0f} MB) > 3x L2"}
@@ -875,6 +920,10 @@ def main(argv=None):
 
     if args.ablation:
         run_ablation(args, [args.workload] if args.workload else list(W.WORKLOADS))
+        return 0
+
+    if args.launch_only:
+        print(json.dumps(launch_only(args, wl)), flush=True)
         return 0
 
     if args.impl == "reference":

@@ -159,8 +159,7 @@ typedef struct rmsnorm_options {
                                 for its rows this many passes past the ones held in
                                 registers to be brought into L2; TMA: each CTA, for this
                                 many chunks past its ring's stages (packed rows only).
-                                rmsnorm_bwd's warp kernel: the rows this many passes
-                                ahead go to L2 instead of the next row to registers.
+                                Ignored by the other variants and by rmsnorm_bwd.
                                 1..15; 0 = planner's choice; -1 = none */
     int32_t reserved;        /* must be 0 */
 } rmsnorm_options_t;
@@ -285,7 +284,12 @@ int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void
  * up to about 56K columns and, past that, in its own row of the workspace (any
  * N; the grid is then capped so that the partial rows stay within 64 MB).
  * Options: variant AUTO, WARP, CTA or GENERIC, lanes_per_row (CTA: threads per
- * CTA), max_ctas, RMSNORM_FLAG_NO_PDL.
+ * CTA), max_ctas, RMSNORM_FLAG_NO_PDL, and
+ * RMSNORM_FLAG_EARLY_LOADS, which here is the caller's promise that no kernel
+ * still running earlier on the stream writes x, w or rstd (dy may be that
+ * kernel's output, as in a chain of backward kernels): the warp and CTA
+ * kernels then read the weights and their first row's x and rstd before that
+ * kernel completes, and dy and every store only after it.
  */
 int rmsnorm_bwd(const void* x, const void* w, const float* rstd, const void* dy, void* dx,
                 float* dw, int64_t M, int64_t N, float offset, int dtype, void* workspace,

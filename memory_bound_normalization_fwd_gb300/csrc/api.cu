@@ -372,6 +372,9 @@ int bwd_plan(const BwdArgs& a, const rmsnorm_options_t* opts, DeviceInfo* d, Lau
         return fail(RMSNORM_ERR_UNSUPPORTED, "no backward kernel takes N=%lld with these options",
                     static_cast<long long>(a.N));
     l.pdl = (k.flags & RMSNORM_FLAG_NO_PDL) == 0;
+    // Early loads: x, w and rstd may be read before the previous kernel on the
+    // stream completes (the general kernel ignores it).
+    l.early = l.pdl && (k.flags & RMSNORM_FLAG_EARLY_LOADS) != 0;
     return RMSNORM_OK;
 }
 

@@ -15,7 +15,6 @@
 // Kernel 2 sums the partials over CTAs in a fixed order (deterministic) into dw.
 // The general kernel takes any N and alignment with element accesses; its dw
 // partial sits in shared memory, or in its workspace row for very long rows.
-#include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -31,7 +30,7 @@ template <int DT, int THREADS, int V>
 __global__ void __launch_bounds__(THREADS)
 bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __restrict__ rstd,
                 const uint4* dy, uint4* dx, float* __restrict__ partial, int64_t M, int nvec,
-                float n, float offset) {
+                float n, float offset, int mode) {
     constexpr int kWarps = THREADS / 32;
     constexpr int E = VecElems<DT>::value;  // elements per 16-byte vector
     extern __shared__ float4 sw[];  // (offset + w) in fp32, E / 4 float4 per 16-byte vector
@@ -39,11 +38,38 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int wid = tid >> 5;
+    // Early loads (caller's promise that no kernel still running earlier on the
+    // stream writes x, w or rstd): the first row's x and rstd and the weights
+    // are read before the previous kernel completes, dy only after it.
+    const bool early = (mode & kModeEarlyLoads) != 0;
+    uint4 xv[V], gv[V];
+    float r = 0.f;
+    auto load_x = [&](int64_t rw) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * THREADS + tid;
+            xv[v] = make_uint4(0u, 0u, 0u, 0u);
+            if (rw < M && c < nvec) xv[v] = ld_stream(x + rw * nvec + c);
+        }
+        r = rw < M ? __ldg(rstd + rw) : 0.f;
+    };
+    auto load_dy = [&](int64_t rw) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int c = v * THREADS + tid;
+            gv[v] = make_uint4(0u, 0u, 0u, 0u);
+            if (rw < M && c < nvec) gv[v] = ld_stream(dy + rw * nvec + c);
+        }
+    };
 
-    pdl_wait();
-    pdl_launch_dependents();
+    if (!early) pdl_wait();
+    int64_t row = blockIdx.x;
+    load_x(row);
     for (int i = tid; i < nvec; i += THREADS) weights_vec_to_smem<DT>(__ldg(w + i), offset, sw, i);
     __syncthreads();
+    pdl_launch_dependents();
+    if (early) pdl_wait();
+    load_dy(row);
     float acc[V][E];
 #pragma unroll
     for (int v = 0; v < V; ++v)
@@ -51,18 +77,7 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
         for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
 
     int parity = 0;
-    for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
-        uint4 xv[V], gv[V];
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-            const int c = v * THREADS + tid;
-            xv[v] = gv[v] = make_uint4(0u, 0u, 0u, 0u);
-            if (c < nvec) {
-                xv[v] = ld_stream(x + row * nvec + c);
-                gv[v] = ld_stream(dy + row * nvec + c);
-            }
-        }
-        const float r = __ldg(rstd + row);
+    for (; row < M; row += gridDim.x) {
         float cs = 0.f;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
@@ -99,6 +114,8 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
             st_stream(dx + row * nvec + c, pack_vec<DT>(o));
         }
         parity ^= 1;
+        load_x(row + gridDim.x);
+        load_dy(row + gridDim.x);
     }
 
     float4* out = reinterpret_cast<float4*>(partial + static_cast<int64_t>(blockIdx.x) * nvec * E);
@@ -119,13 +136,13 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 // memory (summed in warp order) and the CTA writes one partial row, so the
 // number of partial rows is the grid, not the row count.
 //
-// Rows ahead: with P == 0 each warp loads its next row's x, dy and rstd into
-// registers before reducing the current one (one row in flight ahead: 3.84 ->
-// 3.98 TB/s at 16384x512). With P > 0 (the L2 prefetch distance, mode bits)
-// the registers hold only the current row, and lane 0 instead asks for the x
-// and dy rows P passes ahead to be brought into L2 (cp.async.bulk.prefetch),
-// which frees the registers of the second row.
-template <int DT, int V, bool REGS_AHEAD>
+// Rows ahead: each warp loads its next row's x, dy and rstd into registers
+// before reducing the current one (one row in flight ahead: 3.84 -> 3.98 TB/s
+// at 16384x512). L2 prefetch of rows further ahead (cp.async.bulk.prefetch)
+// measured slower on GB300, both beside the register row (16384x512 bf16:
+// 3944 -> 3580 GB/s at one pass, 3282 at four) and instead of it (12-15%
+// slower, although it freed a fourth CTA per SM), so there is none.
+template <int DT, int V>
 __global__ void __launch_bounds__(256)
 bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __restrict__ rstd,
                 const uint4* dy, uint4* dx, float* __restrict__ partial, int64_t M, int nvec,
@@ -135,37 +152,38 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int wid = tid >> 5;
-    const int P = REGS_AHEAD ? 0 : mode_prefetch(mode);
-    const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * 8;
     int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + wid;
-    auto load = [&](int64_t rw, uint4* xv, uint4* gv, float& r) {
+    // Row rw's x and rstd (part == false), its dy (part == true), or both.
+    auto load = [&](int64_t rw, uint4* xv, uint4* gv, float& r, int part = -1) {
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = v * 32 + lane;
-            xv[v] = gv[v] = make_uint4(0u, 0u, 0u, 0u);
-            if (rw < M && c < nvec) {
-                xv[v] = ld_stream(x + rw * nvec + c);
-                gv[v] = ld_stream(dy + rw * nvec + c);
+            if (part != 1) {
+                xv[v] = make_uint4(0u, 0u, 0u, 0u);
+                if (rw < M && c < nvec) xv[v] = ld_stream(x + rw * nvec + c);
+            }
+            if (part != 0) {
+                gv[v] = make_uint4(0u, 0u, 0u, 0u);
+                if (rw < M && c < nvec) gv[v] = ld_stream(dy + rw * nvec + c);
             }
         }
-        r = rw < M ? __ldg(rstd + rw) : 0.f;
+        if (part != 1) r = rw < M ? __ldg(rstd + rw) : 0.f;
     };
-    auto prefetch = [&](int64_t rw) {
-        if (lane == 0 && rw < M) {
-            bulk_prefetch_l2(x + rw * nvec, row_bytes);
-            bulk_prefetch_l2(dy + rw * nvec, row_bytes);
-        }
-    };
-    pdl_wait();
-    // The first row's loads (and prefetches) go out before the weights are read.
+    // The first row's loads go out before the weights are read. Early loads
+    // (caller's promise that no kernel still running earlier on the stream
+    // writes x, w or rstd): the first row's x and rstd and the weights are read
+    // before the previous kernel completes, dy (and every store) only after it.
+    const bool early = (mode & kModeEarlyLoads) != 0;
     uint4 xv[V], gv[V];
     float r;
-    load(row, xv, gv, r);
-    for (int p = 1; p <= P; ++p) prefetch(row + p * stride);
+    if (!early) pdl_wait();
+    load(row, xv, gv, r, 0);
     pdl_launch_dependents();
     for (int i = tid; i < nvec; i += 256) weights_vec_to_smem<DT>(__ldg(w + i), offset, sw, i);
     __syncthreads();
+    if (early) pdl_wait();
+    load(row, xv, gv, r, 1);
     float acc[V][E];
 #pragma unroll
     for (int v = 0; v < V; ++v)
@@ -175,11 +193,7 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
     for (; row < M; row += stride) {
         uint4 xn[V], gn[V];
         float rn = 0.f;
-        if constexpr (REGS_AHEAD) {
-            load(row + stride, xn, gn, rn);
-        } else {
-            prefetch(row + (P + 1) * stride);
-        }
+        load(row + stride, xn, gn, rn);
         float cs = 0.f;
 #pragma unroll
         for (int v = 0; v < V; ++v) {
@@ -210,13 +224,9 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
             }
             st_stream(dx + row * nvec + c, pack_vec<DT>(o));
         }
-        if constexpr (REGS_AHEAD) {
 #pragma unroll
-            for (int v = 0; v < V; ++v) xv[v] = xn[v], gv[v] = gn[v];
-            r = rn;
-        } else {
-            load(row + stride, xv, gv, r);
-        }
+        for (int v = 0; v < V; ++v) xv[v] = xn[v], gv[v] = gn[v];
+        r = rn;
     }
 
     float* red = reinterpret_cast<float*>(sw + nvec * (E / 4));  // [8][N]
@@ -386,14 +396,12 @@ bool reduce_narrow(int64_t N, int G, int dtype) {
 }
 
 using VecFn = void (*)(const uint4*, const uint4*, const float*, const uint4*, uint4*, float*,
-                       int64_t, int, float, float);
-using WarpFn = void (*)(const uint4*, const uint4*, const float*, const uint4*, uint4*, float*,
-                        int64_t, int, float, float, int);
+                       int64_t, int, float, float, int);
+using WarpFn = VecFn;
 
-template <int DT, bool REGS_AHEAD>
+template <int DT>
 WarpFn pick_warp(int V) {
-    return V == 1 ? bwd_warp_kernel<DT, 1, REGS_AHEAD>
-                  : V == 2 ? bwd_warp_kernel<DT, 2, REGS_AHEAD> : bwd_warp_kernel<DT, 4, REGS_AHEAD>;
+    return V == 1 ? bwd_warp_kernel<DT, 1> : V == 2 ? bwd_warp_kernel<DT, 2> : bwd_warp_kernel<DT, 4>;
 }
 using GenFn = void (*)(const void*, const void*, const float*, const void*, void*, float*,
                        int64_t, int64_t, float, float);
@@ -430,16 +438,14 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
                      aligned16(a.dy) && aligned16(a.dx);
     if ((variant == 0 || variant == 1) && vec && nvec <= 128) {
         const int V = nvec <= 32 ? 1 : nvec <= 64 ? 2 : 4;
-        const int P = k.l2_prefetch > 0 ? k.l2_prefetch : 0;
         WarpFn fn = nullptr;
         if (a.dtype == kBF16)
-            fn = P > 0 ? pick_warp<kBF16, false>(V) : pick_warp<kBF16, true>(V);
+            fn = pick_warp<kBF16>(V);
         else if (a.dtype == kFP16)
-            fn = P > 0 ? pick_warp<kFP16, false>(V) : pick_warp<kFP16, true>(V);
+            fn = pick_warp<kFP16>(V);
         else
-            fn = P > 0 ? pick_warp<kFP32, false>(V) : pick_warp<kFP32, true>(V);
+            fn = pick_warp<kFP32>(V);
         l.kernel = reinterpret_cast<const void*>(fn);
-        l.prefetch = P;
         l.bwd_warp = true;
         l.threads = 256;
         l.lanes_per_row = 32;
@@ -527,7 +533,7 @@ cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial) {
                                    static_cast<const uint4*>(a.w), a.rstd,
                                    static_cast<const uint4*>(a.dy), static_cast<uint4*>(a.dx),
                                    partial, a.M, static_cast<int>(a.N / vec_elems(a.dtype)),
-                                   static_cast<float>(a.N), a.offset);
+                                   static_cast<float>(a.N), a.offset, l.mode());
         } else {
             GenFn fn = reinterpret_cast<GenFn>(const_cast<void*>(l.kernel));
             e = cudaLaunchKernelEx(&c.cfg, fn, a.x, a.w, a.rstd, a.dy, a.dx,

@@ -183,21 +183,40 @@ def test_torch_convenience_forward_then_backward():
     assert np.allclose(dw.cpu().numpy(), dw64, rtol=1e-4, atol=1e-4 * np.abs(dw64).max())
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
-@pytest.mark.parametrize("M,N", [(37, 512), (300, 1000), (1000, 256), (130, 520), (3, 8)])
-@pytest.mark.parametrize("P", [1, 2, 7, 15])
-def test_bwd_warp_l2_prefetch(dtype, M, N, P):
-    # The warp kernel's L2-prefetch form (only the current row in registers,
-    # the rows P passes ahead asked for in L2): same tolerance, small grids so
-    # each warp walks many rows, and in place.
-    e = 4 if dtype == "fp32" else 8  # elements per 16-byte vector
-    if N % e or N // e > 128:
-        pytest.skip("the warp kernel takes rows of up to 128 vectors")
-    offset = float(N % 3 == 0)
-    x, w, dy, rstd = _inputs(M, N, dtype, seed=M + N + P, offset=offset)
-    for max_ctas in (0, 1, 3):
-        dx, dw = _run(x, w, dy, rstd, offset, dtype, variant="warp", max_ctas=max_ctas, l2_prefetch=P)
-        _check(x, w, dy, rstd, dx, dw, offset, dtype, where=f"P={P} {M}x{N} {max_ctas}")
-    dx, dw = _run(x, w, dy, rstd, offset, dtype, inplace="x", variant="warp", max_ctas=2,
-                  l2_prefetch=P)
-    _check(x, w, dy, rstd, dx, dw, offset, dtype, where=f"P={P} {M}x{N} in place")
+def _bwd_call(xd, wd, rd, gd, dxd, dwd, offset, dtype, ws, **opts):
+    M, N = xd.shape
+    rc = B.rmsnorm_bwd(xd.data_ptr(), wd.data_ptr(), rd.data_ptr(), gd.data_ptr(), dxd.data_ptr(),
+                       dwd.data_ptr(), M, N, offset, DT[dtype], ws.data_ptr(), ws.numel() * 4,
+                       B.make_options(**opts), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, B.rmsnorm_last_error()
+
+
+@pytest.mark.parametrize("variant,M,N,dtype", [("warp", 3000, 512, "bf16"), ("warp", 777, 1000, "fp16"),
+                                               ("cta", 2000, 4096, "bf16"), ("cta", 300, 2048, "fp32"),
+                                               ("auto", 5000, 768, "bf16")])
+def test_bwd_early_loads_chain(variant, M, N, dtype):
+    # With RMSNORM_FLAG_EARLY_LOADS the caller promises only that x, w and rstd
+    # are not written by the kernel before; dy may be. A chain where each call's
+    # dy is the previous call's dx, launched back to back, must give the bits
+    # of the same calls with the device synchronised between them; and each
+    # first call (whose inputs come from the generator) matches the oracle.
+    x, w, dy, rstd = _inputs(M, N, dtype, seed=N + M + 5, offset=1.0)
+    xd, wd, rd = W.to_torch(x, dtype).cuda(), W.to_torch(w, dtype).cuda(), torch.from_numpy(rstd).cuda()
+    nbytes = B.rmsnorm_bwd_workspace_size(M, N, DT[dtype], B.make_options(variant=variant))
+    ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device="cuda")
+    steps = 4
+    outs = {}
+    for early in (False, True):
+        g = [W.to_torch(dy, dtype).cuda()] + [torch.empty_like(xd) for _ in range(steps)]
+        dws = [torch.empty(N, dtype=torch.float32, device="cuda") for _ in range(steps)]
+        for k in range(steps):
+            _bwd_call(xd, wd, rd, g[k], g[k + 1], dws[k], 1.0, dtype, ws, variant=variant,
+                      early_loads=early)
+            if not early:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        outs[early] = ([W.from_torch(t) for t in g[1:]], [d.cpu().numpy() for d in dws])
+    for k in range(steps):
+        assert np.array_equal(outs[True][0][k], outs[False][0][k]), f"dx differs at step {k}"
+        assert np.array_equal(outs[True][1][k], outs[False][1][k]), f"dw differs at step {k}"
+    _check(x, w, dy, rstd, outs[True][0][0], outs[True][1][0], 1.0, dtype, where="first call")
