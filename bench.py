@@ -820,6 +820,7 @@ def bench_backward(args, wl):
     def make(early):
         return B.make_options(variant=args.variant, max_ctas=args.max_ctas,
                               lanes_per_row=args.lanes_per_row, l2_prefetch=args.l2_prefetch,
+                              rows_per_stage=args.rows_per_stage, stages=args.stages,
                               early_loads=early)
     nbytes = B.rmsnorm_bwd_workspace_size(wl.M, wl.N, dcode, make(False))
     ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device=dev)
@@ -869,7 +870,8 @@ def bench_backward(args, wl):
                             "note": "RMSNORM_FLAG_EARLY_LOADS: x, w and rstd of the first rows read "
                                     "before the previous step completes (steps are independent)"},
             "workspace_bytes": nbytes, "variant": args.variant, "max_ctas": args.max_ctas,
-            "l2_prefetch": args.l2_prefetch,
+            "rows_per_stage": args.rows_per_stage, "stages": args.stages,
+            "plan": B.rmsnorm_bwd_plan_info(wl.M, wl.N, dcode, make(False)),
             "l2": f"rotating pool of {pool} sets ({pool * set_bytes / 1e6:.0f} MB) > 3x L2"}
 
 

@@ -269,6 +269,7 @@ int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void
  *   dw[j] = sum_i dy[i,j] * x[i,j] * rstd[i]                              (fp32)
  * fp32 arithmetic; dx rounded once to nearest even; dw summed per CTA over its
  * rows, then over CTAs in a fixed order (deterministic for a fixed device).
+ * The sum over CTAs is a second launch.
  *   x, dy, dx  [M, N] x's dtype (bf16, fp16 or fp32), contiguous; dx may equal
  *              x or dy exactly
  *   w          [N]    x's dtype
@@ -279,7 +280,9 @@ int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x, const void
  *              overwritten. Calls sharing one workspace must not overlap on
  *              the GPU (one stream, or ordered streams).
  * With N % 8 == 0 and 16-byte aligned buffers, rows of up to 1024 columns take
- * a warp-per-row kernel and rows of up to 16384 columns a CTA-per-row kernel;
+ * a warp-per-row kernel and rows of up to 16384 columns a CTA-per-row kernel
+ * (variant TMA: rows of up to 16 KB staged into shared memory by bulk copies,
+ * bounded waits as in the forward, reported by rmsnorm_check_device_status);
  * others the general kernel, which keeps a CTA's dw partial row in shared memory
  * up to about 56K columns and, past that, in its own row of the workspace (any
  * N; the grid is then capped so that the partial rows stay within 64 MB).
@@ -315,6 +318,12 @@ int rmsnorm_bwd(const void* x, const void* w, const float* rstd, const void* dy,
 int rmsnorm_bwd_noalloc(const void* x, const void* w, const float* rstd, const void* dy, void* dx,
                         float* dw, int64_t M, int64_t N, float offset, int dtype,
                         const rmsnorm_options_t* opts, void* stream);
+
+/* Fills *out with the launch of the row kernel rmsnorm_bwd would make for
+ * these sizes and options on the current device with 16-byte aligned buffers
+ * (no launch); variant is RMSNORM_VARIANT_WARP, _CTA, _TMA or _GENERIC. */
+int rmsnorm_bwd_plan_info(int64_t M, int64_t N, int dtype, const rmsnorm_options_t* opts,
+                          rmsnorm_plan_t* out);
 
 /* Bytes of workspace rmsnorm_bwd needs for these sizes and options on the
  * current device, for any buffer alignment (written to *bytes). */

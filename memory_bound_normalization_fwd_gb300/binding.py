@@ -26,7 +26,8 @@ STATUS = {
 # Every function include/rmsnorm.h declares.
 EXPORTS = ("rmsnorm_fwd", "rmsnorm_fwd_ex", "rmsnorm_fwd_strided", "rmsnorm_fwd_host",
            "rmsnorm_fwd_host_workspace_size", "rmsnorm_bwd", "rmsnorm_bwd_noalloc",
-           "rmsnorm_bwd_workspace_size", "rmsnorm_plan_info", "rmsnorm_check_device_status",
+           "rmsnorm_bwd_workspace_size", "rmsnorm_plan_info", "rmsnorm_bwd_plan_info",
+           "rmsnorm_check_device_status",
            "rmsnorm_strerror", "rmsnorm_last_error", "rmsnorm_version")
 
 
@@ -102,6 +103,9 @@ def lib() -> ctypes.CDLL:
             L.rmsnorm_plan_info.argtypes = [i64, i64, i32, vp, vp, vp, ctypes.POINTER(Options),
                                             ctypes.POINTER(Plan)]
             L.rmsnorm_plan_info.restype = i32
+            L.rmsnorm_bwd_plan_info.argtypes = [i64, i64, i32, ctypes.POINTER(Options),
+                                                ctypes.POINTER(Plan)]
+            L.rmsnorm_bwd_plan_info.restype = i32
             L.rmsnorm_check_device_status.argtypes = [vp]
             L.rmsnorm_check_device_status.restype = i32
             L.rmsnorm_strerror.argtypes = [i32]
@@ -207,6 +211,14 @@ def rmsnorm_plan_info(M: int, N: int, dtype: int, x: int = 0, w: int = 0, y: int
     _check(lib().rmsnorm_plan_info(M, N, dtype, x, w, y,
                                    ctypes.byref(opts) if opts is not None else None,
                                    ctypes.byref(out)))
+    return out.as_dict()
+
+
+def rmsnorm_bwd_plan_info(M: int, N: int, dtype: int, opts: Options | None = None) -> dict:
+    """The backward row kernel's launch for aligned buffers (no launch)."""
+    out = Plan()
+    _check(lib().rmsnorm_bwd_plan_info(M, N, dtype, ctypes.byref(opts) if opts is not None else None,
+                                       ctypes.byref(out)))
     return out.as_dict()
 
 
@@ -341,4 +353,7 @@ def bwd(x, w, rstd, dy, offset: float = 0.0, dx=None, stream=None, **options):
         _check(rmsnorm_bwd(x.data_ptr(), w.data_ptr(), rstd.data_ptr(), dy.data_ptr(),
                            dx.data_ptr(), dw.data_ptr(), M, N, offset, _dtype_code(x),
                            ws.data_ptr(), ws.numel() * 4, opts, s.cuda_stream))
+        # The workspace was allocated on the current stream; keep it from being
+        # reused before the work on `s` is done.
+        ws.record_stream(s)
     return dx, dw

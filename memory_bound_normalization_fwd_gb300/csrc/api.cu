@@ -362,10 +362,9 @@ int bwd_plan(const BwdArgs& a, const rmsnorm_options_t* opts, DeviceInfo* d, Lau
     Knobs k;
     int rc = read_knobs(opts, &variant, &k);
     if (rc != RMSNORM_OK) return rc;
-    if (variant != RMSNORM_VARIANT_AUTO && variant != RMSNORM_VARIANT_WARP &&
-        variant != RMSNORM_VARIANT_CTA && variant != RMSNORM_VARIANT_GENERIC)
+    if (variant == RMSNORM_VARIANT_CLUSTER)
         return fail(RMSNORM_ERR_UNSUPPORTED,
-                    "the backward has the WARP, CTA and GENERIC variants only");
+                    "the backward has the WARP, CTA, TMA and GENERIC variants only");
     cudaError_t e = device_info(d);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
     if (!bwd_choose(a, *d, k, variant, l))
@@ -400,7 +399,7 @@ extern "C" int rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype,
         else o.struct_size = sizeof(o);
         if (pass == 1) o.variant = RMSNORM_VARIANT_GENERIC;
         if (bwd_plan(a, &o, &d, l) == RMSNORM_OK) {
-            const int64_t b = static_cast<int64_t>(l.grid) * N * 4;
+            const int64_t b = bwd_workspace_bytes(l, N);
             if (b > need) need = b;
         }
     }
@@ -420,7 +419,7 @@ extern "C" int rmsnorm_bwd(const void* x, const void* w, const float* rstd, cons
     Launch l;
     rc = bwd_plan(a, opts, &d, l);
     if (rc != RMSNORM_OK) return rc;
-    const int64_t need = M > 0 ? static_cast<int64_t>(l.grid) * N * 4 : 0;
+    const int64_t need = M > 0 ? bwd_workspace_bytes(l, N) : 0;
     if (workspace_bytes < need)
         return fail(RMSNORM_ERR_WORKSPACE, "workspace of %lld bytes, %lld needed",
                     static_cast<long long>(workspace_bytes), static_cast<long long>(need));
@@ -497,14 +496,45 @@ extern "C" int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x,
     return RMSNORM_OK;
 }
 
+extern "C" int rmsnorm_bwd_plan_info(int64_t M, int64_t N, int dtype, const rmsnorm_options_t* opts,
+                                     rmsnorm_plan_t* out) {
+    if (out == nullptr) return fail(RMSNORM_ERR_NULL, "out is NULL");
+    std::memset(out, 0, sizeof(*out));
+    if (dtype != RMSNORM_DTYPE_BF16 && dtype != RMSNORM_DTYPE_FP16 && dtype != RMSNORM_DTYPE_FP32)
+        return fail(RMSNORM_ERR_DTYPE, "dtype %d is not a rmsnorm_dtype_t", dtype);
+    if (M < 1 || N <= 0) return fail(RMSNORM_ERR_SHAPE, "plan needs M >= 1 and N > 0");
+    // 256-byte aligned stand-ins: the plan of a call with aligned buffers.
+    const void* p = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+    const BwdArgs a{p, p, nullptr, p, const_cast<void*>(p), nullptr, M, N, 0.f, dtype, nullptr};
+    DeviceInfo d;
+    Launch l;
+    int rc = bwd_plan(a, opts, &d, l);
+    if (rc != RMSNORM_OK) return rc;
+    out->variant = l.bwd_tma ? RMSNORM_VARIANT_TMA
+                   : l.bwd_warp ? RMSNORM_VARIANT_WARP
+                   : l.vecs_per_lane > 0 ? RMSNORM_VARIANT_CTA : RMSNORM_VARIANT_GENERIC;
+    out->threads = l.threads;
+    out->grid = l.grid;
+    out->lanes_per_row = l.lanes_per_row;
+    out->vecs_per_lane = l.vecs_per_lane;
+    out->rows_per_stage = l.rows_per_stage;
+    out->stages = l.stages;
+    out->smem_bytes = l.smem;
+    out->ctas_per_sm = l.ctas_per_sm;
+    out->sm_count = d.sm_count;
+    return RMSNORM_OK;
+}
+
 extern "C" int rmsnorm_check_device_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "synchronize: %s", cudaGetErrorString(e));
-    unsigned int v = 0, vc = 0;
+    unsigned int v = 0, vc = 0, vb = 0;
     e = status_read_and_clear(&v);
     if (e == cudaSuccess) e = cluster_status_read_and_clear(&vc);
+    if (e == cudaSuccess) e = bwd_status_read_and_clear(&vb);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
-    if (v != 0 || vc != 0) return fail(RMSNORM_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
+    if (v != 0 || vc != 0 || vb != 0)
+        return fail(RMSNORM_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
     return RMSNORM_OK;
 }
 

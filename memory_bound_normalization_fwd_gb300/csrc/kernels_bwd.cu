@@ -15,12 +15,20 @@
 // Kernel 2 sums the partials over CTAs in a fixed order (deterministic) into dw.
 // The general kernel takes any N and alignment with element accesses; its dw
 // partial sits in shared memory, or in its workspace row for very long rows.
+#include "async_copy.cuh"
 #include "common.cuh"
 #include "launch.h"
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
 
 namespace rmsn {
+
+// Bit 0: a bounded wait of the staged backward ran out since the last read.
+__device__ unsigned int g_bwd_status;
+
 namespace {
 
 // (Loading the next row ahead, as the warp kernel does, measured slower here:
@@ -247,6 +255,218 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
     }
 }
 
+// Staged backward for packed rows (x, dy and dx contiguous, rows of whole
+// 16-byte vectors): chunks of R consecutive rows of x and of dy reach shared
+// memory by two bulk copies (cp.async.bulk) per stage, in a ring of S stages
+// completed on one mbarrier each, issued by thread 0; chunks are strided over
+// the persistent grid. Teams of TEAM threads take the stage's rows; each
+// thread holds V 16-byte vectors of x and dy of its row in registers for both
+// passes (c = sum dy s x over the row, then dx and the dw contribution), so
+// the bytes in flight per SM come from shared memory rather than registers.
+// (offset + w) sits in shared memory as fp32; each thread owns fixed columns
+// and keeps its dw contribution in fp32 registers over all its rows; at the
+// end the teams meet in shared memory (the ring's space, summed in team
+// order) and the CTA writes one partial row, reduced over CTAs as for the
+// other kernels. Waits are bounded as in the forward's staged kernel; with
+// early loads x is copied before the dependency wait and dy after it.
+template <int DT, int THREADS, int TEAM, int V>
+__global__ void __launch_bounds__(THREADS)
+bwd_tma_kernel(const uint4* x, const uint4* __restrict__ w, const float* __restrict__ rstd,
+               const uint4* dy, uint4* dx, float* __restrict__ partial, int64_t M, int nvec,
+               float n, float offset, int rows_per_stage, int stages, int stage_stride,
+               int w_bytes, long long limit_cycles, long long drain_cycles, int mode) {
+    constexpr int E = VecElems<DT>::value;
+    constexpr int kTeams = THREADS / TEAM;
+    constexpr int kLanes = TEAM < 32 ? TEAM : 32;
+    constexpr int kTeamWarps = TEAM > 32 ? TEAM / 32 : 1;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float part[2][kTeams][kTeamWarps];
+    const int tid = threadIdx.x;
+    const int team = tid / TEAM;
+    const int t = tid % TEAM;
+    const bool early = (mode & kModeEarlyLoads) != 0;
+    const int R = rows_per_stage;
+    const int64_t ntiles = (M + R - 1) / R;
+    const int64_t nchunks =
+        ntiles > blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
+    // Layout: 128 bytes of barriers, (offset + w) as fp32 (w_bytes, a multiple
+    // of 128), the rstd of two chunks (2 x R floats, rounded up to 128 bytes),
+    // then the stages, each R rows of x followed by R rows of dy.
+    const uint32_t raw = smem_u32(smem);
+    unsigned char* base = smem + (((raw + 127u) & ~127u) - raw);
+    const uint32_t bars = smem_u32(base);
+    float4* sw = reinterpret_cast<float4*>(base + 128);
+    float* srstd = reinterpret_cast<float*>(base + 128 + w_bytes);  // [2][R]
+    unsigned char* buf = base + 128 + w_bytes + (2 * R * 4 + 127) / 128 * 128;
+
+    if (tid == 0) {
+        for (int st = 0; st < stages; ++st) mbar_init(bars + 8 * st, 1);
+        fence_mbar_init();
+    }
+    auto chunk_row = [&](int64_t k) { return (blockIdx.x + k * gridDim.x) * R; };
+    auto chunk_rows = [&](int64_t k) {
+        const int64_t r0 = chunk_row(k);
+        return static_cast<uint32_t>((M - r0) < R ? (M - r0) : R);
+    };
+    // Local chunk k: expect both copies' bytes, then x; dy separately, so that
+    // with early loads x can go before the dependency wait and dy after it.
+    auto issue_x = [&](int64_t k) {
+        if (k >= nchunks) return;
+        const int st = static_cast<int>(k % stages);
+        const uint32_t bytes = chunk_rows(k) * row_bytes;
+        mbar_arrive_expect_tx(bars + 8 * st, 2u * bytes);
+        bulk_g2s(smem_u32(buf + static_cast<int64_t>(st) * stage_stride), x + chunk_row(k) * nvec,
+                 bytes, bars + 8 * st);
+    };
+    auto issue_dy = [&](int64_t k) {
+        if (k >= nchunks) return;
+        const int st = static_cast<int>(k % stages);
+        bulk_g2s(smem_u32(buf + static_cast<int64_t>(st) * stage_stride) + R * row_bytes,
+                 dy + chunk_row(k) * nvec, chunk_rows(k) * row_bytes, bars + 8 * st);
+    };
+
+    if (!early) pdl_wait();
+    if (tid == 0) {
+        for (int k = 0; k < stages; ++k) {
+            issue_x(k);
+            if (!early) issue_dy(k);
+        }
+    }
+    // rstd of chunk k goes to srstd[k & 1] one chunk ahead (R <= THREADS), so
+    // its load does not wait behind the chunk's rows.
+    auto load_rstd = [&](int64_t k) {
+        return (k < nchunks && tid < static_cast<int>(chunk_rows(k))) ? __ldg(rstd + chunk_row(k) + tid)
+                                                                     : 0.f;
+    };
+    const float r_first = load_rstd(0);
+    for (int i = tid; i < nvec; i += THREADS) weights_vec_to_smem<DT>(__ldg(w + i), offset, sw, i);
+    if (tid < R) srstd[tid] = r_first;
+    __syncthreads();  // barriers initialised, weights and the first chunk's rstd in shared memory
+    pdl_launch_dependents();
+    if (early) {
+        pdl_wait();
+        if (tid == 0) {
+            for (int k = 0; k < stages; ++k) issue_dy(k);
+        }
+    }
+
+    float acc[V][E];
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[v][e] = 0.f;
+
+    int pp = 0;
+    int64_t k = 0;
+    bool aborted = false;
+    for (; k < nchunks; ++k) {
+        const int st = static_cast<int>(k % stages);
+        const bool ok = mbar_wait_bounded(bars + 8 * st, static_cast<uint32_t>((k / stages) & 1),
+                                          limit_cycles);
+        if (__syncthreads_or(!ok)) {
+            aborted = true;
+            break;
+        }
+        const float r_next = load_rstd(k + 1);  // lands while this chunk is processed
+        const float* sr = srstd + (k & 1) * R;
+        const uint4* sx = reinterpret_cast<const uint4*>(buf + static_cast<int64_t>(st) * stage_stride);
+        const uint4* sg = sx + static_cast<int64_t>(R) * nvec;
+        const int64_t r0 = chunk_row(k);
+        const int rows = static_cast<int>(chunk_rows(k));
+        const int iters = (rows + kTeams - 1) / kTeams;  // CTA-uniform
+        for (int i = 0; i < iters; ++i) {
+            const int rr = i * kTeams + team;
+            const bool act = rr < rows;
+            uint4 xv[V], gv[V];
+            float cs = 0.f;
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const int c = v * TEAM + t;
+                xv[v] = gv[v] = make_uint4(0u, 0u, 0u, 0u);
+                if (act && c < nvec) {
+                    xv[v] = sx[rr * nvec + c];
+                    gv[v] = sg[rr * nvec + c];
+                }
+                if (c < nvec) {
+                    float xf[E], gf[E], sv[E];
+                    unpack_vec<DT>(xv[v], xf);
+                    unpack_vec<DT>(gv[v], gf);
+                    weights_from_smem<DT>(sw, c, sv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) cs = fmaf(gf[e] * sv[e], xf[e], cs);
+                }
+            }
+#pragma unroll
+            for (int off = kLanes / 2; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
+            if constexpr (TEAM > 32) {
+                if ((t & 31) == 0) part[pp][team][t >> 5] = cs;
+                asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(TEAM) : "memory");
+                cs = 0.f;
+#pragma unroll
+                for (int q = 0; q < kTeamWarps; ++q) cs += part[pp][team][q];
+                pp ^= 1;
+            }
+            if (act) {
+                const int64_t row = r0 + rr;
+                const float r = sr[rr];
+                const float kk = (r * r) * cs / n;
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const int c = v * TEAM + t;
+                    if (c >= nvec) continue;
+                    float xf[E], gf[E], sv[E], o[E];
+                    unpack_vec<DT>(xv[v], xf);
+                    unpack_vec<DT>(gv[v], gf);
+                    weights_from_smem<DT>(sw, c, sv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        o[e] = r * (gf[e] * sv[e] - xf[e] * kk);
+                        acc[v][e] = fmaf(gf[e] * xf[e], r, acc[v][e]);
+                    }
+                    st_stream(dx + row * nvec + c, pack_vec<DT>(o));
+                }
+            }
+        }
+        if (tid < R) srstd[((k + 1) & 1) * R + tid] = r_next;
+        __syncthreads();  // every thread is done reading this stage (and the next rstd is in place)
+        if (tid == 0) {
+            issue_x(k + stages);
+            issue_dy(k + stages);
+        }
+    }
+
+    if (aborted) {
+        if (tid == 0) {
+            atomicOr(&g_bwd_status, 1u);
+            // Copies for the local chunks k .. k + stages - 1 may still be in
+            // flight into this CTA's shared memory: wait for them (bounded).
+            for (int64_t j = k; j < k + stages && j < nchunks; ++j)
+                mbar_wait_bounded(bars + 8 * static_cast<int>(j % stages),
+                                  static_cast<uint32_t>((j / stages) & 1), drain_cycles);
+        }
+        return;
+    }
+    // The teams' dw contributions meet in the ring's space (every copy has
+    // landed and been consumed), summed in team order into this CTA's row.
+    float* red = reinterpret_cast<float*>(buf);  // [kTeams][N]
+    const int N8 = nvec * E;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = v * TEAM + t;
+        if (c < nvec)
+#pragma unroll
+            for (int e = 0; e < E; ++e) red[team * N8 + c * E + e] = acc[v][e];
+    }
+    __syncthreads();
+    for (int j = tid; j < N8; j += THREADS) {
+        float s = 0.f;
+#pragma unroll
+        for (int q = 0; q < kTeams; ++q) s += red[q * N8 + j];
+        partial[static_cast<int64_t>(blockIdx.x) * N8 + j] = s;
+    }
+}
+
 // General backward: any N and 2-byte alignment. dw partial in shared memory (N floats).
 // GACC: rows too long for a dw partial row in shared memory accumulate it in
 // this CTA's own row of the workspace instead (each thread owns fixed
@@ -429,13 +649,117 @@ GenFn pick_gen(int T, bool gacc) {
     }
 }
 
+using TmaFn = void (*)(const uint4*, const uint4*, const float*, const uint4*, uint4*, float*,
+                      int64_t, int, float, float, int, int, int, int, long long, long long, int);
+
+template <int DT>
+TmaFn pick_tma(int team, int V) {
+#define RMSN_CASE(tm, v) \
+    if (team == tm && V == v) return bwd_tma_kernel<DT, (tm < 256 ? 256 : tm), tm, v>;
+    RMSN_CASE(16, 1) RMSN_CASE(16, 2) RMSN_CASE(16, 4)
+    RMSN_CASE(32, 1) RMSN_CASE(32, 2) RMSN_CASE(32, 4)
+    RMSN_CASE(64, 2) RMSN_CASE(128, 2) RMSN_CASE(256, 2) RMSN_CASE(512, 2)
+#undef RMSN_CASE
+    return nullptr;
+}
+
+// Opts a kernel into the device's dynamic shared memory, once per device;
+// returns the byte count available (0 on failure). Later calls touch only a
+// cache, so planning makes no CUDA call (and stays legal in stream capture).
+int max_dynamic_smem(const void* fn, int max_optin) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> g(mu);
+    auto it = done.find({dev, fn});
+    if (it != done.end()) return it->second;
+    cudaFuncAttributes attr;
+    int bytes = 0;
+    if (cudaFuncGetAttributes(&attr, fn) == cudaSuccess) {
+        bytes = max_optin - static_cast<int>(attr.sharedSizeBytes);
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+            cudaSuccess)
+            bytes = 0;
+    }
+    done[{dev, fn}] = bytes;
+    return bytes;
+}
+
+int next_pow2(int64_t v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// The staged kernel's plan: rows of up to 16 KB, teams of 32 threads (two or
+// fewer vectors each) for rows of up to 64 vectors, else of nvec / 2; stages
+// of about 16 KB of x (and as much dy), two deep.
+bool bwd_tma_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
+    const int64_t nvec = a.N / vec_elems(a.dtype);
+    if (nvec > 1024) return false;
+    int team = k.lanes_per_row;
+    if (team == 0) team = nvec <= 64 ? 32 : next_pow2((nvec + 1) / 2);
+    if (team < 16 || team > 512 || (team & (team - 1)) != 0) return false;
+    const int V = next_pow2((nvec + team - 1) / team);
+    TmaFn fn = a.dtype == kBF16   ? pick_tma<kBF16>(team, V)
+               : a.dtype == kFP16 ? pick_tma<kFP16>(team, V)
+                                  : pick_tma<kFP32>(team, V);
+    if (!fn) return false;
+    const int threads = team < 256 ? 256 : team;
+    const int teams = threads / team;
+    const int max_dyn = max_dynamic_smem(reinterpret_cast<const void*>(fn), d.max_smem_optin);
+    if (max_dyn <= 0) return false;
+    const int64_t row_bytes = nvec * 16;
+    int64_t R = k.rows_per_stage > 0 ? k.rows_per_stage : std::max<int64_t>(1, 16384 / row_bytes);
+    if (k.rows_per_stage == 0 && R > teams) R = R / teams * teams;
+    if (a.M > 0 && R > a.M) R = a.M;
+    if (R > threads) return false;  // one thread loads each row's rstd
+    const int S = k.stages > 0 ? k.stages : 2;
+    if (S < 1 || S > 8 || R * row_bytes >= (1 << 20)) return false;
+    const int64_t stage_stride = (2 * R * row_bytes + 127) / 128 * 128;
+    const int64_t w_bytes = (a.N * 4 + 127) / 128 * 128;
+    // The ring also holds the teams' dw rows at the end.
+    const int64_t ring = std::max<int64_t>(S * stage_stride, int64_t(teams) * a.N * 4);
+    const int64_t smem = 128 + 128 + w_bytes + (2 * R * 4 + 127) / 128 * 128 + ring;
+    if (smem > max_dyn) return false;
+    l.kernel = reinterpret_cast<const void*>(fn);
+    l.threads = threads;
+    l.lanes_per_row = team;
+    l.vecs_per_lane = V;
+    l.rows_per_stage = static_cast<int>(R);
+    l.stages = S;
+    l.smem = static_cast<int>(smem);
+    l.ctas_per_sm = occupancy(l.kernel, threads, l.smem);
+    if (l.ctas_per_sm < 1) return false;
+    l.work_items = a.M;
+    l.grid = persistent_grid(a.M > 0 ? (a.M + R - 1) / R : 1, 1, d.sm_count, l.ctas_per_sm,
+                             k.max_ctas);
+    l.wait_limit_ns = k.wait_limit_ns > 0 ? k.wait_limit_ns : 1000000000LL;
+    l.bwd_tma = true;
+    return true;
+}
+
 }  // namespace
 
+bool bwd_choose_plan(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int variant, Launch& l);
+
 bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int variant, Launch& l) {
+    if (!bwd_choose_plan(a, d, k, variant, l)) return false;
+    if (l.wait_limit_ns == 0) l.wait_limit_ns = k.wait_limit_ns > 0 ? k.wait_limit_ns : 1000000000LL;
+    return true;
+}
+
+int64_t bwd_workspace_bytes(const Launch& l, int64_t N) {
+    return static_cast<int64_t>(l.grid) * N * 4;  // one fp32 partial row per CTA
+}
+
+bool bwd_choose_plan(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int variant, Launch& l) {
     const int64_t e = vec_elems(a.dtype);
     const int64_t nvec = a.N / e;
     const bool vec = a.N % e == 0 && aligned16(a.x) && aligned16(a.w) &&
                      aligned16(a.dy) && aligned16(a.dx);
+    if (variant == 3) return vec && bwd_tma_choose(a, d, k, l);
     if ((variant == 0 || variant == 1) && vec && nvec <= 128) {
         const int V = nvec <= 32 ? 1 : nvec <= 64 ? 2 : 4;
         WarpFn fn = nullptr;
@@ -516,18 +840,39 @@ bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int varia
     return true;
 }
 
+cudaError_t bwd_status_read_and_clear(unsigned int* value) {
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_bwd_status, sizeof(v));
+    if (e != cudaSuccess) return e;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(zero));
+        if (e != cudaSuccess) return e;
+    }
+    *value = v;
+    return cudaSuccess;
+}
+
 cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial) {
     if (a.M > 0) {
         LaunchCfg c(l, a.stream, l.pdl);
         cudaError_t e;
-        if (l.bwd_warp) {
-            WarpFn fn = reinterpret_cast<WarpFn>(const_cast<void*>(l.kernel));
+        if (l.bwd_tma) {
+            TmaFn fn = reinterpret_cast<TmaFn>(const_cast<void*>(l.kernel));
+            const int64_t row_bytes = a.N / vec_elems(a.dtype) * 16;
+            const int stage_stride =
+                static_cast<int>((2 * l.rows_per_stage * row_bytes + 127) / 128 * 128);
+            const int w_bytes = static_cast<int>((a.N * 4 + 127) / 128 * 128);
+            // Bounds in SM cycles at 2.1 cycles per ns (the top SM clock).
+            const long long limit = l.wait_limit_ns * 21 / 10;
             e = cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                                    static_cast<const uint4*>(a.w), a.rstd,
                                    static_cast<const uint4*>(a.dy), static_cast<uint4*>(a.dx),
                                    partial, a.M, static_cast<int>(a.N / vec_elems(a.dtype)),
-                                   static_cast<float>(a.N), a.offset, l.mode());
-        } else if (l.vecs_per_lane > 0) {  // the CTA-per-row vector kernel
+                                   static_cast<float>(a.N), a.offset, l.rows_per_stage, l.stages,
+                                   stage_stride, w_bytes, limit < 1 ? 1LL : limit,
+                                   1000000000LL * 21 / 10, l.mode());
+        } else if (l.bwd_warp || l.vecs_per_lane > 0) {  // warp or CTA per row
             VecFn fn = reinterpret_cast<VecFn>(const_cast<void*>(l.kernel));
             e = cudaLaunchKernelEx(&c.cfg, fn, static_cast<const uint4*>(a.x),
                                    static_cast<const uint4*>(a.w), a.rstd,

@@ -62,7 +62,8 @@ struct Launch {
     bool early = false;    // x and w may be read before the previous kernel completes
     bool early_weights = false;  // w may be read before the previous kernel completes
     int prefetch = 0;            // L2 prefetch distance (kModePrefetchShift); 0 = none
-    bool bwd_warp = false;       // backward: the warp-per-row kernel (takes a mode argument)
+    bool bwd_warp = false;       // backward: the warp-per-row kernel
+    bool bwd_tma = false;        // backward: the staged kernel
     int mode() const {
         return (blocked ? kModeBlocked : 0) | (early ? kModeEarlyLoads : 0) |
                (early_weights ? kModeEarlyWeights : 0) | (prefetch << kModePrefetchShift);
@@ -125,11 +126,14 @@ struct BwdArgs {
     int dtype;
     cudaStream_t stream;
 };
-// variant: 0 automatic, 1 warp per row (N <= 1024), 2 CTA per row, 4 the general kernel.
+// variant: 0 automatic, 1 warp per row (N <= 1024), 2 CTA per row, 3 staged (bulk copies
+// into shared memory, packed rows up to 16 KB), 4 the general kernel.
 bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int variant, Launch& l);
 // Launches the row kernel (writing one fp32 dw partial row per CTA into `partial`,
 // l.grid rows of N floats) and the reduction of the partials into dw.
 cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial);
+// Workspace bytes a backward plan needs (its partial rows).
+int64_t bwd_workspace_bytes(const Launch& l, int64_t N);
 // The backward's built-in scratch on the current device (set up on first use).
 cudaError_t bwd_builtin_scratch(float** ptr, int64_t* floats);
 
@@ -153,6 +157,7 @@ int forward_knobs(const void* x, int64_t ldx, const void* w, void* y, int64_t ld
 // clear on the current device.
 cudaError_t status_read_and_clear(unsigned int* value);
 cudaError_t cluster_status_read_and_clear(unsigned int* value);
+cudaError_t bwd_status_read_and_clear(unsigned int* value);
 
 // Grid size: min(work items / items per CTA, SMs x resident CTAs), at least 1.
 inline int persistent_grid(int64_t work_items, int64_t items_per_cta, int sm_count,

@@ -78,7 +78,7 @@ SHAPES = [(1, 8), (37, 512), (300, 1000), (64, 4096), (33, 8192), (17, 16384), (
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("M,N", SHAPES)
-@pytest.mark.parametrize("variant", ["auto", "warp", "cta", "generic"])
+@pytest.mark.parametrize("variant", ["auto", "warp", "cta", "tma", "generic"])
 def test_bwd_parity(dtype, M, N, variant):
     offset = float((M + N) % 2)
     x, w, dy, rstd = _inputs(M, N, dtype, seed=M * 7 + N, offset=offset)
@@ -94,7 +94,8 @@ def test_bwd_parity(dtype, M, N, variant):
             e = 4 if dtype == "fp32" else 8   # elements per 16-byte vector
             nvec = N // e                      # vector kernels: up to 2048 (CTA), 128 (warp)
             if (variant == "cta" and (N % e or nvec > 2048)) or \
-                    (variant == "warp" and (N % e or nvec > 128)):
+                    (variant == "warp" and (N % e or nvec > 128)) or \
+                    (variant == "tma" and (N % e or nvec > 1024)):
                 pytest.skip("vector kernel does not take this shape")
             raise
         _check(x, w, dy, rstd, dx, dw, offset, dtype, where=f"{variant} {M}x{N} {max_ctas}")
@@ -193,7 +194,8 @@ def _bwd_call(xd, wd, rd, gd, dxd, dwd, offset, dtype, ws, **opts):
 
 @pytest.mark.parametrize("variant,M,N,dtype", [("warp", 3000, 512, "bf16"), ("warp", 777, 1000, "fp16"),
                                                ("cta", 2000, 4096, "bf16"), ("cta", 300, 2048, "fp32"),
-                                               ("auto", 5000, 768, "bf16")])
+                                               ("tma", 3000, 512, "bf16"), ("tma", 500, 4096, "fp16"),
+                                               ("tma", 777, 1000, "fp32"), ("auto", 5000, 768, "bf16")])
 def test_bwd_early_loads_chain(variant, M, N, dtype):
     # With RMSNORM_FLAG_EARLY_LOADS the caller promises only that x, w and rstd
     # are not written by the kernel before; dy may be. A chain where each call's
@@ -220,3 +222,45 @@ def test_bwd_early_loads_chain(variant, M, N, dtype):
         assert np.array_equal(outs[True][0][k], outs[False][0][k]), f"dx differs at step {k}"
         assert np.array_equal(outs[True][1][k], outs[False][1][k]), f"dw differs at step {k}"
     _check(x, w, dy, rstd, outs[True][0][0], outs[True][1][0], 1.0, dtype, where="first call")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("N", [8, 512, 1000, 4096, 8192])
+@pytest.mark.parametrize("rows,stages", [(1, 1), (3, 2), (8, 3), (16, 2), (0, 0)])
+def test_bwd_tma_stage_shapes(dtype, N, rows, stages):
+    # The staged backward over stage shapes, grids small enough that every CTA
+    # walks many chunks (ragged last chunk: M is not a multiple of the rows per
+    # stage), and in place (dx == x, dx == dy).
+    e = 4 if dtype == "fp32" else 8
+    if N // e > 1024:
+        pytest.skip("the staged kernel takes rows of up to 16 KB")
+    M = 203
+    opts = dict(variant="tma", rows_per_stage=rows, stages=stages)
+    try:
+        B.rmsnorm_bwd_plan_info(M, N, DT[dtype], B.make_options(**opts))
+    except B.RMSNormError as err:
+        assert err.status == -8
+        pytest.skip("the stages do not fit in shared memory")
+    x, w, dy, rstd = _inputs(M, N, dtype, seed=N + rows + stages, offset=float(rows % 2))
+    for max_ctas in (0, 1, 5):
+        dx, dw = _run(x, w, dy, rstd, float(rows % 2), dtype, max_ctas=max_ctas, **opts)
+        _check(x, w, dy, rstd, dx, dw, float(rows % 2), dtype, where=f"{N} {rows}x{stages} {max_ctas}")
+    for inplace in ("x", "dy"):
+        dx, dw = _run(x, w, dy, rstd, float(rows % 2), dtype, inplace=inplace, max_ctas=3, **opts)
+        _check(x, w, dy, rstd, dx, dw, float(rows % 2), dtype, where=f"{N} in place {inplace}")
+
+
+def test_bwd_tma_bounded_wait_reports_timeout_and_recovers():
+    # A 1 ns wait bound makes the first stage's wait give up before its copies
+    # land: the kernel records the timeout, waits for its own copies and exits;
+    # the status call reports it once, and the next normal call is exact.
+    M, N, dtype = 4096, 1024, "bf16"
+    x, w, dy, rstd = _inputs(M, N, dtype, seed=21)
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.rmsnorm_check_device_status(s) == 0
+    _run(x, w, dy, rstd, 0.0, dtype, variant="tma", wait_limit_ns=1)
+    assert B.rmsnorm_check_device_status(s) == -7
+    assert B.rmsnorm_check_device_status(s) == 0
+    dx, dw = _run(x, w, dy, rstd, 0.0, dtype, variant="tma")
+    assert B.rmsnorm_check_device_status(s) == 0
+    _check(x, w, dy, rstd, dx, dw, 0.0, dtype, where="after timeout")
