@@ -696,6 +696,47 @@ def per_workload(args, dev, peak: float) -> dict:
     return out
 
 
+def launch_only_backward(args, wl) -> dict:
+    """N direct rmsnorm_bwd calls over a rotating pool of x, dy and dx sets
+    (early loads unless --strict-order), the plan bench_backward times;
+    nothing is timed."""
+    import torch
+    from memory_bound_normalization_fwd_gb300 import binding as B
+    from memory_bound_normalization_fwd_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    dcode = DCODE[wl.dtype]
+    x_bits, w_bits = W.generate(wl)
+    dy_bits, _ = W.generate(W.custom(wl.M, wl.N, wl.dtype, seed=99))
+    x0, dy0 = W.to_torch(x_bits, wl.dtype).to(dev), W.to_torch(dy_bits, wl.dtype).to(dev)
+    w = W.to_torch(w_bits, wl.dtype).to(dev)
+    r0 = torch.empty(wl.M, dtype=torch.float32, device=dev)
+    B.fwd(x0, w, eps=wl.eps, offset=wl.offset, y=torch.empty_like(x0), rstd=r0)
+    eb = W.ELEM_BYTES[wl.dtype]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool = max(2, -(-3 * l2 // (3 * eb * wl.M * wl.N + 4 * wl.M)))
+    xs = [x0.clone() for _ in range(pool)]
+    dys = [dy0.clone() for _ in range(pool)]
+    dxs = [torch.empty_like(x0) for _ in range(pool)]
+    dw = torch.empty(wl.N, dtype=torch.float32, device=dev)
+    opts = B.make_options(variant=args.variant, max_ctas=args.max_ctas,
+                          lanes_per_row=args.lanes_per_row, rows_per_stage=args.rows_per_stage,
+                          stages=args.stages, early_loads=not args.strict_order)
+    nbytes = B.rmsnorm_bwd_workspace_size(wl.M, wl.N, dcode, opts)
+    ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    for k in range(args.launch_only):
+        i = k % pool
+        rc = B.rmsnorm_bwd(xs[i].data_ptr(), w.data_ptr(), r0.data_ptr(), dys[i].data_ptr(),
+                           dxs[i].data_ptr(), dw.data_ptr(), wl.M, wl.N, wl.offset, dcode,
+                           ws.data_ptr(), ws.numel() * 4, opts, s)
+        if rc != 0:
+            raise RuntimeError(B.rmsnorm_last_error())
+    torch.cuda.synchronize()
+    return {"launch_only_backward": wl.name, "launches": args.launch_only, "pool_sets": pool,
+            "launch_order": "strict" if args.strict_order else "early loads",
+            "plan": B.rmsnorm_bwd_plan_info(wl.M, wl.N, dcode, opts)}
+
+
 def launch_only(args, wl) -> dict:
     """N direct rmsnorm_fwd_ex calls over the rotating pool, the plan bench_ours
     times for this workload and launch mode; nothing is timed."""
@@ -915,17 +956,18 @@ def main(argv=None):
     wl = W.get(args.workload or W.BENCH_WORKLOAD)
     rank, world, local_rank = dist_env()
 
-    if args.backward:
-        for name in ([args.workload] if args.workload else list(W.WORKLOADS)):
-            print(json.dumps(bench_backward(args, W.get(name))), flush=True)
-        return 0
-
     if args.ablation:
         run_ablation(args, [args.workload] if args.workload else list(W.WORKLOADS))
         return 0
 
     if args.launch_only:
-        print(json.dumps(launch_only(args, wl)), flush=True)
+        fn = launch_only_backward if args.backward else launch_only
+        print(json.dumps(fn(args, wl)), flush=True)
+        return 0
+
+    if args.backward:
+        for name in ([args.workload] if args.workload else list(W.WORKLOADS)):
+            print(json.dumps(bench_backward(args, W.get(name))), flush=True)
         return 0
 
     if args.impl == "reference":
