@@ -665,8 +665,11 @@ def bench_ours(args, wl, rank, world, local_rank):
 
 def per_workload(args, dev, peak: float) -> dict:
     """Every named workload (the metric is per M x N x dtype), in both launch
-    modes, timed as the headline is: a CUDA graph of `steps` ABI calls over a
-    rotating pool (>= 3x L2) replayed back to back for at least 100 ms. Each
+    modes, timed as the headline is (a CUDA graph of ABI calls over a rotating
+    pool >= 3x L2, replayed back to back, here for at least 100 ms) except that
+    the graphs hold a fixed 200 calls whatever --steps is: these entries
+    describe the workloads, and a short graph would add its launch boundary
+    every few steps. Each
     entry: GB/s, fraction of the peak, the plan, and the DRAM traffic per
     launch from the committed ncu summary when it matches the current kernel
     sources and plan (else null)."""
@@ -677,7 +680,7 @@ def per_workload(args, dev, peak: float) -> dict:
     for name, wl in W.WORKLOADS.items():
         x_bits, w_bits = W.generate(wl)
         pb = PoolBench(wl, x_bits, w_bits, dev)
-        K = max(1, min(args.steps, 200))
+        K = 200
         entry = {"M": wl.M, "N": wl.N, "dtype": wl.dtype, "bytes_per_step": wl.algorithmic_bytes,
                  "pool_sets": pb.pool}
         for mode, early in (("early_loads", True), ("strict", False)):
