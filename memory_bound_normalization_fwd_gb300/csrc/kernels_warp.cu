@@ -230,17 +230,29 @@ bool warp_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) 
     l.work_items = a.M;
     l.grid = persistent_grid(a.M, static_cast<int64_t>(kWarps) * (32 / G), d.sm_count,
                              l.ctas_per_sm, k.max_ctas);
+    // Strict order, whole-warp teams of up to two vectors, many passes of rows
+    // per warp: fewer resident CTAs move the bytes faster (GB300, 1 KB rows:
+    // 65536 rows 5668 GB/s at 6 CTAs per SM, 5973 at 4; 131072 rows 5731 at 6,
+    // 6113 at 3; 65536x256 fp32 5714 at 6, 5886 at 4; up to ~5 passes, as at
+    // 16384 and 32768 rows, the full grid stays ahead).
+    const bool early_plan =
+        (k.flags & RMSNORM_FLAG_EARLY_LOADS) && !(k.flags & RMSNORM_FLAG_NO_PDL);
+    if (k.max_ctas == 0 && !early_plan && G == 32 && V <= 2 && D == 1) {
+        const int64_t passes = a.M / (static_cast<int64_t>(l.grid) * kWarps);
+        const int per_sm = passes >= 16 ? 3 : (passes >= 6 ? 4 : 0);
+        if (per_sm > 0 && per_sm < l.ctas_per_sm)
+            l.grid = persistent_grid(a.M, static_cast<int64_t>(kWarps), d.sm_count, per_sm, 0);
+    }
     // L2 prefetch: the caller's distance, or by default one pass ahead for
     // whole-warp teams under strict stream order when each team walks at least
     // two passes of rows (GB300, strict: 16384x512 bf16 4605 -> 4781 GB/s,
     // 16384x768 bf16 4688 -> 5057, 16384x256 fp32 4908 -> 5153; teams of 4-8
     // lanes, single-pass grids (2048x512) and early loads gain nothing or
     // lose). Never for operands in host memory (host-direct calls).
-    const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) && !(k.flags & RMSNORM_FLAG_NO_PDL);
     const int64_t pass_rows = static_cast<int64_t>(l.grid) * kWarps * (32 / G);
     if (k.l2_prefetch > 0)
         l.prefetch = k.l2_prefetch;
-    else if (k.l2_prefetch == 0 && G == 32 && !early && a.M >= 2 * pass_rows)
+    else if (k.l2_prefetch == 0 && G == 32 && !early_plan && a.M >= 2 * pass_rows)
         l.prefetch = 1;
     else
         l.prefetch = 0;
