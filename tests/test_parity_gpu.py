@@ -17,7 +17,7 @@ import torch
 import oracle
 from memory_bound_normalization_fwd_gb300 import binding as B
 from memory_bound_normalization_fwd_gb300 import workloads as W
-from parity_util import (DT, DeviceCase, compare, compare_blocked, oracle_rows,
+from parity_util import (DT, DeviceCase, compare, compare_blocked, compare_fp32, oracle_rows,
                          oracle_threaded, sample_rows)
 
 pytestmark = pytest.mark.gpu
@@ -85,6 +85,29 @@ def test_workload_full_size_automatic_launch(name, early, parity_report):
         ", ".join(f"{k}: {v}" for k, v in sorted(hist.items())) + f"), max rstd rel err {max_rel:.3g}")
     if wl.dtype == "fp16":
         assert abs(float(np.mean(r)) * wl.x_std - 1.0) < 0.01  # rstd ~ 1/64
+
+
+@pytest.mark.parametrize("M,N,dtype,max_per_sm", [(65536, 512, "bf16", 4), (131072, 512, "bf16", 3),
+                                                (65536, 256, "fp32", 4), (32768, 512, "bf16", 6)])
+def test_strict_warp_grid_for_many_passes(M, N, dtype, max_per_sm):
+    # Under strict order whole-warp teams that walk many passes of rows run
+    # fewer CTAs per SM (4 from 6 passes at the full grid, 3 from 16); the rows
+    # are the same work whatever the grid, so every row must still match.
+    wl = W.custom(M, N, dtype, seed=M + N)
+    x, w = W.generate(wl)
+    case = DeviceCase(x, w, dtype)
+    plan = _plan(M, N, dtype, case)
+    assert plan["variant"] == "warp" and plan["lanes_per_row"] == 32
+    assert plan["grid"] <= max_per_sm * plan["sm_count"]
+    assert case.run(wl.eps, wl.offset) == 0, B.rmsnorm_last_error()
+    y, r = case.results()
+    case.check_guards()
+    if dtype == "fp32":
+        _, ro, y64 = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, dtype, want_y64=True)
+        compare_fp32(y, r, y64, ro, where=f"{M}x{N}")
+    else:
+        yo, ro = oracle_threaded(x, w, wl.eps, wl.offset, dtype)
+        compare_blocked(y, r, yo, ro, dtype, where=f"{M}x{N}")
 
 
 # ---------------------------------------------------------------- every variant
