@@ -68,6 +68,9 @@ def parse_args(argv=None):
     p.add_argument("--cluster-size", type=int, default=0)
     p.add_argument("--l2-prefetch", type=int, default=0,
                    help="L2 prefetch distance (rmsnorm_options_t.l2_prefetch; 0 = planner's choice)")
+    p.add_argument("--prewait-prefetch", type=int, default=0,
+                   help="rows/chunks prefetched before the PDL wait "
+                        "(rmsnorm_options_t.prewait_prefetch; 0 = planner's choice, -1 = none)")
     p.add_argument("--ablation", action="store_true",
                    help="time a matrix of kernel variants and knobs per workload, one JSON line each")
     p.add_argument("--backward", action="store_true",
@@ -137,7 +140,7 @@ def kernel_hash(variant: str | None = None) -> str:
 
 
 PLAN_KEYS = ("variant", "threads", "grid", "lanes_per_row", "vecs_per_lane", "rows_per_stage",
-             "stages", "smem_bytes", "cluster_size", "l2_prefetch")
+             "stages", "smem_bytes", "cluster_size", "l2_prefetch", "prewait_prefetch")
 
 
 def load_traffic(workload: str, plan: dict, profiles_dir: str | None = None):
@@ -480,7 +483,8 @@ def bench_ours(args, wl, rank, world, local_rank):
                               stages=args.stages, rows_per_stage=args.rows_per_stage,
                               max_ctas=args.max_ctas, early_loads=early, blocked=args.blocked,
                               pdl=not args.no_pdl, cluster_size=args.cluster_size,
-                              early_weights=early_weights, l2_prefetch=args.l2_prefetch)
+                              early_weights=early_weights, l2_prefetch=args.l2_prefetch,
+                              prewait_prefetch=args.prewait_prefetch)
 
     # Main measurement. The steps are independent batches (x and w are written
     # by no step), which meets the precondition of RMSNORM_FLAG_EARLY_LOADS:
@@ -753,7 +757,8 @@ def launch_only(args, wl) -> dict:
                           stages=args.stages, rows_per_stage=args.rows_per_stage,
                           max_ctas=args.max_ctas, early_loads=not args.strict_order,
                           blocked=args.blocked, pdl=not args.no_pdl,
-                          cluster_size=args.cluster_size, l2_prefetch=args.l2_prefetch)
+                          cluster_size=args.cluster_size, l2_prefetch=args.l2_prefetch,
+                          prewait_prefetch=args.prewait_prefetch)
     plan = B.rmsnorm_plan_info(wl.M, wl.N, pb.dcode, pb.xs[0].data_ptr(), pb.w_dev.data_ptr(),
                                pb.ys[0].data_ptr(), opts)
     with torch.cuda.stream(pb.stream):
@@ -864,6 +869,7 @@ def bench_backward(args, wl):
     def make(early):
         return B.make_options(variant=args.variant, max_ctas=args.max_ctas,
                               lanes_per_row=args.lanes_per_row, l2_prefetch=args.l2_prefetch,
+                              prewait_prefetch=args.prewait_prefetch,
                               rows_per_stage=args.rows_per_stage, stages=args.stages,
                               early_loads=early)
     nbytes = B.rmsnorm_bwd_workspace_size(wl.M, wl.N, dcode, make(False))

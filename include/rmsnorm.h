@@ -119,8 +119,10 @@ typedef enum rmsnorm_variant {
 /* The caller promises that no kernel still running earlier on the stream
  * writes x or w. The kernel may then start reading them while the previous
  * kernel finishes (overlapping launches); its writes of y and rstd still wait
- * for that kernel to complete. Without the promise every access waits. Ignored
- * with RMSNORM_FLAG_NO_PDL and by the general kernel. */
+ * for that kernel to complete. Without the promise every read and write waits
+ * (the kernel may still ask for its first rows of x to be brought into L2
+ * before it waits: a hint that returns no values, see prewait_prefetch).
+ * Ignored with RMSNORM_FLAG_NO_PDL and by the general kernel. */
 #define RMSNORM_FLAG_EARLY_LOADS 4
 /* The caller promises only that no kernel still running earlier on the stream
  * writes w (a weight that is not being updated, as in inference); x may be
@@ -161,7 +163,18 @@ typedef struct rmsnorm_options {
                                 many chunks past its ring's stages (packed rows only).
                                 Ignored by the other variants and by rmsnorm_bwd.
                                 1..15; 0 = planner's choice; -1 = none */
-    int32_t reserved;        /* must be 0 */
+    int32_t prewait_prefetch; /* WARP and TMA: before it waits for the previous kernel on
+                                the stream, the kernel asks for its first rows to be brought
+                                into L2 (cp.async.bulk.prefetch.L2, a hint: x is still read
+                                after the wait, so the stream order is kept) and the WARP
+                                kernel lets the next kernel be scheduled at once. WARP: this
+                                many passes of each team's rows; TMA: this many chunks of
+                                each CTA's. Under RMSNORM_FLAG_EARLY_LOADS a positive count
+                                (or the planner, for the shapes where it measured faster)
+                                replaces the loads before the wait with it; -1 keeps them.
+                                Ignored by the other variants and by rmsnorm_bwd; without
+                                PDL the planner never picks it.
+                                1..15; 0 = planner's choice; -1 = none */
 } rmsnorm_options_t;
 
 /* What the planner picked (rmsnorm_plan_info). */
@@ -178,6 +191,8 @@ typedef struct rmsnorm_plan {
     int32_t sm_count;        /* SMs on the device */
     int32_t cluster_size;    /* CTAs per cluster (cluster variant; else 0) */
     int32_t l2_prefetch;     /* L2 prefetch distance in use (WARP, TMA; 0 = none) */
+    int32_t prewait_prefetch; /* pre-wait L2 prefetch in use (WARP passes, TMA chunks; 0 =
+                                none); when positive, x is read only after the wait */
 } rmsnorm_plan_t;
 
 /*

@@ -43,13 +43,14 @@ class Options(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("rows_per_stage", ctypes.c_int32),
                 ("flags", ctypes.c_int32), ("cluster_size", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64), ("l2_prefetch", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("prewait_prefetch", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "variant", "threads", "grid", "lanes_per_row", "vecs_per_lane", "rows_per_stage",
-        "stages", "smem_bytes", "ctas_per_sm", "sm_count", "cluster_size", "l2_prefetch")]
+        "stages", "smem_bytes", "ctas_per_sm", "sm_count", "cluster_size", "l2_prefetch",
+        "prewait_prefetch")]
 
     def as_dict(self) -> dict:
         d = {n: getattr(self, n) for n, _ in self._fields_}
@@ -137,13 +138,13 @@ def make_options(variant: str | int = "auto", max_ctas: int = 0, lanes_per_row: 
                  pdl: bool = True, blocked: bool = False, early_loads: bool = False,
                  cluster_size: int = 0, host_direct: bool = False,
                  early_weights: bool = False, bulk_store: bool = False,
-                 l2_prefetch: int = 0) -> Options:
+                 l2_prefetch: int = 0, prewait_prefetch: int = 0) -> Options:
     v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
     flags = ((0 if pdl else FLAG_NO_PDL) | (FLAG_BLOCKED_ROWS if blocked else 0)
              | (FLAG_EARLY_LOADS if early_loads else 0) | (FLAG_HOST_DIRECT if host_direct else 0)
              | (FLAG_EARLY_WEIGHTS if early_weights else 0) | (FLAG_BULK_STORE if bulk_store else 0))
     return Options(ctypes.sizeof(Options), v, max_ctas, lanes_per_row, stages, rows_per_stage,
-                   flags, cluster_size, wait_limit_ns, l2_prefetch, 0)
+                   flags, cluster_size, wait_limit_ns, l2_prefetch, prewait_prefetch)
 
 
 # ---- raw C ABI (integer device addresses) --------------------------------

@@ -119,7 +119,8 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
                     o->variant);
     if (o->max_ctas < 0 || o->lanes_per_row < 0 || o->rows_per_stage < 0 || o->stages < 0 ||
         o->stages > 8 || o->wait_limit_ns < 0 || o->cluster_size < 0 || o->cluster_size > 16 ||
-        o->l2_prefetch < -1 || o->l2_prefetch > kMaxPrefetch || o->reserved != 0 ||
+        o->l2_prefetch < -1 || o->l2_prefetch > kMaxPrefetch || o->prewait_prefetch < -1 ||
+        o->prewait_prefetch > kMaxPrefetch ||
         (o->flags & ~(RMSNORM_FLAG_NO_PDL | RMSNORM_FLAG_BLOCKED_ROWS | RMSNORM_FLAG_EARLY_LOADS |
                       RMSNORM_FLAG_HOST_DIRECT | RMSNORM_FLAG_EARLY_WEIGHTS |
                       RMSNORM_FLAG_BULK_STORE)) != 0)
@@ -133,6 +134,7 @@ int read_knobs(const rmsnorm_options_t* o, int* variant, Knobs* k) {
     k->wait_limit_ns = o->wait_limit_ns;
     k->cluster_size = o->cluster_size;
     k->l2_prefetch = o->l2_prefetch;
+    k->prewait_prefetch = o->prewait_prefetch;
     return RMSNORM_OK;
 }
 
@@ -141,10 +143,11 @@ namespace {
 // Chooses the variant. The automatic choice, when x, w and y are 16-byte
 // aligned and rows are whole 16-byte vectors (measured on GB300, bf16; the
 // limits are row bytes, so fp32 rows switch at half the column count):
-//   rows of up to 1536 bytes (768 bf16 columns) under strict stream order, and
-//     rows of up to 256 bytes in either mode: the warp-team kernel (ahead of
-//     the TMA kernel at N = 512 strict; with early loads the TMA kernel is
-//     ahead from N = 512 up, the warp kernel up to N = 128);
+//   rows of up to 256 bytes in either mode, and rows of up to 1536 bytes
+//     under strict stream order without the pre-wait prefetch (PDL off, or
+//     batches under 4 MB): the warp-team kernel (with early loads or the
+//     pre-wait prefetch the TMA kernel is ahead from N = 512 bf16 up, the warp
+//     kernel up to N = 128);
 //   rows of up to 16 KB (8192 columns): the TMA-staged kernel (ahead from
 //     N = 1000 to 8192);
 //   rows of up to 64 KB (32768 columns): the register CTA kernel (6.4 TB/s at
@@ -190,14 +193,22 @@ int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch
         case RMSNORM_VARIANT_GENERIC: ok = generic_choose(a, d, k, l); break;
         case RMSNORM_VARIANT_CLUSTER: ok = cluster_choose(a, d, k, l); break;
         default:
-            const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) &&
-                               !(k.flags & RMSNORM_FLAG_NO_PDL);
+            const bool pdl_on = !(k.flags & RMSNORM_FLAG_NO_PDL);
+            const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) && pdl_on;
             const int64_t row_bytes = a.N * elem_bytes(a.dtype);
+            // Under strict order the TMA kernel's pre-wait prefetch is ahead of
+            // the warp kernel from 512-byte rows up on batches of 4 MB or more
+            // (GB300, strict: 16384x512 bf16 6304 against 5592 GB/s, 16384x256
+            // bf16 4544 against 4284, 32768x192 fp32 6736 against 5992); without
+            // it (PDL off, or -1) the warp kernel stays ahead up to 1.5 KB rows.
+            const bool tma_prewait = pdl_on && k.prewait_prefetch >= 0 &&
+                                     a.M * row_bytes >= (int64_t{4} << 20);
             // Rows of up to 16 vectors would leave much of a TMA team (16 threads
             // at least) idle: the warp kernel takes them in both launch modes
             // (early loads, GB300: N = 64 bf16 4.97 against 2.47 TB/s, N = 128
             // 5.72 against 5.37; at N = 256 the two trade places by M).
-            if ((!early || row_bytes <= 256) && row_bytes <= 1536 && warp_choose(a, d, k, l)) {
+            if ((row_bytes <= 256 || (!early && !tma_prewait && row_bytes <= 1536)) &&
+                warp_choose(a, d, k, l)) {
                 variant = RMSNORM_VARIANT_WARP;
             } else if (row_bytes <= 16384 && (l = Launch{}, tma_choose(a, d, k, l)) &&
                        (l.stages >= 2 || k.stages > 0)) {
@@ -281,7 +292,7 @@ int forward_knobs(const void* x, int64_t ldx, const void* w, void* y, int64_t ld
     if (rc != RMSNORM_OK) return rc;
     l.pdl = (k.flags & RMSNORM_FLAG_NO_PDL) == 0;
     l.blocked = (k.flags & RMSNORM_FLAG_BLOCKED_ROWS) != 0;
-    l.early = l.pdl && (k.flags & RMSNORM_FLAG_EARLY_LOADS) != 0;
+    l.early = l.pdl && (k.flags & RMSNORM_FLAG_EARLY_LOADS) != 0 && !l.strict_x;
     l.early_weights = l.pdl && (k.flags & RMSNORM_FLAG_EARLY_WEIGHTS) != 0;
     e = run(chosen, a, l);
     if (e != cudaSuccess) return fail(RMSNORM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
@@ -493,6 +504,7 @@ extern "C" int rmsnorm_plan_info(int64_t M, int64_t N, int dtype, const void* x,
     out->sm_count = d.sm_count;
     out->cluster_size = l.cluster;
     out->l2_prefetch = l.prefetch;
+    out->prewait_prefetch = l.prewait;
     return RMSNORM_OK;
 }
 

@@ -55,8 +55,11 @@ __device__ __forceinline__ void team_barrier(int id, int threads) {
 // memory and leaves with one bulk copy per stage (cp.async.bulk shared ->
 // global, issued by the thread that issues the loads) instead of per-thread
 // 16-byte stores; the stage is reloaded only after that copy has read it.
-template <int DT, int THREADS, int TEAM, int V, bool CONTIG, bool BULK_ST>
-__global__ void __launch_bounds__(THREADS)
+// MINB: resident CTAs per SM the register budget must allow; 0 leaves the
+// register count to the compiler, 4 holds the lean 256-thread instances to 64
+// registers (four CTAs per SM, no spills for bf16).
+template <int DT, int THREADS, int TEAM, int V, bool CONTIG, bool BULK_ST, int MINB = 0>
+__global__ void __launch_bounds__(THREADS, MINB)
 tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __restrict__ rstd,
                 int64_t M, int nvec, int64_t ldx, int64_t ldy, float n, float eps, float offset,
                 int rows_per_stage,
@@ -99,6 +102,19 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         for (int st = 0; st < stages; ++st) mbar_init(bars + 8 * st, 1);
         fence_mbar_init();
     }
+    // L2 prefetch of local chunk k (a hint: no effect on the values read).
+    const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
+    auto prefetch_chunk = [&](int64_t k) {
+        const int64_t r0 = chunk_row(k);
+        const int64_t rows = (r_end - r0) < R ? (r_end - r0) : R;
+        if (CONTIG) {
+            bulk_prefetch_l2(x + r0 * nvec, static_cast<uint32_t>(rows) * row_bytes);
+        } else {
+            for (int64_t q = 0; q < rows; ++q) bulk_prefetch_l2(x + (r0 + q) * ldx, row_bytes);
+        }
+    };
+    const int PW = early ? 0 : mode_prewait(mode);  // chunks prefetched before the wait
+    const int64_t pf_from = stages > PW ? stages : PW;  // first chunk the ring prefetches
     // Local chunk k goes to stage k % stages (issued by thread 0 alone, in
     // increasing order).
     auto issue = [&](int64_t k) {
@@ -106,30 +122,32 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
         const int st = static_cast<int>(k % stages);
         const int64_t r0 = chunk_row(k);
         const int64_t rows = (r_end - r0) < R ? (r_end - r0) : R;
-        const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
         const uint32_t dst = smem_u32(buf + static_cast<int64_t>(st) * stage_stride);
         mbar_arrive_expect_tx(bars + 8 * st, static_cast<uint32_t>(rows) * row_bytes);
         if (CONTIG) {  // contiguous rows: the whole stage is one span of x
             bulk_g2s(dst, x + r0 * nvec, static_cast<uint32_t>(rows) * row_bytes, bars + 8 * st);
             // L2 prefetch of the chunk P issues ahead (chunks below `stages` are
-            // the ring's first loads, so each later chunk is asked for once).
+            // the ring's first loads, and chunks below PW were asked for before
+            // the wait, so each later chunk is asked for once).
             const int64_t kp = k + mode_prefetch(mode);
-            if (kp > k && kp >= stages && kp < nchunks) {
-                const int64_t rp = chunk_row(kp);
-                const int64_t nrp = (r_end - rp) < R ? (r_end - rp) : R;
-                bulk_prefetch_l2(x + rp * nvec, static_cast<uint32_t>(nrp) * row_bytes);
-            }
+            if (kp > k && kp >= pf_from && kp < nchunks) prefetch_chunk(kp);
         } else {       // strided rows: one copy per row, all counted on the same barrier
             for (int64_t q = 0; q < rows; ++q)
                 bulk_g2s(dst + static_cast<uint32_t>(q) * row_bytes, x + (r0 + q) * ldx, row_bytes,
                          bars + 8 * st);
         }
     };
-    // No global memory is touched before the previous kernel completes, unless the
+    // No global memory is read before the previous kernel completes, unless the
     // caller promised w (early weights) or x and w (early loads) are not being
-    // written: then those reads go first and only the rest waits. The weight
-    // loads are issued, then the first stages' copies, and only then are the
-    // weights converted, so the weights' L2 round trip hides under the copies.
+    // written: then those reads go first and only the rest waits. Before the
+    // wait, thread 0 may ask for this CTA's first PW chunks to be brought into
+    // L2 while the previous kernel finishes (the copies after the wait see its
+    // writes all the same). The weight loads are issued, then the first
+    // stages' copies, and only then are the weights converted, so the weights'
+    // L2 round trip hides under the copies.
+    if (PW > 0 && tid == 0) {
+        for (int64_t kk = 0; kk < PW && kk < nchunks; ++kk) prefetch_chunk(kk);
+    }
     if (!early && !early_w) pdl_wait();
     uint4 wv[V];
 #pragma unroll
@@ -273,6 +291,18 @@ Fn pick(int team, int V, bool contig, bool bulk_store) {
     return pick_c<DT, false, false>(team, V);  // strided rows keep per-thread stores
 }
 
+// Lean instances (four 256-thread CTAs per SM) for packed bf16 rows of 512
+// bytes to 4 KB; nullptr for other shapes. (The fp16 body needs about 107
+// registers at these shapes, so it would spill at 64.)
+template <int DT>
+Fn pick_lean(int team, int V) {
+    if (team == 16 && V == 2) return tma_rows_kernel<DT, 256, 16, 2, true, false, 4>;
+    if (team == 16 && V == 4) return tma_rows_kernel<DT, 256, 16, 4, true, false, 4>;
+    if (team == 32 && V == 4) return tma_rows_kernel<DT, 256, 32, 4, true, false, 4>;
+    if (team == 64 && V == 4) return tma_rows_kernel<DT, 256, 64, 4, true, false, 4>;
+    return nullptr;
+}
+
 // Opts a TMA kernel into all of the device's dynamic shared memory, once per
 // device; returns that byte count (0 on failure). Later calls touch only a cache,
 // so planning makes no CUDA call (and stays legal inside stream capture).
@@ -320,9 +350,36 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     if (V > 4) return false;
     const bool contig = a.ldx == a.N && a.ldy == a.N;
     const bool bulk = (k.flags & RMSNORM_FLAG_BULK_STORE) != 0;
-    Fn fn = a.dtype == kBF16   ? pick<kBF16>(team, V, contig, bulk)
-            : a.dtype == kFP16 ? pick<kFP16>(team, V, contig, bulk)
-                               : pick<kFP32>(team, V, contig, bulk);
+    const int64_t row_bytes = nvec * 16;
+    const int64_t x_bytes = a.M * row_bytes;
+    // Pre-wait prefetch instead of loads before the wait: always under strict
+    // stream order (unless the caller says -1 or PDL is off); with early loads
+    // allowed, when the caller asks for it, and by default for bf16 and fp32
+    // rows of 512 B to 4 KB in batches of 4 MB or more (16 MB for 512-byte
+    // rows), where it measured faster than loading the first stages before the
+    // wait (GB300, GB/s early loads -> pre-wait prefetch: 16384x512 bf16 5919
+    // -> 6305, 32768x512 bf16 6423 -> 6859, 16384x1024 bf16 5752 -> 6869,
+    // 65536x256 bf16 6429 -> 6888, 32768x1000 bf16 6596 -> 6783, 16384x512
+    // fp32 6414 -> 6967; 16384x256 bf16 4727 -> 4526, 16384x512 fp16 5661 ->
+    // 5476, 2 MB batches and 8-16 KB rows the other way round or even).
+    const bool pdl_on = !(k.flags & RMSNORM_FLAG_NO_PDL);
+    const bool early_flag = (k.flags & RMSNORM_FLAG_EARLY_LOADS) && pdl_on;
+    const bool early_prewait = a.dtype != kFP16 && row_bytes >= 512 && row_bytes < 4096 &&
+                               x_bytes >= (int64_t{row_bytes > 512 ? 4 : 16} << 20);
+    const bool prewait_path = pdl_on && k.prewait_prefetch >= 0 &&
+                              (k.prewait_prefetch > 0 || !early_flag || early_prewait);
+    const bool early = early_flag && !prewait_path;  // first stages loaded before the wait
+    // Lean instances (four CTAs per SM instead of three) with the pre-wait
+    // prefetch on bf16 batches of up to 48 MB (GB300, strict: 16384x512 6065 ->
+    // 6304 GB/s, 32768x512 6671 -> 6852, 16384x768 6034 -> 6491; 65536x512
+    // 6798 -> 6589 and 32768x1000 6782 -> 6571 the other way round).
+    const bool lean = prewait_path && a.dtype == kBF16 && contig && !bulk &&
+                      x_bytes <= (int64_t{48} << 20);
+    Fn fn = lean ? pick_lean<kBF16>(team, V) : nullptr;
+    if (!fn)
+        fn = a.dtype == kBF16   ? pick<kBF16>(team, V, contig, bulk)
+             : a.dtype == kFP16 ? pick<kFP16>(team, V, contig, bulk)
+                                : pick<kFP32>(team, V, contig, bulk);
     if (!fn) return false;
     const int threads = team < 256 ? 256 : team;
     const int teams = threads / team;
@@ -330,7 +387,6 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     const int max_dyn = max_dynamic_smem(reinterpret_cast<const void*>(fn), d.max_smem_optin);
     if (max_dyn <= 0) return false;
 
-    const int64_t row_bytes = nvec * 16;
     // Stage shape, measured on GB300 (1 KB .. 16 KB rows): rows under 4 KB take
     // 16 KB stages, two deep (small footprint, so the next launch's CTAs fit in
     // early); 4-8 KB rows take 32 KB stages, four deep. Longer 16-bit rows take
@@ -352,7 +408,6 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     const int64_t stage_stride = (R * row_bytes + 127) / 128 * 128;
     // With early loads, 2-4 KB rows gain from four stages too (32768x1000 bf16:
     // 6.6-6.75 TB/s against 6.1-6.55 at two stages); 1 KB rows do not.
-    const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) && !(k.flags & RMSNORM_FLAG_NO_PDL);
     int S = k.stages > 0 ? k.stages
                          : (short_rows && !(early && row_bytes >= 2048) ? 2 : (long_narrow ? 3 : 4));
     if (S < 1 || S > kMaxStages) return false;
@@ -374,6 +429,22 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     l.grid = persistent_grid(l.work_items, 1, d.sm_count, l.ctas_per_sm, k.max_ctas);
     l.wait_limit_ns = k.wait_limit_ns > 0 ? k.wait_limit_ns : 1000000000LL;
     l.prefetch = (contig && k.l2_prefetch > 0) ? k.l2_prefetch : 0;
+    // Pre-wait prefetch: the caller's chunk count, or by default about half the
+    // chunks each CTA walks, one to three (GB300, strict, GB/s without -> with:
+    // 32768x1000 bf16 6154 -> 6763 at three chunks, 16384x512 fp32 5687 -> 6946
+    // at two, 16384x2048 bf16 5154 -> 5657 at two, 16384x8192 bf16 6260 ->
+    // 6360; lean 16384x512 bf16, under two chunks per CTA: 6304 at one, 5694 at
+    // two, where the prefetches of the next launch slow this one's last chunks).
+    const int64_t chunks_per_cta = l.grid > 0 ? (l.work_items + l.grid - 1) / l.grid : 0;
+    l.strict_x = early_flag && prewait_path;
+    if (!prewait_path) {
+        l.prewait = 0;
+    } else if (k.prewait_prefetch > 0) {
+        l.prewait = k.prewait_prefetch;
+    } else {
+        const int64_t pw = (chunks_per_cta + 1) / 2;
+        l.prewait = static_cast<int>(pw < 1 ? 1 : (pw > 3 ? 3 : pw));
+    }
     return true;
 }
 

@@ -87,15 +87,28 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
     // into L2, and later, each time a slot is refilled, for the row P passes
     // past the refill, so rows come from L2 when their turn in registers comes.
     const int P = mode_prefetch(mode);
+    const int PW = early ? 0 : mode_prewait(mode);  // passes prefetched before the wait
     const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
-    auto prefetch_first = [&]() {
-        if (P > 0 && sub == 0) {
-            for (int p = D; p < D + P; ++p) {
+    auto prefetch_passes = [&](int p0, int p1) {
+        if (sub == 0) {
+            for (int p = p0; p < p1; ++p) {
                 const int64_t prow = first0 + p * stride + team;
                 if (prow < r_end) bulk_prefetch_l2(x + prow * ldx, row_bytes);
             }
         }
     };
+    auto prefetch_first = [&]() {
+        if (P > 0) prefetch_passes(D > PW ? D : PW, D + P);
+    };
+    // Pre-wait prefetch (x not read before the wait): the next kernel may be
+    // scheduled now, and the team's first PW passes of rows are asked into L2
+    // while the previous kernel finishes; the loads after the wait see its
+    // writes all the same (a prefetch only moves lines into L2, where every
+    // store lands).
+    if (PW > 0) {
+        pdl_launch_dependents();
+        prefetch_passes(0, PW);
+    }
     const bool x_first = early || !early_w;
     if (!early && !early_w) pdl_wait();
     if (x_first) {
@@ -105,12 +118,13 @@ warp_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* _
     for (int i = threadIdx.x; i < nvec; i += kWarps * 32)
         weights_vec_to_smem<DT>(__ldg(w + i), offset, sw, i);
     __syncthreads();
-    // The next kernel on the stream may be scheduled early only when the caller
-    // promised launch overlap; under strict order it is launched at this
-    // kernel's exit, which measured faster on GB300 (16384x512 bf16 4725 ->
-    // 4898 GB/s, 2048x512 1590 -> 1652; the staged kernel is the other way
-    // round and keeps the early trigger).
-    if (early || early_w) pdl_launch_dependents();
+    // The next kernel on the stream may be scheduled early when the caller
+    // promised launch overlap, or (above) when it will prefetch before its wait;
+    // otherwise, under strict order, it is launched at this kernel's exit,
+    // which measured faster on GB300 when nothing is done before the wait
+    // (16384x512 bf16 4725 -> 4898 GB/s, 2048x512 1590 -> 1652; the staged
+    // kernel is the other way round and keeps the early trigger).
+    if ((early || early_w) && PW == 0) pdl_launch_dependents();
     if (!x_first) {
         pdl_wait();  // x only after the previous kernel completes
         load_first();
@@ -231,32 +245,70 @@ bool warp_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) 
     l.grid = persistent_grid(a.M, static_cast<int64_t>(kWarps) * (32 / G), d.sm_count,
                              l.ctas_per_sm, k.max_ctas);
     // Strict order, whole-warp teams of up to two vectors, many passes of rows
-    // per warp: fewer resident CTAs move the bytes faster (GB300, 1 KB rows:
-    // 65536 rows 5668 GB/s at 6 CTAs per SM, 5973 at 4; 131072 rows 5731 at 6,
-    // 6113 at 3; 65536x256 fp32 5714 at 6, 5886 at 4; up to ~5 passes, as at
-    // 16384 and 32768 rows, the full grid stays ahead).
-    const bool early_plan =
+    // per warp: half the resident CTAs move the bytes faster once each warp
+    // walks 16 passes or more (GB300, 1 KB rows with the pre-wait prefetch
+    // below: 131072 rows 6156 GB/s at 3 CTAs per SM, 6026 at 6; at 65536 rows
+    // the full grid stays ahead, 6187 against 6079).
+    // Loads before the wait when the caller allows them, unless the caller asks
+    // for the pre-wait prefetch instead.
+    const bool early_flag =
         (k.flags & RMSNORM_FLAG_EARLY_LOADS) && !(k.flags & RMSNORM_FLAG_NO_PDL);
+    const bool early_plan = early_flag && k.prewait_prefetch <= 0;
     if (k.max_ctas == 0 && !early_plan && G == 32 && V <= 2 && D == 1) {
         const int64_t passes = a.M / (static_cast<int64_t>(l.grid) * kWarps);
-        const int per_sm = passes >= 16 ? 3 : (passes >= 6 ? 4 : 0);
-        if (per_sm > 0 && per_sm < l.ctas_per_sm)
-            l.grid = persistent_grid(a.M, static_cast<int64_t>(kWarps), d.sm_count, per_sm, 0);
+        if (passes >= 16 && 2 * 3 <= l.ctas_per_sm)
+            l.grid = persistent_grid(a.M, static_cast<int64_t>(kWarps), d.sm_count, 3, 0);
     }
-    // L2 prefetch: the caller's distance, or by default one pass ahead for
-    // whole-warp teams under strict stream order when each team walks at least
-    // two passes of rows (GB300, strict: 16384x512 bf16 4605 -> 4781 GB/s,
-    // 16384x768 bf16 4688 -> 5057, 16384x256 fp32 4908 -> 5153; teams of 4-8
-    // lanes, single-pass grids (2048x512) and early loads gain nothing or
+    // Pre-wait prefetch (x read only after the wait). It pays when the next
+    // launch's CTAs start as this one's retire (a full grid), when all of them
+    // fit beside it (at most half the resident slots), or when each CTA takes a
+    // single pass of rows; it loses when only part of the next grid fits early
+    // (GB300, 65536x512 bf16 at 4 of 6 CTAs per SM: 5811 -> 5418 GB/s) and on
+    // batches under 4 MB, which launch latency bounds. By default it covers
+    // about 8 KB of rows per CTA for teams of 8 or 32 lanes, which then also
+    // prefetch one pass ahead in the loop, and three passes for other teams
+    // (GB300, strict, GB/s without -> with: 16384x512 bf16 4734 -> 5580,
+    // 32768x512 bf16 5574 -> 6312, 16384x768 bf16 5171 -> 6045, 16384x384 bf16
+    // 4128 -> 4498, 65536x256 bf16 5369 -> 6207, 65536x128 bf16 4485 -> 5462,
+    // 16384x256 fp32 4735 -> 6088, 16384x128 fp32 3931 -> 5358).
+    const bool pdl_on = !(k.flags & RMSNORM_FLAG_NO_PDL);
+    const int64_t rows_per_cta_pass = static_cast<int64_t>(kWarps) * (32 / G);
+    const int64_t pass_rows = static_cast<int64_t>(l.grid) * rows_per_cta_pass;
+    const int64_t slots = static_cast<int64_t>(l.ctas_per_sm) * d.sm_count;
+    const bool grid_fits = l.grid == slots || 2 * static_cast<int64_t>(l.grid) <= slots ||
+                           a.M <= pass_rows;
+    const bool prewait_auto = k.prewait_prefetch == 0 && pdl_on && !early_plan && grid_fits &&
+                              a.M * nvec * 16 >= (int64_t{4} << 20);
+    const bool loop_teams = G == 32 || G == 8;  // teams that prefetch in the loop too
+    if (k.prewait_prefetch > 0) {
+        l.prewait = k.prewait_prefetch;
+    } else if (prewait_auto) {
+        const int64_t cta_pass_bytes = rows_per_cta_pass * nvec * 16;
+        const int64_t pw = loop_teams ? (8192 + cta_pass_bytes - 1) / cta_pass_bytes : 3;
+        l.prewait = static_cast<int>(pw < 1 ? 1 : (pw > kMaxPrefetch ? kMaxPrefetch : pw));
+    } else {
+        l.prewait = 0;
+    }
+    // L2 prefetch in the loop: the caller's distance, or by default one pass
+    // ahead for teams of 8 or 32 lanes with the pre-wait prefetch, and for
+    // whole-warp teams under strict order when each team walks at least two
+    // passes of rows (GB300, strict without the pre-wait prefetch: 16384x512
+    // bf16 4605 -> 4781 GB/s, 16384x768 bf16 4688 -> 5057; teams of 4 lanes,
+    // single-pass grids without it (2048x512) and early loads gain nothing or
     // lose). Never for operands in host memory (host-direct calls).
-    const int64_t pass_rows = static_cast<int64_t>(l.grid) * kWarps * (32 / G);
     if (k.l2_prefetch > 0)
         l.prefetch = k.l2_prefetch;
+    else if (k.l2_prefetch == 0 && loop_teams && l.prewait > 0 && k.prewait_prefetch == 0)
+        l.prefetch = 1;
     else if (k.l2_prefetch == 0 && G == 32 && !early_plan && a.M >= 2 * pass_rows)
         l.prefetch = 1;
     else
         l.prefetch = 0;
-    if (k.flags & kKnobNoBulkCopies) l.prefetch = 0;
+    if (k.flags & kKnobNoBulkCopies) {
+        l.prefetch = 0;
+        l.prewait = 0;
+    }
+    l.strict_x = early_flag && l.prewait > 0;
     return true;
 }
 

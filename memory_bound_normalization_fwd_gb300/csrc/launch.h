@@ -41,6 +41,16 @@ constexpr int kMaxPrefetch = 15;
 __host__ __device__ inline int mode_prefetch(int mode) {
     return (mode >> kModePrefetchShift) & kMaxPrefetch;
 }
+// Bits 12..15: pre-wait L2 prefetch (0 = none; ignored with early loads). The
+// kernel lets the next kernel on the stream be scheduled at once and asks for
+// its first rows (WARP: this many passes of each team's rows; TMA: this many
+// chunks of each CTA's) to be brought into L2 before it waits for the previous
+// kernel. A prefetch is only a hint: the loads after the wait still return
+// every write of the previous kernel.
+constexpr int kModePrewaitShift = 12;
+__host__ __device__ inline int mode_prewait(int mode) {
+    return (mode >> kModePrewaitShift) & kMaxPrefetch;
+}
 
 // A launch shape chosen by a variant's planner.
 struct Launch {
@@ -62,11 +72,14 @@ struct Launch {
     bool early = false;    // x and w may be read before the previous kernel completes
     bool early_weights = false;  // w may be read before the previous kernel completes
     int prefetch = 0;            // L2 prefetch distance (kModePrefetchShift); 0 = none
+    int prewait = 0;             // pre-wait L2 prefetch (kModePrewaitShift); 0 = none
+    bool strict_x = false;       // x read only after the wait although the caller allowed early loads
     bool bwd_warp = false;       // backward: the warp-per-row kernel
     bool bwd_tma = false;        // backward: the staged kernel
     int mode() const {
         return (blocked ? kModeBlocked : 0) | (early ? kModeEarlyLoads : 0) |
-               (early_weights ? kModeEarlyWeights : 0) | (prefetch << kModePrefetchShift);
+               (early_weights ? kModeEarlyWeights : 0) | (prefetch << kModePrefetchShift) |
+               (prewait << kModePrewaitShift);
     }
 };
 
@@ -84,6 +97,7 @@ struct Knobs {
     int cluster_size = 0;
     int64_t wait_limit_ns = 0;
     int l2_prefetch = 0;  // -1 none, 0 planner's choice, 1..kMaxPrefetch distance
+    int prewait_prefetch = 0;  // -1 none, 0 planner's choice, 1..kMaxPrefetch passes/chunks
 };
 
 // Device facts, cached per device by the front end.

@@ -132,7 +132,8 @@ def test_m_zero_is_ok_without_buffers(lib):
                                          ("lanes_per_row", -2), ("struct_size", 8),
                                          ("flags", 64), ("cluster_size", 17),
                                          ("cluster_size", -1), ("l2_prefetch", -2),
-                                         ("l2_prefetch", 16), ("reserved", 1)])
+                                         ("l2_prefetch", 16), ("prewait_prefetch", -2),
+                                         ("prewait_prefetch", 16)])
 def test_bad_options(lib, field, value):
     o = B.make_options()
     setattr(o, field, value)

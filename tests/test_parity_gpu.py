@@ -87,19 +87,21 @@ def test_workload_full_size_automatic_launch(name, early, parity_report):
         assert abs(float(np.mean(r)) * wl.x_std - 1.0) < 0.01  # rstd ~ 1/64
 
 
-@pytest.mark.parametrize("M,N,dtype,max_per_sm", [(65536, 512, "bf16", 4), (131072, 512, "bf16", 3),
-                                                (65536, 256, "fp32", 4), (32768, 512, "bf16", 6)])
+@pytest.mark.parametrize("M,N,dtype,max_per_sm", [(65536, 512, "bf16", 6), (131072, 512, "bf16", 3),
+                                                (65536, 256, "fp32", 6), (32768, 512, "bf16", 6)])
 def test_strict_warp_grid_for_many_passes(M, N, dtype, max_per_sm):
-    # Under strict order whole-warp teams that walk many passes of rows run
-    # fewer CTAs per SM (4 from 6 passes at the full grid, 3 from 16); the rows
-    # are the same work whatever the grid, so every row must still match.
+    # Under strict order the warp kernel's whole-warp teams that walk 16 passes
+    # of rows or more run half the resident CTAs, and every plan here
+    # prefetches its first rows into L2 before the wait; the rows are the same
+    # work whatever the grid, so every row must still match.
     wl = W.custom(M, N, dtype, seed=M + N)
     x, w = W.generate(wl)
     case = DeviceCase(x, w, dtype)
-    plan = _plan(M, N, dtype, case)
+    plan = _plan(M, N, dtype, case, variant="warp")
     assert plan["variant"] == "warp" and plan["lanes_per_row"] == 32
     assert plan["grid"] <= max_per_sm * plan["sm_count"]
-    assert case.run(wl.eps, wl.offset) == 0, B.rmsnorm_last_error()
+    assert plan["prewait_prefetch"] >= 1 and plan["l2_prefetch"] == 1
+    assert case.run(wl.eps, wl.offset, variant="warp") == 0, B.rmsnorm_last_error()
     y, r = case.results()
     case.check_guards()
     if dtype == "fp32":
@@ -166,6 +168,100 @@ def test_l2_prefetch_parity(variant, G, M, N, P):
                    lanes_per_row=G, l2_prefetch=P, max_ctas=2, expect_variant=variant)
     plan = _plan(M, N, "bf16", variant=variant, lanes_per_row=G, l2_prefetch=P)
     assert plan["l2_prefetch"] == P
+
+
+@pytest.mark.parametrize("variant,G", [("warp", 32), ("warp", 8), ("warp", 4), ("tma", 0),
+                                       ("tma", 64)])
+@pytest.mark.parametrize("M,N", [(37, 512), (1000, 256), (130, 520), (64, 4096), (4099, 1000)])
+@pytest.mark.parametrize("PW", [1, 4, 15])
+def test_prewait_prefetch_parity(variant, G, M, N, PW):
+    # Rows (warp) or chunks (TMA) asked into L2 before the wait for the previous
+    # kernel: a hint only, so the bits must not change. Strict order and early
+    # weights, strided and blocked rows, one CTA walking every row, in place,
+    # and row strides wider than the row (one prefetch per row).
+    if G and (N // 8 + G - 1) // G > 4:
+        pytest.skip("more than 4 vectors per lane")
+    wl = W.custom(M, N, "bf16", seed=M + N + PW + G, offset=float(PW % 2))
+    x, w = W.generate(wl)
+    for max_ctas, blocked, early_w in ((0, False, False), (1, False, True), (3, True, False),
+                                       (5, False, True)):
+        _run_and_check(x, w, "bf16", wl.eps, wl.offset, variant=variant, lanes_per_row=G,
+                       prewait_prefetch=PW, max_ctas=max_ctas, blocked=blocked,
+                       early_weights=early_w, expect_variant=variant)
+    _run_and_check(x, w, "bf16", wl.eps, wl.offset, inplace=True, variant=variant,
+                   lanes_per_row=G, prewait_prefetch=PW, max_ctas=2, expect_variant=variant)
+    plan = _plan(M, N, "bf16", variant=variant, lanes_per_row=G, prewait_prefetch=PW)
+    assert plan["prewait_prefetch"] == PW
+    ldx = ldy = N + 24
+    _, _, xd, yd = _strided_case(x, w, "bf16", ldx, ldy)
+    wd = W.to_torch(w, "bf16").cuda()
+    rd = torch.full((M,), -1.0, dtype=torch.float32, device="cuda")
+    o = B.make_options(variant=variant, lanes_per_row=G, prewait_prefetch=PW)
+    rc = B.rmsnorm_fwd_strided(xd.data_ptr(), ldx, wd.data_ptr(), yd.data_ptr(), ldy,
+                               rd.data_ptr(), M, N, wl.eps, wl.offset, B.BF16, o,
+                               torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, B.rmsnorm_last_error()
+    torch.cuda.synchronize()
+    yo, ro = oracle.rmsnorm_fwd(x, w, wl.eps, wl.offset, "bf16")
+    yg = W.from_torch(yd).reshape(M, ldy)
+    compare(yg[:, :N], rd.cpu().numpy(), yo, ro, "bf16", where=f"strided {M}x{N}")
+
+
+@pytest.mark.parametrize("M,N,dtype,variant,per_sm,pw,P,early_pw", [
+    (16384, 512, "bf16", "tma", 4, 1, 0, 1), (16384, 384, "bf16", "tma", 4, 1, 0, 1),
+    (32768, 512, "bf16", "tma", 4, 2, 0, 2), (65536, 512, "bf16", "tma", 3, 3, 0, 3),
+    (65536, 256, "bf16", "tma", 4, 2, 0, 2), (16384, 256, "bf16", "tma", 4, 1, 0, 0),
+    (65536, 128, "bf16", "warp", 3, 3, 0, 0), (2048, 512, "bf16", "warp", 6, 0, 0, 0),
+    (16384, 256, "fp32", "tma", 4, 1, 0, 1), (16384, 512, "fp32", "tma", 4, 2, 0, 2),
+    (16384, 512, "fp16", "tma", 2, 2, 0, 0), (32768, 1000, "bf16", "tma", 3, 3, 0, 3),
+    (16384, 8192, "bf16", "tma", 2, 3, 0, 0)])
+def test_automatic_prewait_plan(M, N, dtype, variant, per_sm, pw, P, early_pw):
+    # The planner's pre-wait prefetch under strict order: the kernel, its CTAs
+    # per SM (four for the lean bf16 instances on batches up to 48 MB), the
+    # rows or chunks it covers and the loop's own prefetch distance; with early
+    # loads allowed, where it replaces the loads before the wait (early_pw > 0)
+    # and where it does not; none without PDL or when the caller says -1.
+    plan = _plan(M, N, dtype)
+    assert plan["variant"] == variant and plan["ctas_per_sm"] == per_sm
+    assert (plan["prewait_prefetch"], plan["l2_prefetch"]) == (pw, P)
+    assert _plan(M, N, dtype, early_loads=True)["prewait_prefetch"] == early_pw
+    assert _plan(M, N, dtype, pdl=False)["prewait_prefetch"] == 0
+    assert _plan(M, N, dtype, prewait_prefetch=-1)["prewait_prefetch"] == 0
+    assert _plan(M, N, dtype, early_loads=True, prewait_prefetch=-1)["prewait_prefetch"] == 0
+
+
+@pytest.mark.parametrize("variant,N", [("warp", 512), ("warp", 256), ("tma", 1000), ("tma", 2048)])
+@pytest.mark.parametrize("pw", [0, 1, 4])
+def test_prewait_chain_keeps_stream_order(variant, N, pw):
+    # A dependent chain at a size where the automatic plan prefetches before the
+    # wait (each call reads the previous call's output): bit-identical to the
+    # same calls separated by a device synchronize.
+    M = 16384
+    wl = W.custom(M, N, "bf16", seed=N + pw)
+    x, w = W.generate(wl)
+    w_dev = W.to_torch(w, "bf16").cuda()
+    if pw:
+        assert _plan(M, N, "bf16", variant=variant, prewait_prefetch=pw)["prewait_prefetch"] == pw
+    else:
+        assert _plan(M, N, "bf16", variant=variant)["prewait_prefetch"] > 0
+
+    def chain(sync: bool):
+        a = W.to_torch(x, "bf16").cuda()
+        b = torch.empty_like(a)
+        r = torch.empty(M, dtype=torch.float32, device="cuda")
+        for _ in range(6):
+            _raw_call(a, w_dev, b, r, M, N, 1e-6, 0.0, variant=variant, prewait_prefetch=pw)
+            if sync:
+                torch.cuda.synchronize()
+            _raw_call(b, w_dev, a, r, M, N, 1e-6, 0.0, variant=variant, prewait_prefetch=pw)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return W.from_torch(a), r.cpu().numpy()
+
+    ya, ra = chain(False)
+    yb, rb = chain(True)
+    assert np.array_equal(ya, yb) and np.array_equal(ra, rb)
 
 
 @pytest.mark.parametrize("T", [64, 128, 256, 512, 1024])
