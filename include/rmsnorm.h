@@ -172,8 +172,9 @@ typedef struct rmsnorm_options {
                                 each CTA's. Under RMSNORM_FLAG_EARLY_LOADS a positive count
                                 (or the planner, for the shapes where it measured faster)
                                 replaces the loads before the wait with it; -1 keeps them.
-                                Ignored by the other variants and by rmsnorm_bwd; without
-                                PDL the planner never picks it.
+                                rmsnorm_bwd: the warp and CTA row kernels prefetch this many
+                                of their first rows of x and dy (default 1). Ignored by the
+                                other variants; without PDL the planner never picks it.
                                 1..15; 0 = planner's choice; -1 = none */
 } rmsnorm_options_t;
 

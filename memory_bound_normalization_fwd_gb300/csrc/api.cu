@@ -534,6 +534,7 @@ extern "C" int rmsnorm_bwd_plan_info(int64_t M, int64_t N, int dtype, const rmsn
     out->smem_bytes = l.smem;
     out->ctas_per_sm = l.ctas_per_sm;
     out->sm_count = d.sm_count;
+    out->prewait_prefetch = l.prewait;
     return RMSNORM_OK;
 }
 

@@ -138,6 +138,19 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
         }
     };
 
+    // Pre-wait prefetch: thread 0 asks for the CTA's first PW rows of x and dy
+    // to be brought into L2 before the wait (a hint; the loads after the wait
+    // see the previous kernel's writes all the same).
+    const int PW = mode_prewait(mode);
+    if (PW > 0 && tid == 0) {
+        const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
+        for (int p = 0; p < PW; ++p) {
+            const int64_t rw = blockIdx.x + static_cast<int64_t>(p) * gridDim.x;
+            if (rw >= M) break;
+            bulk_prefetch_l2(x + rw * nvec, row_bytes);
+            bulk_prefetch_l2(dy + rw * nvec, row_bytes);
+        }
+    }
     if (!early) pdl_wait();
     int64_t row = blockIdx.x;
     load_x(row);
@@ -198,10 +211,12 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 //
 // Rows ahead: each warp loads its next row's x, dy and rstd into registers
 // before reducing the current one (one row in flight ahead: 3.84 -> 3.98 TB/s
-// at 16384x512). L2 prefetch of rows further ahead (cp.async.bulk.prefetch)
-// measured slower on GB300, both beside the register row (16384x512 bf16:
-// 3944 -> 3580 GB/s at one pass, 3282 at four) and instead of it (12-15%
-// slower, although it freed a fourth CTA per SM), so there is none.
+// at 16384x512). L2 prefetch of rows further ahead inside the loop
+// (cp.async.bulk.prefetch) measured slower on GB300, both beside the register
+// row (16384x512 bf16: 3944 -> 3580 GB/s at one pass, 3282 at four) and
+// instead of it (12-15% slower, although it freed a fourth CTA per SM); only
+// the first rows are prefetched, before the wait (3973 -> 4194 strict). A
+// 64-register build (four CTAs per SM) spills and ran 3335.
 template <int DT, int V>
 __global__ void __launch_bounds__(256)
 bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __restrict__ rstd,
@@ -237,6 +252,19 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
     const bool early = (mode & kModeEarlyLoads) != 0;
     uint4 xv[V], gv[V];
     float r;
+    // Pre-wait prefetch: each warp's first lane asks for the warp's first PW
+    // rows of x and dy to be brought into L2 before the wait (a hint; the
+    // loads after the wait see the previous kernel's writes all the same).
+    const int PW = mode_prewait(mode);
+    if (PW > 0 && lane == 0) {
+        const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
+        for (int p = 0; p < PW; ++p) {
+            const int64_t rw = row + p * stride;
+            if (rw >= M) break;
+            bulk_prefetch_l2(x + rw * nvec, row_bytes);
+            bulk_prefetch_l2(dy + rw * nvec, row_bytes);
+        }
+    }
     if (!early) pdl_wait();
     load(row, xv, gv, r, 0);
     pdl_launch_dependents();
@@ -555,11 +583,13 @@ __global__ void __launch_bounds__(1024)
 dw_reduce_kernel(const float* __restrict__ partial, float* __restrict__ dw, int G, int64_t N,
                  int early) {
     __shared__ float red[32][33];
-    // With early loads the next kernel on the stream may be scheduled at once
-    // (it reads only what the caller promised is not being written before its
-    // own wait): 16384x512 bf16 backward 3988 -> 4179 GB/s on GB300. Under
-    // strict order it is launched at this kernel's exit, which measured faster
-    // there (3970 against 3818).
+    // `early` (set for calls with early loads or with the row kernels'
+    // pre-wait prefetch): the next kernel on the stream may be scheduled at
+    // once, so a following row kernel's prefetches and early loads overlap
+    // this reduction (GB300, 16384x512 bf16 backward, strict with the
+    // prefetch: 4042 -> 4194 GB/s; early loads without it 3988 -> 4179).
+    // Otherwise it is launched at this kernel's exit, which measured faster
+    // when the next kernel does nothing before its wait (3970 against 3818).
     if (early) pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -775,6 +805,16 @@ bool bwd_choose_plan(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int 
 bool bwd_choose(const BwdArgs& a, const DeviceInfo& d, const Knobs& k, int variant, Launch& l) {
     if (!bwd_choose_plan(a, d, k, variant, l)) return false;
     if (l.wait_limit_ns == 0) l.wait_limit_ns = k.wait_limit_ns > 0 ? k.wait_limit_ns : 1000000000LL;
+    // Pre-wait prefetch (rows of x and dy asked into L2 before the wait) for the
+    // warp and CTA row kernels: the caller's row count, or by default one row.
+    const bool takes = !l.bwd_tma && (l.bwd_warp || l.vecs_per_lane > 0);
+    const bool pdl_on = !(k.flags & RMSNORM_FLAG_NO_PDL);
+    if (takes && k.prewait_prefetch > 0)
+        l.prewait = k.prewait_prefetch;
+    else if (takes && k.prewait_prefetch == 0 && pdl_on)
+        l.prewait = 1;
+    else
+        l.prewait = 0;
     return true;
 }
 
@@ -924,7 +964,7 @@ cudaError_t bwd_run(const BwdArgs& a, const Launch& l, float* partial) {
     LaunchCfg c2(r, a.stream, l.pdl);
     return cudaLaunchKernelEx(&c2.cfg, narrow ? dw_reduce_narrow_kernel : dw_reduce_kernel,
                               static_cast<const float*>(partial), a.dw, G, a.N,
-                              static_cast<int>(l.early));
+                              static_cast<int>(l.early || l.prewait > 0));
 }
 
 }  // namespace rmsn

@@ -264,3 +264,70 @@ def test_bwd_tma_bounded_wait_reports_timeout_and_recovers():
     dx, dw = _run(x, w, dy, rstd, 0.0, dtype, variant="tma")
     assert B.rmsnorm_check_device_status(s) == 0
     _check(x, w, dy, rstd, dx, dw, 0.0, dtype, where="after timeout")
+
+
+@pytest.mark.parametrize("variant", ["warp", "cta"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("M,N", [(37, 512), (300, 1000), (64, 4096), (130, 520)])
+@pytest.mark.parametrize("PW", [1, 4, 15])
+def test_bwd_prewait_prefetch_parity(variant, dtype, M, N, PW):
+    # Rows of x and dy asked into L2 before the wait for the previous kernel: a
+    # hint only, so dx and dw must still match the oracle, for strict order and
+    # early loads, the full grid and a grid of three CTAs walking every row.
+    e = 4 if dtype == "fp32" else 8
+    if variant == "warp" and N // e > 128:
+        pytest.skip("the warp kernel takes rows of up to 128 vectors")
+    x, w, dy, rstd = _inputs(M, N, dtype, seed=M + N + PW, offset=1.0)
+    plan = B.rmsnorm_bwd_plan_info(M, N, DT[dtype], B.make_options(variant=variant, prewait_prefetch=PW))
+    assert plan["prewait_prefetch"] == PW
+    for max_ctas in (0, 3):
+        for early in (False, True):
+            dx, dw = _run(x, w, dy, rstd, 1.0, dtype, variant=variant, max_ctas=max_ctas,
+                          prewait_prefetch=PW, early_loads=early)
+            _check(x, w, dy, rstd, dx, dw, 1.0, dtype, where=f"{variant} {M}x{N} PW {PW}")
+
+
+def test_bwd_automatic_prewait_plan():
+    # The row kernels prefetch one row of x and dy per warp (CTA) before the
+    # wait by default; none without PDL or when the caller says -1; the staged
+    # and general kernels take none.
+    for N, dtype in ((512, "bf16"), (4096, "bf16"), (512, "fp32")):
+        assert B.rmsnorm_bwd_plan_info(16384, N, DT[dtype])["prewait_prefetch"] == 1
+        assert B.rmsnorm_bwd_plan_info(16384, N, DT[dtype], B.make_options(pdl=False))["prewait_prefetch"] == 0
+        assert B.rmsnorm_bwd_plan_info(16384, N, DT[dtype],
+                                       B.make_options(prewait_prefetch=-1))["prewait_prefetch"] == 0
+    assert B.rmsnorm_bwd_plan_info(16384, 512, DT["bf16"],
+                                   B.make_options(variant="tma"))["prewait_prefetch"] == 0
+    assert B.rmsnorm_bwd_plan_info(100, 70001, DT["fp32"])["prewait_prefetch"] == 0
+
+
+@pytest.mark.parametrize("variant,M,N,dtype", [("warp", 16384, 512, "bf16"), ("cta", 4000, 4096, "bf16"),
+                                               ("warp", 8000, 512, "fp32")])
+@pytest.mark.parametrize("PW", [0, 2])
+def test_bwd_prewait_chain_keeps_stream_order(variant, M, N, dtype, PW):
+    # Each call's dy is the previous call's dx, launched back to back under
+    # strict order with the pre-wait prefetch (and the reduction letting the
+    # next row kernel start early): the bits of the same calls with the device
+    # synchronised between them.
+    x, w, dy, rstd = _inputs(M, N, dtype, seed=N + M + PW, offset=0.0)
+    xd, wd, rd = W.to_torch(x, dtype).cuda(), W.to_torch(w, dtype).cuda(), torch.from_numpy(rstd).cuda()
+    o = B.make_options(variant=variant, prewait_prefetch=PW)
+    assert B.rmsnorm_bwd_plan_info(M, N, DT[dtype], o)["prewait_prefetch"] == (PW or 1)
+    nbytes = B.rmsnorm_bwd_workspace_size(M, N, DT[dtype], o)
+    ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device="cuda")
+    steps = 4
+    outs = {}
+    for sync in (False, True):
+        g = [W.to_torch(dy, dtype).cuda()] + [torch.empty_like(xd) for _ in range(steps)]
+        dws = [torch.empty(N, dtype=torch.float32, device="cuda") for _ in range(steps)]
+        for k in range(steps):
+            _bwd_call(xd, wd, rd, g[k], g[k + 1], dws[k], 0.0, dtype, ws, variant=variant,
+                      prewait_prefetch=PW)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        outs[sync] = ([W.from_torch(t) for t in g[1:]], [d.cpu().numpy() for d in dws])
+    for k in range(steps):
+        assert np.array_equal(outs[True][0][k], outs[False][0][k]), f"dx differs at step {k}"
+        assert np.array_equal(outs[True][1][k], outs[False][1][k]), f"dw differs at step {k}"
+    _check(x, w, dy, rstd, outs[False][0][0], outs[False][1][0], 0.0, dtype, where="first call")
