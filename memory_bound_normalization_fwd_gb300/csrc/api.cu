@@ -145,8 +145,8 @@ namespace {
 // limits are row bytes, so fp32 rows switch at half the column count):
 //   rows of up to 256 bytes in either mode, and rows of up to 1536 bytes
 //     under strict stream order without the pre-wait prefetch (PDL off, or
-//     batches under 4 MB): the warp-team kernel (with early loads or the
-//     pre-wait prefetch the TMA kernel is ahead from N = 512 bf16 up, the warp
+//     prewait_prefetch -1): the warp-team kernel (with early loads or the
+//     pre-wait prefetch the TMA kernel is ahead from N = 256 bf16 up, the warp
 //     kernel up to N = 128);
 //   rows of up to 16 KB (8192 columns): the TMA-staged kernel (ahead from
 //     N = 1000 to 8192);
@@ -197,12 +197,12 @@ int plan(const Args& a, const DeviceInfo& d, int variant, const Knobs& k, Launch
             const bool early = (k.flags & RMSNORM_FLAG_EARLY_LOADS) && pdl_on;
             const int64_t row_bytes = a.N * elem_bytes(a.dtype);
             // Under strict order the TMA kernel's pre-wait prefetch is ahead of
-            // the warp kernel from 512-byte rows up on batches of 4 MB or more
-            // (GB300, strict: 16384x512 bf16 6304 against 5592 GB/s, 16384x256
-            // bf16 4544 against 4284, 32768x192 fp32 6736 against 5992); without
-            // it (PDL off, or -1) the warp kernel stays ahead up to 1.5 KB rows.
-            const bool tma_prewait = pdl_on && k.prewait_prefetch >= 0 &&
-                                     a.M * row_bytes >= (int64_t{4} << 20);
+            // the warp kernel for rows over 256 bytes (GB300, strict: 16384x512
+            // bf16 6304 against 5592 GB/s, 2048x512 bf16 2011 against 1673,
+            // 16384x256 bf16 4544 against 4284, 32768x192 fp32 6736 against 5992);
+            // without it (PDL off, or -1) the warp kernel stays ahead up to
+            // 1.5 KB rows.
+            const bool tma_prewait = pdl_on && k.prewait_prefetch >= 0;
             // Rows of up to 16 vectors would leave much of a TMA team (16 threads
             // at least) idle: the warp kernel takes them in both launch modes
             // (early loads, GB300: N = 64 bf16 4.97 against 2.47 TB/s, N = 128

@@ -355,17 +355,18 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     // Pre-wait prefetch instead of loads before the wait: always under strict
     // stream order (unless the caller says -1 or PDL is off); with early loads
     // allowed, when the caller asks for it, and by default for bf16 and fp32
-    // rows of 512 B to 4 KB in batches of 4 MB or more (16 MB for 512-byte
+    // rows of 512 B to 4 KB in batches over 4 MB (over 16 MB for 512-byte
     // rows), where it measured faster than loading the first stages before the
     // wait (GB300, GB/s early loads -> pre-wait prefetch: 16384x512 bf16 5919
     // -> 6305, 32768x512 bf16 6423 -> 6859, 16384x1024 bf16 5752 -> 6869,
     // 65536x256 bf16 6429 -> 6888, 32768x1000 bf16 6596 -> 6783, 16384x512
-    // fp32 6414 -> 6967; 16384x256 bf16 4727 -> 4526, 16384x512 fp16 5661 ->
-    // 5476, 2 MB batches and 8-16 KB rows the other way round or even).
+    // fp32 6414 -> 6967, 4096x640 bf16 3295 -> 3432; 4096x512 bf16 3209 ->
+    // 2904, 16384x256 bf16 4727 -> 4526, 16384x512 fp16 5661 -> 5476, and 8-16
+    // KB rows the other way round or even).
     const bool pdl_on = !(k.flags & RMSNORM_FLAG_NO_PDL);
     const bool early_flag = (k.flags & RMSNORM_FLAG_EARLY_LOADS) && pdl_on;
     const bool early_prewait = a.dtype != kFP16 && row_bytes >= 512 && row_bytes < 4096 &&
-                               x_bytes >= (int64_t{row_bytes > 512 ? 4 : 16} << 20);
+                               x_bytes > (int64_t{row_bytes > 512 ? 4 : 16} << 20);
     const bool prewait_path = pdl_on && k.prewait_prefetch >= 0 &&
                               (k.prewait_prefetch > 0 || !early_flag || early_prewait);
     const bool early = early_flag && !prewait_path;  // first stages loaded before the wait

@@ -211,7 +211,8 @@ def test_prewait_prefetch_parity(variant, G, M, N, PW):
     (16384, 512, "bf16", "tma", 4, 1, 0, 1), (16384, 384, "bf16", "tma", 4, 1, 0, 1),
     (32768, 512, "bf16", "tma", 4, 2, 0, 2), (65536, 512, "bf16", "tma", 3, 3, 0, 3),
     (65536, 256, "bf16", "tma", 4, 2, 0, 2), (16384, 256, "bf16", "tma", 4, 1, 0, 0),
-    (65536, 128, "bf16", "warp", 3, 3, 0, 0), (2048, 512, "bf16", "warp", 6, 0, 0, 0),
+    (65536, 128, "bf16", "warp", 3, 3, 0, 0), (2048, 512, "bf16", "tma", 4, 1, 0, 0),
+    (4096, 512, "bf16", "tma", 4, 1, 0, 0), (4096, 640, "bf16", "tma", 4, 1, 0, 1),
     (16384, 256, "fp32", "tma", 4, 1, 0, 1), (16384, 512, "fp32", "tma", 4, 2, 0, 2),
     (16384, 512, "fp16", "tma", 2, 2, 0, 0), (32768, 1000, "bf16", "tma", 3, 3, 0, 3),
     (16384, 8192, "bf16", "tma", 2, 3, 0, 0)])
