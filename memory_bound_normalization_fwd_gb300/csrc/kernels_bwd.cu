@@ -77,6 +77,19 @@ __device__ __forceinline__ float bwd_dot_vec(const uint4& xv, const uint4& gv, c
     return a + b;
 }
 
+// dy * x for the two bf16 elements of each of two words, exact in fp32 (a
+// product of two bf16 values fits in fp32's significand), by mixed-precision
+// FMAs (fma.rn.f32.bf16 with a zero addend): no widening instructions.
+__device__ __forceinline__ uint64_t bf16_prod2(uint32_t g, uint32_t x, float zero) {
+    uint64_t d;
+    asm("{\n .reg .b16 gl, gh, xl, xh;\n .reg .f32 tl, th;\n"
+        " mov.b32 {gl, gh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+        " fma.rn.f32.bf16 tl, gl, xl, %3;\n fma.rn.f32.bf16 th, gh, xh, %3;\n"
+        " mov.b64 %0, {tl, th};\n}"
+        : "=l"(d) : "r"(g), "r"(x), "f"(zero));
+    return d;
+}
+
 // Pass 2: dx = r * (dy * s - x * k) for the vector (k = r^2 c / N; the
 // difference taken by one fused multiply-add), rounded once to the dtype, and
 // the dw contribution (dy * x) * r added into acc.
@@ -97,6 +110,57 @@ __device__ __forceinline__ uint4 bwd_dx_vec(const uint4& xv, const uint4& gv, co
         f2_unpack(f2_fma(f2_mul(g2, x2), rr, f2_pack(acc[e], acc[e + 1])), acc[e], acc[e + 1]);
     }
     return pack_vec<DT>(o);
+}
+
+// The two per-vector passes as the row kernels run them. Pass 1 returns cs plus
+// the vector's part of c = sum dy s x; pass 2 returns dx. The dw contribution
+// (dy x) r goes into acc in pass 1 for bf16 (where dy x is taken exactly, once,
+// by mixed-precision FMAs and serves both sums: c as sum (dy x) s) and in pass
+// 2 for the other dtypes (c as sum (dy s) x). GB300: fewer instructions per
+// element for bf16, where the row kernels are bound by issue.
+template <int DT>
+__device__ __forceinline__ float bwd_pass1(const uint4& xv, const uint4& gv, const float4* sw, int c,
+                                           float r, float cs, float* acc) {
+    if constexpr (DT == kBF16) {
+        float sv[8];
+        weights_from_smem<DT>(sw, c, sv);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+        const uint64_t rr = f2_pack(r, r);
+        uint64_t a2 = f2_pack(cs, 0.f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint64_t t2 = bf16_prod2(gw[q], xw[q], 0.f);
+            a2 = f2_fma(t2, f2_pack(sv[2 * q], sv[2 * q + 1]), a2);
+            f2_unpack(f2_fma(t2, rr, f2_pack(acc[2 * q], acc[2 * q + 1])), acc[2 * q], acc[2 * q + 1]);
+        }
+        float a, b;
+        f2_unpack(a2, a, b);
+        return a + b;
+    } else {
+        return bwd_dot_vec<DT>(xv, gv, sw, c, cs);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 bwd_pass2(const uint4& xv, const uint4& gv, const float4* sw, int c,
+                                           float r, float k, float* acc) {
+    if constexpr (DT == kBF16) {
+        float xf[8], gf[8], sv[8], o[8];
+        unpack_vec<DT>(xv, xf);
+        unpack_vec<DT>(gv, gf);
+        weights_from_smem<DT>(sw, c, sv);
+        const uint64_t rr = f2_pack(r, r), nk = f2_pack(-k, -k);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const uint64_t g2 = f2_pack(gf[e], gf[e + 1]), x2 = f2_pack(xf[e], xf[e + 1]);
+            const uint64_t d = f2_fma(x2, nk, f2_mul(g2, f2_pack(sv[e], sv[e + 1])));
+            f2_unpack(f2_mul(d, rr), o[e], o[e + 1]);
+        }
+        return pack_vec<DT>(o);
+    } else {
+        return bwd_dx_vec<DT>(xv, gv, sw, c, r, k, acc);
+    }
 }
 
 // (Loading the next row ahead, as the warp kernel does, measured slower here:
@@ -171,7 +235,7 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = v * THREADS + tid;
-            if (c < nvec) cs = bwd_dot_vec<DT>(xv[v], gv[v], sw, c, cs);
+            if (c < nvec) cs = bwd_pass1<DT>(xv[v], gv[v], sw, c, r, cs, acc[v]);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
@@ -184,7 +248,7 @@ bwd_rows_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = v * THREADS + tid;
-            if (c < nvec) st_stream(dx + row * nvec + c, bwd_dx_vec<DT>(xv[v], gv[v], sw, c, r, k, acc[v]));
+            if (c < nvec) st_stream(dx + row * nvec + c, bwd_pass2<DT>(xv[v], gv[v], sw, c, r, k, acc[v]));
         }
         parity ^= 1;
         load_x(row + gridDim.x);
@@ -286,7 +350,7 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = v * 32 + lane;
-            if (c < nvec) cs = bwd_dot_vec<DT>(xv[v], gv[v], sw, c, cs);
+            if (c < nvec) cs = bwd_pass1<DT>(xv[v], gv[v], sw, c, r, cs, acc[v]);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
@@ -294,7 +358,7 @@ bwd_warp_kernel(const uint4* x, const uint4* __restrict__ w, const float* __rest
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const int c = v * 32 + lane;
-            if (c < nvec) st_stream(dx + row * nvec + c, bwd_dx_vec<DT>(xv[v], gv[v], sw, c, r, k, acc[v]));
+            if (c < nvec) st_stream(dx + row * nvec + c, bwd_pass2<DT>(xv[v], gv[v], sw, c, r, k, acc[v]));
         }
 #pragma unroll
         for (int v = 0; v < V; ++v) xv[v] = xn[v], gv[v] = gn[v];
