@@ -780,11 +780,18 @@ def launch_only(args, wl) -> dict:
 def ablation_configs(wl):
     """Kernel variants and knobs to compare on one workload (the pages' knobs:
     TMA staging on or off, prefetch depth, rows per warp, registers and
-    occupancy; plus launch overlap and row order)."""
+    occupancy; plus launch overlap, the pre-wait prefetch and row order)."""
     eb = 4 if wl.dtype == "fp32" else 2
     nvec, row = wl.N * eb // 16, eb * wl.N
     cfgs = [dict(), dict(early_loads=True), dict(early_weights=True), dict(pdl=False),
             dict(blocked=True)]
+    # Pre-wait L2 prefetch off (the plans the planner takes without it), and
+    # its depth per kernel.
+    cfgs += [dict(prewait_prefetch=-1), dict(early_loads=True, prewait_prefetch=-1)]
+    for PW in (1, 2, 3):
+        cfgs.append(dict(variant="tma", prewait_prefetch=PW))
+        if nvec <= 128:
+            cfgs.append(dict(variant="warp", prewait_prefetch=PW))
     if nvec <= 128:
         for G in (8, 16, 32):
             for D in (1, 2, 4):

@@ -160,9 +160,10 @@ typedef struct rmsnorm_options {
                                 prefetch.L2, no effect on results). WARP: each team asks
                                 for its rows this many passes past the ones held in
                                 registers to be brought into L2; TMA: each CTA, for this
-                                many chunks past its ring's stages (packed rows only).
-                                Ignored by the other variants and by rmsnorm_bwd.
-                                1..15; 0 = planner's choice; -1 = none */
+                                many chunks past its ring's stages (packed rows; not in
+                                the 512-thread plans nor fp16 plans of 128-thread teams
+                                and up, where it reads 0). Ignored by the other variants
+                                and by rmsnorm_bwd. 1..15; 0 = planner's choice; -1 = none */
     int32_t prewait_prefetch; /* WARP and TMA: before it waits for the previous kernel on
                                 the stream, the kernel asks for its first rows to be brought
                                 into L2 (cp.async.bulk.prefetch.L2, a hint: x is still read

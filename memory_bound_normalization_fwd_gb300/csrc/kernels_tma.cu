@@ -55,6 +55,17 @@ __device__ __forceinline__ void team_barrier(int id, int threads) {
 // memory and leaves with one bulk copy per stage (cp.async.bulk shared ->
 // global, issued by the thread that issues the loads) instead of per-thread
 // 16-byte stores; the stage is reloaded only after that copy has read it.
+// Whether an instance compiles the ring's L2 prefetch of chunks ahead (the
+// l2_prefetch option). The 512-thread instances and the fp16 ones with teams
+// of 128 threads or more leave it out: its code in their refill path cost the
+// consumer loop speed (GB300, early loads: 131072x4096 fp16 6754 -> 7086 GB/s
+// without it, 65536x4096 fp32 6426 -> 6861, 16384x8192 bf16 6403 -> 6523),
+// while the other instances measured as fast or faster with it in the build
+// (16384x2048 bf16 5541 against 5260, 65536x2048 fp32 6746 against 6293).
+__host__ __device__ constexpr bool tma_ring_prefetch(int dt, int threads, int team) {
+    return !(threads == 512 || (dt == kFP16 && team >= 128));
+}
+
 // MINB: resident CTAs per SM the register budget must allow; 0 leaves the
 // register count to the compiler, 4 holds the lean 256-thread instances to 64
 // registers (four CTAs per SM, no spills for bf16).
@@ -129,8 +140,10 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
             // L2 prefetch of the chunk P issues ahead (chunks below `stages` are
             // the ring's first loads, and chunks below PW were asked for before
             // the wait, so each later chunk is asked for once).
-            const int64_t kp = k + mode_prefetch(mode);
-            if (kp > k && kp >= pf_from && kp < nchunks) prefetch_chunk(kp);
+            if constexpr (tma_ring_prefetch(DT, THREADS, TEAM)) {
+                const int64_t kp = k + mode_prefetch(mode);
+                if (kp > k && kp >= pf_from && kp < nchunks) prefetch_chunk(kp);
+            }
         } else {       // strided rows: one copy per row, all counted on the same barrier
             for (int64_t q = 0; q < rows; ++q)
                 bulk_g2s(dst + static_cast<uint32_t>(q) * row_bytes, x + (r0 + q) * ldx, row_bytes,
@@ -426,10 +439,27 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     l.smem = static_cast<int>(smem);
     l.ctas_per_sm = occupancy(l.kernel, threads, l.smem);
     if (l.ctas_per_sm < 1) return false;
+    // Three CTAs per SM for 16-bit rows under 4 KB outside the lean plans
+    // (batches over 48 MB, or early copies): where registers alone would let a
+    // fourth in, the dynamic shared memory is padded so that it does not
+    // (GB300: 32768x1000 bf16 6783 at three against 6334 at four; 65536x512
+    // bf16 6798 against 6589). A grid cap would not do: the CTAs would then
+    // fill some SMs four deep and leave others idle (5593).
+    if (!lean && elem_bytes(a.dtype) == 2 && short_rows && threads == 256) {
+        int padded = l.smem;
+        while (l.ctas_per_sm > 3 && padded + 4096 <= max_dyn) {
+            padded += 4096;
+            l.ctas_per_sm = occupancy(l.kernel, threads, padded);
+        }
+        l.smem = padded;
+    }
     l.work_items = (a.M + R - 1) / R;
     l.grid = persistent_grid(l.work_items, 1, d.sm_count, l.ctas_per_sm, k.max_ctas);
     l.wait_limit_ns = k.wait_limit_ns > 0 ? k.wait_limit_ns : 1000000000LL;
-    l.prefetch = (contig && k.l2_prefetch > 0) ? k.l2_prefetch : 0;
+    // The ring's L2 prefetch: only on the caller's request (it measured no
+    // faster by default), for packed rows, in the instances that compile it.
+    l.prefetch = (contig && k.l2_prefetch > 0 && tma_ring_prefetch(a.dtype, threads, team))
+                     ? k.l2_prefetch : 0;
     // Pre-wait prefetch: the caller's chunk count, or by default about half the
     // chunks each CTA walks, one to three (GB300, strict, GB/s without -> with:
     // 32768x1000 bf16 6154 -> 6763 at three chunks, 16384x512 fp32 5687 -> 6946

@@ -81,15 +81,19 @@ def test_full_size_automatic_launch(wl, early):
     _check(x, w, wl.eps, wl.offset, rows=rows, runs=2 if early else 1, early_loads=early)
 
 
-@pytest.mark.parametrize("N,variant", [(256, "warp"), (384, "warp"), (512, "tma"),
-                                       (4096, "tma"), (8192, "cta"), (16384, "cta"),
-                                       (32768, "cluster")])
-def test_planner_switches_at_row_bytes(N, variant):
+@pytest.mark.parametrize("N,variant,without_prewait", [
+    (64, "warp", "warp"), (256, "tma", "warp"), (384, "tma", "warp"), (512, "tma", "tma"),
+    (4096, "tma", "tma"), (8192, "cta", "cta"), (16384, "cta", "cta"),
+    (32768, "cluster", "cluster")])
+def test_planner_switches_at_row_bytes(N, variant, without_prewait):
     # The planner's limits are row bytes: an fp32 row switches kernels at half
-    # the column count of a bf16 row.
+    # the column count of a bf16 row. Under strict order rows over 256 bytes
+    # take the TMA kernel with the pre-wait prefetch; without it (-1) the warp
+    # kernel keeps rows of up to 1.5 KB.
     wl = W.custom(64, N, "fp32", seed=N)
     x, w = W.generate(wl)
     _check(x, w, wl.eps, wl.offset, expect_variant=variant)
+    _check(x, w, wl.eps, wl.offset, expect_variant=without_prewait, prewait_prefetch=-1)
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 5, 7, 9, 31, 127, 1023, 1025, 4097])
