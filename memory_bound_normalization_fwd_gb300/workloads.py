@@ -74,7 +74,8 @@ BENCH_WORKLOAD = "rmsnorm_16384x512_bf16"
 
 # fp32 activations (x, w, y in fp32) at the benchmark shapes: not among the
 # named workloads above, which are the method's own; measured and tested as a
-# boundary variant of the same forward.
+# boundary variant of the same forward. Also one smaller size of a named
+# workload for profiler captures.
 EXTRA_WORKLOADS = {
     w.name: w
     for w in [
@@ -84,12 +85,15 @@ EXTRA_WORKLOADS = {
         Workload("rmsnorm_16384x8192_fp32_heavytail", 16384, 8192, dtype="fp32", outlier_p=0.01,
                  outlier_std=100.0, eps=1e-5),
         Workload("rmsnorm_65536x4096_fp32", 65536, 4096, dtype="fp32", x_std=64.0),
+        # The 131072x4096 fp16 workload's kernel and plan at an eighth of its
+        # rows (x 128 MB, still above L2), for profiler captures of one launch.
+        Workload("rmsnorm_16384x4096_fp16", 16384, 4096, dtype="fp16", x_std=64.0),
     ]
 }
 
 
 def get(name: str) -> Workload:
-    """A named workload, or one of the fp32 ones."""
+    """A named workload, or one of the extra ones (fp32, profiling size)."""
     if name in WORKLOADS:
         return WORKLOADS[name]
     return EXTRA_WORKLOADS[name]
