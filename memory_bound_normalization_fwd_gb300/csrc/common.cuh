@@ -158,6 +158,30 @@ __device__ __forceinline__ float sumsq_vec(const uint4& v, float acc) {
     }
 }
 
+// The same sum for fp16 by mixed-precision FMAs (fma.rn.f32.f16, sm_100 and
+// later), which widen each element exactly: the bits of widening first and
+// calling fmaf, without keeping the widened values live until the scale step
+// (used by the TMA kernel's short-row instances, where that live range cost
+// a resident CTA per SM).
+__device__ __forceinline__ float sumsq2_f16(uint32_t u, float acc) {
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n"
+        " fma.rn.f32.f16 %0, lo, lo, %0;\n fma.rn.f32.f16 %0, hi, hi, %0;\n}"
+        : "+f"(acc) : "r"(u));
+    return acc;
+}
+
+template <int DT>
+__device__ __forceinline__ float sumsq_vec_packed(const uint4& v, float acc) {
+    if constexpr (DT == kFP16) {
+        acc = sumsq2_f16(v.x, acc);
+        acc = sumsq2_f16(v.y, acc);
+        acc = sumsq2_f16(v.z, acc);
+        return sumsq2_f16(v.w, acc);
+    } else {
+        return sumsq_vec<DT>(v, acc);
+    }
+}
+
 template <int DT>
 __device__ __forceinline__ uint4 scale_vec(const uint4& v, float r, const float* s) {
     if constexpr (DT == kFP32) {

@@ -206,7 +206,10 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
                 const int c = v * TEAM + t;
                 xv[v] = make_uint4(0u, 0u, 0u, 0u);
                 if (act && c < nvec) xv[v] = sx[rr * nvec + c];
-                ss = sumsq_vec<DT>(xv[v], ss);
+                if constexpr (DT == kFP16 && TEAM <= 64)
+                    ss = sumsq_vec_packed<DT>(xv[v], ss);
+                else
+                    ss = sumsq_vec<DT>(xv[v], ss);
             }
 #pragma unroll
             for (int off = kLanes / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -305,8 +308,9 @@ Fn pick(int team, int V, bool contig, bool bulk_store) {
 }
 
 // Lean instances (four 256-thread CTAs per SM) for packed bf16 rows of 512
-// bytes to 4 KB; nullptr for other shapes. (The fp16 body needs about 107
-// registers at these shapes, so it would spill at 64.)
+// bytes to 4 KB; nullptr for other shapes. (fp16 held to 64 registers spills
+// 36-40 bytes and ran slower: 16384x512 fp16 strict 5325 against 6018 at three
+// CTAs per SM.)
 template <int DT>
 Fn pick_lean(int team, int V) {
     if (team == 16 && V == 2) return tma_rows_kernel<DT, 256, 16, 2, true, false, 4>;
@@ -367,18 +371,18 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     const int64_t x_bytes = a.M * row_bytes;
     // Pre-wait prefetch instead of loads before the wait: always under strict
     // stream order (unless the caller says -1 or PDL is off); with early loads
-    // allowed, when the caller asks for it, and by default for bf16 and fp32
-    // rows of 512 B to 4 KB in batches over 4 MB (over 16 MB for 512-byte
-    // rows), where it measured faster than loading the first stages before the
-    // wait (GB300, GB/s early loads -> pre-wait prefetch: 16384x512 bf16 5919
-    // -> 6305, 32768x512 bf16 6423 -> 6859, 16384x1024 bf16 5752 -> 6869,
-    // 65536x256 bf16 6429 -> 6888, 32768x1000 bf16 6596 -> 6783, 16384x512
-    // fp32 6414 -> 6967, 4096x640 bf16 3295 -> 3432; 4096x512 bf16 3209 ->
-    // 2904, 16384x256 bf16 4727 -> 4526, 16384x512 fp16 5661 -> 5476, and 8-16
-    // KB rows the other way round or even).
+    // allowed, when the caller asks for it, and by default for rows of 512 B to
+    // 4 KB in batches over 4 MB (over 16 MB for 512-byte rows), where it
+    // measured faster than loading the first stages before the wait (GB300,
+    // GB/s early loads -> pre-wait prefetch: 16384x512 bf16 5919 -> 6305,
+    // 32768x512 bf16 6423 -> 6859, 16384x1024 bf16 5752 -> 6869, 65536x256 bf16
+    // 6429 -> 6888, 32768x1000 bf16 6596 -> 6783, 16384x512 fp32 6414 -> 6967,
+    // 4096x640 bf16 3295 -> 3432, 16384x1024 fp16 5994 -> 6679, 65536x512 fp16
+    // 6659 -> 6798; 4096x512 bf16 3209 -> 2904, 16384x256 bf16 4727 -> 4526,
+    // and 8-16 KB rows the other way round or even).
     const bool pdl_on = !(k.flags & RMSNORM_FLAG_NO_PDL);
     const bool early_flag = (k.flags & RMSNORM_FLAG_EARLY_LOADS) && pdl_on;
-    const bool early_prewait = a.dtype != kFP16 && row_bytes >= 512 && row_bytes < 4096 &&
+    const bool early_prewait = row_bytes >= 512 && row_bytes < 4096 &&
                                x_bytes > (int64_t{row_bytes > 512 ? 4 : 16} << 20);
     const bool prewait_path = pdl_on && k.prewait_prefetch >= 0 &&
                               (k.prewait_prefetch > 0 || !early_flag || early_prewait);

@@ -214,7 +214,7 @@ def test_prewait_prefetch_parity(variant, G, M, N, PW):
     (65536, 128, "bf16", "warp", 3, 3, 0, 0), (2048, 512, "bf16", "tma", 4, 1, 0, 0),
     (4096, 512, "bf16", "tma", 4, 1, 0, 0), (4096, 640, "bf16", "tma", 4, 1, 0, 1),
     (16384, 256, "fp32", "tma", 4, 1, 0, 1), (16384, 512, "fp32", "tma", 4, 2, 0, 2),
-    (16384, 512, "fp16", "tma", 2, 2, 0, 0), (32768, 1000, "bf16", "tma", 3, 3, 0, 3),
+    (16384, 512, "fp16", "tma", 3, 2, 0, 2), (32768, 1000, "bf16", "tma", 3, 3, 0, 3),
     (16384, 8192, "bf16", "tma", 2, 3, 0, 0)])
 def test_automatic_prewait_plan(M, N, dtype, variant, per_sm, pw, P, early_pw):
     # The planner's pre-wait prefetch under strict order: the kernel, its CTAs
