@@ -443,13 +443,18 @@ bool tma_choose(const Args& a, const DeviceInfo& d, const Knobs& k, Launch& l) {
     l.smem = static_cast<int>(smem);
     l.ctas_per_sm = occupancy(l.kernel, threads, l.smem);
     if (l.ctas_per_sm < 1) return false;
-    // Three CTAs per SM for 16-bit rows under 4 KB outside the lean plans
-    // (batches over 48 MB, or early copies): where registers alone would let a
-    // fourth in, the dynamic shared memory is padded so that it does not
-    // (GB300: 32768x1000 bf16 6783 at three against 6334 at four; 65536x512
-    // bf16 6798 against 6589). A grid cap would not do: the CTAs would then
-    // fill some SMs four deep and leave others idle (5593).
-    if (!lean && elem_bytes(a.dtype) == 2 && short_rows && threads == 256) {
+    // Three CTAs per SM for 16-bit rows under 4 KB in batches of 16 MB or more
+    // outside the lean plans (batches over 48 MB, or early copies): where
+    // registers alone would let a fourth in, the dynamic shared memory is
+    // padded so that it does not (GB300, GB/s at three against four:
+    // 131072x256 bf16 6805 / 6734, 131072x256 fp16 6803 / 6632, 32768x256
+    // bf16 early loads 5661 / 5357; three CTAs also won where registers set
+    // them: 32768x1000 bf16 6783 against 6334, 65536x512 6798 against 6589).
+    // Smaller batches keep four (16384x256 bf16 early loads 4977 against
+    // 4649). A grid cap would not do: the CTAs would then fill some SMs four
+    // deep and leave others idle (5593).
+    if (!lean && elem_bytes(a.dtype) == 2 && short_rows && threads == 256 &&
+        x_bytes >= (int64_t{16} << 20)) {
         int padded = l.smem;
         while (l.ctas_per_sm > 3 && padded + 4096 <= max_dyn) {
             padded += 4096;

@@ -231,6 +231,25 @@ def test_automatic_prewait_plan(M, N, dtype, variant, per_sm, pw, P, early_pw):
     assert _plan(M, N, dtype, early_loads=True, prewait_prefetch=-1)["prewait_prefetch"] == 0
 
 
+def test_padded_shared_memory_holds_three_ctas_per_sm():
+    # 512-byte bf16 rows in a 64 MB batch: the TMA instance's registers would
+    # admit four CTAs per SM, so the planner pads the dynamic shared memory to
+    # hold three; the kernel ignores the padding and every row must match.
+    M, N = 131072, 256
+    wl = W.custom(M, N, "bf16", seed=5)
+    x, w = W.generate(wl)
+    case = DeviceCase(x, w, "bf16")
+    plan = _plan(M, N, "bf16", case)
+    assert plan["variant"] == "tma" and plan["ctas_per_sm"] == 3
+    assert plan["smem_bytes"] > 128 + 128 + plan["stages"] * plan["rows_per_stage"] * N * 2
+    for early in (False, True):
+        assert case.run(wl.eps, wl.offset, early_loads=early) == 0, B.rmsnorm_last_error()
+        y, r = case.results()
+        case.check_guards()
+        yo, ro = oracle_threaded(x, w, wl.eps, wl.offset, "bf16")
+        compare_blocked(y, r, yo, ro, "bf16", where=f"padded {M}x{N} early={early}")
+
+
 @pytest.mark.parametrize("variant,N", [("warp", 512), ("warp", 256), ("tma", 1000), ("tma", 2048)])
 @pytest.mark.parametrize("pw", [0, 1, 4])
 def test_prewait_chain_keeps_stream_order(variant, N, pw):
