@@ -175,7 +175,8 @@ typedef struct rmsnorm_options {
                                 replaces the loads before the wait with it; -1 keeps them.
                                 rmsnorm_bwd: the warp and CTA row kernels prefetch this many
                                 of their first rows of x and dy (default 1). Ignored by the
-                                other variants; without PDL the planner never picks it.
+                                other variants. With RMSNORM_FLAG_NO_PDL the planner never
+                                picks it and the forward TMA kernel ignores a count.
                                 1..15; 0 = planner's choice; -1 = none */
 } rmsnorm_options_t;
 
