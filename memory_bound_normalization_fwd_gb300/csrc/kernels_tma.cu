@@ -66,6 +66,12 @@ __host__ __device__ constexpr bool tma_ring_prefetch(int dt, int threads, int te
     return !(threads == 512 || (dt == kFP16 && team >= 128));
 }
 
+// Whether an instance, under early loads, computes its first rows before the
+// PDL wait that guards its stores (measured per instance, see the kernel).
+__host__ __device__ constexpr bool tma_late_wait(int dt, int threads, int team, int minb) {
+    return threads == 512 && dt != kFP32 && team == 512 && minb == 0;
+}
+
 // MINB: resident CTAs per SM the register budget must allow; 0 leaves the
 // register count to the compiler, 4 holds the lean 256-thread instances to 64
 // registers (four CTAs per SM, no spills for bf16).
@@ -178,7 +184,15 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
     for (int v = 0; v < V; ++v) weights_vec<DT>(wv[v], offset, s[v]);
     __syncthreads();  // the barriers' initialisation is visible to every thread
     pdl_launch_dependents();
-    if (early) pdl_wait();
+    // With early loads the wait guards only the stores. The 16-bit 512-thread
+    // instances compute their first rows before it (GB300, early loads, GB/s:
+    // 16384x8192 bf16 6521 -> 6701, 32768x8192 bf16 6517 -> 6635; 4096x8192
+    // 6690 -> 6616); the others wait here, where the later wait measured
+    // slower or even (16384x2048 bf16 5535 against 5412, 65536x4096 fp32 6859
+    // against 6790, 16384x512 fp16 5989 against 5936; small batches within
+    // the run-to-run spread).
+    bool waited = !early || !tma_late_wait(DT, THREADS, TEAM, MINB);
+    if (early && !tma_late_wait(DT, THREADS, TEAM, MINB)) pdl_wait();
 
     int pp = 0;
     int64_t k = 0;
@@ -220,6 +234,12 @@ tma_rows_kernel(const uint4* x, const uint4* __restrict__ w, uint4* y, float* __
 #pragma unroll
                 for (int q = 0; q < kTeamWarps; ++q) ss += part[pp][team][q];
                 pp ^= 1;
+            }
+            if constexpr (tma_late_wait(DT, THREADS, TEAM, MINB)) {
+                if (!waited) {  // CTA-uniform: the first pass of the first chunk
+                    pdl_wait();
+                    waited = true;
+                }
             }
             if (act) {
                 const int64_t row = r0 + rr;
