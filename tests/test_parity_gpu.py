@@ -190,6 +190,12 @@ def test_prewait_prefetch_parity(variant, G, M, N, PW):
                        early_weights=early_w, expect_variant=variant)
     _run_and_check(x, w, "bf16", wl.eps, wl.offset, inplace=True, variant=variant,
                    lanes_per_row=G, prewait_prefetch=PW, max_ctas=2, expect_variant=variant)
+    # With early loads allowed, a positive count replaces the loads before the
+    # wait (x is then read only after it).
+    _run_and_check(x, w, "bf16", wl.eps, wl.offset, variant=variant, lanes_per_row=G,
+                   prewait_prefetch=PW, early_loads=True, expect_variant=variant)
+    assert _plan(M, N, "bf16", variant=variant, lanes_per_row=G, prewait_prefetch=PW,
+                 early_loads=True)["prewait_prefetch"] == PW
     plan = _plan(M, N, "bf16", variant=variant, lanes_per_row=G, prewait_prefetch=PW)
     assert plan["prewait_prefetch"] == PW
     ldx = ldy = N + 24
