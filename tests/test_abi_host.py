@@ -247,3 +247,30 @@ def test_plain_c_and_cpp_consumers_compile_link_and_call(lib, tmp_path, compiler
     assert version == B.rmsnorm_version()
     assert rc == rc_ex == -1 and strerr == B.rmsnorm_strerror(-1) and detail
     assert rc_ws == 0 and nbytes == B.rmsnorm_fwd_host_workspace_size(1000, 512, B.BF16, 0)
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    # The binding's ctypes structures mirror rmsnorm_options_t and
+    # rmsnorm_plan_t: every field at the header's offset, same total size.
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not installed")
+    fields = {"rmsnorm_options_t": B.Options, "rmsnorm_plan_t": B.Plan}
+    lines = []
+    for cname, cls in fields.items():
+        lines.append(f'    printf("{cname} size %zu\\n", sizeof({cname}));')
+        for name, _ in cls._fields_:
+            lines.append(f'    printf("{cname} {name} %zu\\n", offsetof({cname}, {name}));')
+    src = tmp_path / "layout.c"
+    src.write_text('#include "rmsnorm.h"\n#include <stddef.h>\n#include <stdio.h>\n'
+                   "int main(void) {\n" + "\n".join(lines) + "\n    return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for cname, cls in fields.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for name, _ in cls._fields_:
+            assert got[(cname, name)] == getattr(cls, name).offset, (cname, name)
