@@ -624,7 +624,10 @@ def bench_ours(args, wl, rank, world, local_rank):
                    "launch": main.launch,
                    "launch_order": ("early loads (RMSNORM_FLAG_EARLY_LOADS): steps are independent "
                                     "batches, so step k+1 may start loading x while step k "
-                                    "finishes; all stores stay in stream order") if early
+                                    "finishes; all stores stay in stream order"
+                                    + ("; this plan uses the pre-wait L2 prefetch instead (x read "
+                                       "after the wait, its first chunks asked into L2 before it)"
+                                       if plan.get("prewait_prefetch") else "")) if early
                                    else "strict stream order",
                    "plan": plan},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
